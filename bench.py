@@ -1,0 +1,280 @@
+"""CSA2 decode benchmark: query-layers/s of the 20-layer decoder step on one GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m]
+               [--impl gb300|reference]
+
+A step = one decode token for B independent sequences of N visible entries: the new
+token's entry is compressed into the cache (m = 1), then the decoder schedule
+[Full, Reuse x3] + 4 x [Reindex, Reuse x3] runs, each layer its own index step and
+sparse attention.  One query-layer = one query through one attention layer including
+its index step.  Under torchrun every rank runs its own batch of sequences (weak
+scaling, no collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp4_compressed_sparse_02_gb300 import build as libbuild  # noqa: E402
+from fp4_compressed_sparse_02_gb300 import synth, workload  # noqa: E402
+
+METRIC = "CSA2 decode query-layers/s at 128K–1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
+WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.proc = None
+        self.f = tempfile.TemporaryFile(mode="w+")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.dev)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.seek(0)
+        rows = [ln.split(",") for ln in self.f.read().strip().splitlines() if ln.strip()]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for nm, v in zip(names, r[4:8]):
+                    if v.strip() == "Active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(N, queries, config_name):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "oracle.timing", "--N", str(N), "--queries", str(queries),
+                        "--config", config_name], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr else "failed"}
+    j = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": j["value"], "unit": "query-layers/s", "cores": 1, "kind": "oracle",
+            "sample": f"{queries} query-steps (1 query x 20 layers each, own sequence of N={N} entries), "
+                      f"{j['seconds']:.1f} s single-threaded float64 numpy"}
+
+
+def run_reference(a):
+    """The CPU oracle timed as the reference arm: each step is one query-step (append +
+    20 decoder layers) of the same workload on the host."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cfg = WORKLOADS[a.workload]
+    name = "DEC128K" if a.workload == "decode128k" else "DEC1M"
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    sys.path.insert(0, ROOT)
+    os.environ.update(env)
+    from oracle import timing
+    import numpy as np
+    r = np.random.default_rng(0)
+    xs = [timing.make_query(r, cfg["N"], dict(cfg)) for _ in range(a.warmup + a.steps)]
+    for x in xs[:a.warmup]:
+        timing.run_query(x, cfg["N"], dict(cfg))
+    t0 = time.perf_counter()
+    for x in xs[a.warmup:]:
+        timing.run_query(x, cfg["N"], dict(cfg))
+    dt = time.perf_counter() - t0
+    val = a.steps * 20 / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "query-layers/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000 * dt / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{a.workload}: CPU oracle, 1 query (own sequence of N={cfg['N']}) per step"},
+            "cpu_baseline": {"value": val, "unit": "query-layers/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{a.steps} query-steps of 20 layers, N={cfg['N']}"},
+            "e2e": {"value": val, "unit": "query-layers/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-queries", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    a.warmup = max(a.warmup, 3)
+    if a.impl == "reference":
+        run_reference(a)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    libbuild.build()
+    cfg = WORKLOADS[a.workload]
+    step, info = workload.build_decode(cfg, seed=1000 + rank, device=f"cuda:{local}")
+    nbytes = workload.algorithmic_bytes(info)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    # eager warm-up sizes the workspace and sets kernel attributes before capture
+    with torch.cuda.stream(stream):
+        step.run()
+    torch.cuda.synchronize()
+    graphs = []
+    parts = [lambda: step.run_append(), lambda: step.run_layer(0),
+             lambda: [step.run_layer(i) for i in range(1, len(step.layers))]]
+    for fn in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    ga, gf, gr = graphs
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            ga.replay(); gf.replay(); gr.replay()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for i in range(a.steps):
+            ga.replay()
+            ev[i][0].record(stream)
+            gf.replay()
+            ev[i][1].record(stream)
+            gr.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    full_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    if world > 1:
+        t = torch.tensor([ms_total], device=f"cuda:{local}")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = t.item()
+    ms_step = ms_total / a.steps
+    B = info["B"]
+    ql = B * info["layers"] * world
+    value = ql * a.steps / (ms_total / 1000.0)
+
+    # end to end: per step, copy the step's inputs from pinned host memory, run the step,
+    # read the last layer's output back.
+    host_in = []
+    for L in step.layers:
+        for key in ("q", "q_idx", "w"):
+            if key in L:
+                host_in.append((L[key], torch.empty(L[key].shape, dtype=L[key].dtype, pin_memory=True).copy_(L[key])))
+    host_in.append((step.append["H"], torch.empty(step.append["H"].shape, dtype=torch.bfloat16,
+                                                   pin_memory=True).copy_(step.append["H"])))
+    host_out = torch.empty(step.out[-1].shape, dtype=step.out[-1].dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(10, a.steps // 10)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for dev_t, host_t in host_in:
+                dev_t.copy_(host_t, non_blocking=True)
+            ga.replay(); gf.replay(); gr.replay()
+            host_out.copy_(step.out[-1], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=f"cuda:{local}")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = t.item()
+    e2e_val = ql / (e2e_ms / 1000.0)
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        full_bytes = B * nbytes["per_query"]["full"]
+        achieved = full_bytes / (full_ms / 1000.0) / 1e9
+        step_gbs = nbytes["total"] / (ms_step / 1000.0) / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "query-layers/s", "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{a.workload}: 20-layer CSA2 decoder step, N={info['N']} visible entries, "
+                                   f"B={B} sequences per GPU, Top-{info['k']}, SWA {info['W']}, "
+                                   f"pool {info['NB']}x{info['P']}",
+                       "N": info["N"], "B": B, "layers": info["layers"], "d_kv": info["d"], "Hq": info["Hq"],
+                       "indexer": f"{info['H_i']}x{info['d_ik']}", "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB algorithmic bytes per step"},
+            "roofline": {"bound": "hbm", "kernel": "csa2_index_full (scan + pool Top-k)", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": peak_kind},
+            "step_hbm": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": step_gbs, "frac": step_gbs / peak},
+            "clocks": clk,
+            "gpu_launches": a.steps * (3 + 2 + 2 * info["schedule"].count("reindex") + 2 * info["layers"]),
+            "e2e": {"value": e2e_val, "unit": "query-layers/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+        }
+        if not a.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(info["N"], a.cpu_queries,
+                                                "DEC128K" if a.workload == "decode128k" else "DEC1M")
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""Python face of the CSA2 C ABI: torch tensors in, device pointers to libcsa2.so.
+
+Names follow include/csa2.h: compress_quant, index_full, index_reindex, sparse_attn.
+PyTorch provides device memory and the current stream; every computation runs in the
+library's kernels.  Outputs are allocated here when the caller passes none (pass them
+in, together with a pre-sized Workspace, to capture calls in a CUDA graph).
+"""
+import ctypes
+import math
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+PAGE = 64
+BF16, F32 = 0, 1
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _expect(t, dtypes, name):
+    if t is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+
+
+_I32 = (torch.int32,)
+_B16 = (torch.bfloat16, torch.int16)
+_U8 = (torch.uint8,)
+_F32 = (torch.float32,)
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+@dataclass
+class PagedCache:
+    """Paged Main KV planes: codes uint8 [pages, 64, d/2], scales uint8 [pages, 64, d/16],
+    idx_k bf16 [pages, 64, d_ik] (optional), page_table int32 [seqs, max_pages]."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    idx_k: Optional[torch.Tensor]
+    page_table: torch.Tensor
+
+    @property
+    def d(self):
+        return self.codes.shape[-1] * 2
+
+    @property
+    def d_ik(self):
+        return self.idx_k.shape[-1] if self.idx_k is not None else 0
+
+    @property
+    def num_pages(self):
+        return self.codes.shape[0]
+
+    @property
+    def num_seqs(self):
+        return self.page_table.shape[0]
+
+    @property
+    def max_pages(self):
+        return self.page_table.shape[1]
+
+    @staticmethod
+    def allocate(num_seqs, entries_per_seq, d, d_ik, device, page_table=None):
+        mp = (entries_per_seq + PAGE - 1) // PAGE
+        npg = num_seqs * mp
+        if page_table is None:
+            page_table = torch.arange(npg, dtype=torch.int32).reshape(num_seqs, mp)
+        page_table = page_table.to(device=device, dtype=torch.int32).contiguous()
+        npg = max(npg, int(page_table.max().item()) + 1) if page_table.numel() else npg
+        codes = torch.zeros((npg, PAGE, d // 2), dtype=torch.uint8, device=device)
+        scales = torch.zeros((npg, PAGE, d // 16), dtype=torch.uint8, device=device)
+        idx_k = torch.zeros((npg, PAGE, d_ik), dtype=torch.bfloat16, device=device) if d_ik else None
+        return PagedCache(codes, scales, idx_k, page_table)
+
+    def c_struct(self):
+        for t, n in [(self.codes, "codes"), (self.scales, "scales")]:
+            _expect(t, _U8, n)
+        _expect(self.idx_k, _B16, "idx_k")
+        _expect(self.page_table, _I32, "page_table")
+        return _lib.Cache(_ptr(self.codes), _ptr(self.scales), _ptr(self.idx_k), _ptr(self.page_table),
+                          self.num_pages, PAGE, self.num_seqs, self.max_pages, self.d, self.d_ik)
+
+
+class Workspace:
+    """Grow-only device scratch buffer handed to the library calls."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.buf = torch.empty(0, dtype=torch.uint8, device=device)
+
+    def get(self, nbytes):
+        if self.buf.numel() < nbytes:
+            if torch.cuda.is_current_stream_capturing():
+                raise RuntimeError("workspace must be sized before CUDA graph capture")
+            self.buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _ws(ws, device):
+    if ws is not None:
+        return ws
+    key = str(device)
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(device)
+    return _default_ws[key]
+
+
+def _call(fn, args, ws, device):
+    L = _lib.lib()
+    need = ctypes.c_size_t(0)
+    _lib.check(getattr(L, fn + "_workspace")(ctypes.byref(args), ctypes.byref(need)))
+    buf = _ws(ws, device).get(need.value)
+    _lib.check(getattr(L, fn)(ctypes.byref(args), ctypes.c_void_p(buf.data_ptr()), need.value, _stream()))
+
+
+def compress_quant(cache: PagedCache, seq, entry, *, m=1, C=None, Z=None, H=None, W_kv=None, W_z=None,
+                   pos=None, rope_cos=None, rope_sin=None, W_ik=None, y_out=None, ws=None):
+    """Compress m-token groups into FP4 Main KV entries written through the page table.
+    Given mode: C (and Z when m > 1) float32 [T, d].  Projection mode: H [T, d_model]
+    (bf16 or float32) with W_kv, W_z bf16 [d_model, d].  seq/entry/pos: int32 [T/m]."""
+    if W_kv is not None:
+        T, d_model = H.shape
+        _expect(H, _B16 + _F32, "H")
+        h_dtype = F32 if H.dtype == torch.float32 else BF16
+    else:
+        T, d_model, h_dtype = C.shape[0], 0, BF16
+        _expect(C, _F32, "C")
+        _expect(Z, _F32, "Z")
+    for t, n in [(seq, "seq"), (entry, "entry"), (pos, "pos")]:
+        _expect(t, _I32, n)
+    d_rope = 0 if rope_cos is None else rope_cos.shape[1] * 2
+    a = _lib.CompressArgs()
+    a.struct_size = ctypes.sizeof(_lib.CompressArgs)
+    a.T, a.m, a.d_model, a.h_dtype = T, m, d_model, h_dtype
+    a.H, a.W_kv, a.W_z, a.C, a.Z = _ptr(H), _ptr(W_kv), _ptr(W_z), _ptr(C), _ptr(Z)
+    a.d_rope = d_rope
+    a.rope_max_pos = rope_cos.shape[0] if rope_cos is not None else 0
+    a.rope_cos, a.rope_sin, a.pos = _ptr(rope_cos), _ptr(rope_sin), _ptr(pos)
+    a.seq, a.entry, a.W_ik = _ptr(seq), _ptr(entry), _ptr(W_ik)
+    a.cache = cache.c_struct()
+    a.y_out = _ptr(y_out)
+    _call("csa2_compress_quant", a, ws, cache.codes.device)
+
+
+def index_full(cache: PagedCache, q_idx, w, seq_of, n_vis, max_n, num_blocks=2048, per_block=8, k=512,
+               relu=True, out=None, ws=None):
+    """Full-mode indexer.  q_idx bf16 [B, H_i, d_ik], w float32 [B, H_i], seq_of / n_vis
+    int32 [B].  Returns (pool [B, NB*P], pool_len [B], topk [B, k], topk_len [B])."""
+    B, H_i, _ = q_idx.shape
+    dev = q_idx.device
+    if out is None:
+        out = (torch.empty((B, num_blocks * per_block), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty((B, k), dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev))
+    pool, pool_len, topk, topk_len = out
+    _expect(q_idx, _B16, "q_idx")
+    _expect(w, _F32, "w")
+    a = _lib.IndexFullArgs()
+    a.struct_size = ctypes.sizeof(_lib.IndexFullArgs)
+    a.B, a.H_i = B, H_i
+    a.q_idx, a.w = _ptr(q_idx), _ptr(w)
+    a.cache = cache.c_struct()
+    a.seq_of, a.n_vis, a.max_n = _ptr(seq_of), _ptr(n_vis), int(max_n)
+    a.num_blocks, a.per_block, a.k, a.relu = num_blocks, per_block, k, int(bool(relu))
+    a.pool, a.pool_len, a.topk, a.topk_len = _ptr(pool), _ptr(pool_len), _ptr(topk), _ptr(topk_len)
+    _call("csa2_index_full", a, ws, dev)
+    return out
+
+
+def index_reindex(cache: PagedCache, q_idx, w, seq_of, pool, pool_len, k=512, relu=True, out=None, ws=None):
+    """Reindex mode: re-score only the pool.  Returns (topk [B, k], topk_len [B])."""
+    B, H_i, _ = q_idx.shape
+    dev = q_idx.device
+    if out is None:
+        out = (torch.empty((B, k), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev))
+    topk, topk_len = out
+    a = _lib.IndexReindexArgs()
+    a.struct_size = ctypes.sizeof(_lib.IndexReindexArgs)
+    a.B, a.H_i = B, H_i
+    a.q_idx, a.w = _ptr(q_idx), _ptr(w)
+    a.cache = cache.c_struct()
+    a.seq_of, a.pool, a.pool_len, a.pool_stride = _ptr(seq_of), _ptr(pool), _ptr(pool_len), pool.shape[1]
+    a.k, a.relu = k, int(bool(relu))
+    a.topk, a.topk_len = _ptr(topk), _ptr(topk_len)
+    _call("csa2_index_reindex", a, ws, dev)
+    return out
+
+
+def sparse_attn(cache: PagedCache, q, seq_of, topk, topk_len, swa, swa_scale, swa_start, swa_len, swa_max,
+                softmax_scale=None, out_dtype=torch.bfloat16, out=None, lse=None, ws=None):
+    """One softmax over the selected FP4 entries plus the SWA window.  q bf16 [B, Hq, d].
+    Returns (out [B, Hq, d], lse float32 [B, Hq])."""
+    B, Hq, d = q.shape
+    dev = q.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    _expect(q, _B16, "q")
+    a = _lib.AttnArgs()
+    a.struct_size = ctypes.sizeof(_lib.AttnArgs)
+    a.B, a.Hq, a.q = B, Hq, _ptr(q)
+    a.cache = cache.c_struct()
+    a.seq_of, a.topk, a.topk_len, a.k = _ptr(seq_of), _ptr(topk), _ptr(topk_len), topk.shape[1]
+    a.swa, a.swa_scale = _ptr(swa), _ptr(swa_scale)
+    a.swa_rows = swa.shape[0] if swa is not None else 0
+    a.swa_start, a.swa_len, a.swa_max = _ptr(swa_start), _ptr(swa_len), int(swa_max)
+    a.softmax_scale = float(softmax_scale)
+    a.out = _ptr(out)
+    a.out_dtype = F32 if out.dtype == torch.float32 else BF16
+    a.lse = _ptr(lse)
+    _call("csa2_sparse_attn", a, ws, dev)
+    return out, lse
+
+
+def device_error():
+    """Synchronise and return (and clear) the device error word."""
+    w = ctypes.c_uint32(0)
+    _lib.check(_lib.lib().csa2_get_device_error(ctypes.byref(w)))
+    return w.value
+
+
+def version():
+    return _lib.lib().csa2_version()

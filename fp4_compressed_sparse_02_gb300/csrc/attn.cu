@@ -1,0 +1,436 @@
+// Sparse MQA attention of each decode query over its selected FP4 Main KV entries plus
+// its FP8 SWA window, in one softmax.
+//
+// "DeepSeek-V4.1-Flash deep dive", section 3.1: Main Q attends to (selected Main KV +
+// layer-local SWA KV); section 6.3: 64 query heads x 512 dims, Top-K 512, n_win 128.
+//
+// Split over keys: CTA (query b, chunk c) takes key slots [c*128, c*128+128) of the
+// list [topk slots 0..k) ++ [window rows 0..swa_max), gathers and dequantises them into
+// shared memory as fp16 (FP4 x E4M3 and E4M3 values are exact in fp16), runs
+// S = Q K^T and O = P V on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
+// accumulate) and writes an unnormalised partial (O, row max, row sum).  k_combine
+// merges the chunks of a query.  The entry vector is both K and V, so one shared-memory
+// tile serves both products (row-major for S, transposed ldmatrix for O).
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+CSA2_DEFINE_ERROR_WORD(g_err_attn);
+
+constexpr unsigned AFULL = 0xffffffffu;
+constexpr int KC = 128;          // keys per CTA
+constexpr int ATHREADS = 512;    // 16 warps
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct AttnParams {
+  const uint16_t* q;
+  csa2_cache cache;
+  const int* seq_of;
+  const int* topk;
+  const int* topk_len;
+  int k;
+  const uint8_t* swa;
+  const float* swa_scale;
+  int swa_rows;
+  const int* swa_start;
+  const int* swa_len;
+  int swa_max;
+  int Hq;
+  int nchunk;
+  float scale_log2;               // softmax_scale * log2(e)
+  float* opart;                   // [B][nchunk][Hq][DIM]
+  float2* ml;                     // [B][nchunk][Hq]  (row max in log2 units, row sum)
+};
+
+// byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile of `rowbytes`
+__device__ __forceinline__ uint32_t swz(int row, int ch, int rowbytes) {
+  return (uint32_t)(row * rowbytes + ((ch ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int DIM, int MT>
+struct ACfg {
+  static constexpr int HP = 16 * MT;                  // padded heads
+  static constexpr int ROWB = DIM * 2;                // bytes per f16 row of Q / KV
+  static constexpr int PROWB = KC * 2;                // bytes per f16 row of P
+  static constexpr int KG = 16 / MT;                  // key groups in S
+  static constexpr int KPW = KC / KG;                 // keys per warp in S (= 8*MT)
+  static constexpr int DPW = DIM * MT / 16;           // dims per warp in O
+  static constexpr int NTO = DPW / 8;                 // n-tiles per warp in O
+  static constexpr int SMEM_Q = HP * ROWB;
+  static constexpr int SMEM_KV = KC * ROWB;
+  static constexpr int SMEM_P = HP * PROWB;
+  static constexpr int SMEM_RED = 2 * HP * KG * 4;
+  static constexpr int SMEM = SMEM_Q + SMEM_KV + SMEM_P + SMEM_RED;
+};
+
+template <int DIM, int MT>
+__global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
+  using C = ACfg<DIM, MT>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sQ = smem;
+  uint8_t* sKV = sQ + C::SMEM_Q;
+  uint8_t* sP = sKV + C::SMEM_KV;
+  float* sMax = reinterpret_cast<float*>(sP + C::SMEM_P);   // [HP][KG]
+  float* sSum = sMax + C::HP * C::KG;                         // [HP][KG]
+  __shared__ long long keyrow[KC];
+  __shared__ float keyscale[KC];
+  __shared__ int keykind[KC];       // 0 none, 1 FP4 entry, 2 SWA row
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int b = blockIdx.y, chunk = blockIdx.x;
+  const uint32_t qs = smem_u32(sQ), kvs = smem_u32(sKV), ps = smem_u32(sP);
+
+  // ---- 1. resolve this chunk's key slots --------------------------------------
+  if (tid < KC) {
+    const int j = chunk * KC + tid;
+    int kind = 0;
+    long long row = -1;
+    float sc = 0.f;
+    if (j < p.k) {
+      int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
+      if (j < tl) {
+        int e = __ldg(p.topk + (long long)b * p.k + j);
+        if (e >= 0) {
+          row = entry_row(p.cache, __ldg(p.seq_of + b), e, &g_err_attn);
+          kind = row >= 0 ? 1 : 0;
+        }
+      }
+    } else if (j - p.k < p.swa_max) {
+      int w = j - p.k;
+      if (w < __ldg(p.swa_len + b)) {
+        long long r = (long long)__ldg(p.swa_start + b) + w;
+        if (r >= 0 && r < p.swa_rows) {
+          row = r;
+          kind = 2;
+          sc = __ldg(p.swa_scale + r);
+        } else {
+          raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
+        }
+      }
+    }
+    keyrow[tid] = row;
+    keykind[tid] = kind;
+    keyscale[tid] = sc;
+  }
+  // ---- 2. Q (bf16 -> fp16), rows >= Hq are zero ------------------------------
+  for (int i = tid; i < C::HP * (DIM / 8); i += ATHREADS) {
+    const int h = i / (DIM / 8), ch = i % (DIM / 8);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (h < p.Hq) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + h) * DIM) + ch);
+    uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                         bf16x2_to_f16x2(v.w));
+    *reinterpret_cast<uint4*>(sQ + swz(h, ch, C::ROWB)) = o;
+  }
+  __syncthreads();
+  // ---- 3. gather + dequantise the 128 keys (4 threads per key) -----------------
+  {
+    const int key = tid >> 2, qtr = tid & 3;
+    const int kind = keykind[key];
+    const long long row = keyrow[key];
+    constexpr int DQ = DIM / 4;                 // dims per thread
+    if (kind == 1) {
+      const uint8_t* cp = p.cache.codes + row * (DIM / 2) + qtr * (DQ / 2);
+      const uint8_t* sp = p.cache.scales + row * (DIM / 16) + qtr * (DQ / 16);
+#pragma unroll
+      for (int cc = 0; cc < DQ / 32; ++cc) {      // 16 code bytes = 32 dims = 2 scale groups
+        uint4 cw = ldg_stream_v4(cp + cc * 16);
+        uint16_t s2 = (uint16_t)sp[cc * 2] | ((uint16_t)sp[cc * 2 + 1] << 8);
+        uint32_t sh = e4m3x2_to_f16x2(s2);
+        uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
+        uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        uint32_t outw[16];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int bi = 0; bi < 4; ++bi) {
+            uint32_t h2 = e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu);
+            outw[wi * 4 + bi] = hmul2_u32(h2, wi < 2 ? s0 : s1);
+          }
+        const int ch0 = (qtr * DQ + cc * 32) / 8;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          *reinterpret_cast<uint4*>(sKV + swz(key, ch0 + t, C::ROWB)) =
+              make_uint4(outw[4 * t], outw[4 * t + 1], outw[4 * t + 2], outw[4 * t + 3]);
+      }
+    } else if (kind == 2) {
+      const uint8_t* rp = p.swa + row * DIM + qtr * DQ;
+      const float sc = keyscale[key];
+#pragma unroll
+      for (int cc = 0; cc < DQ / 16; ++cc) {      // 16 bytes = 16 dims = 2 smem chunks
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + cc * 16));
+        uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t outw[8];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
+            __half2 hv = *reinterpret_cast<__half2*>(&h2);
+            __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
+            outw[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
+          }
+        const int ch0 = (qtr * DQ + cc * 16) / 8;
+        *reinterpret_cast<uint4*>(sKV + swz(key, ch0, C::ROWB)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        *reinterpret_cast<uint4*>(sKV + swz(key, ch0 + 1, C::ROWB)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+      }
+    } else {
+      const int ch0 = qtr * DQ / 8;
+#pragma unroll
+      for (int t = 0; t < DQ / 8; ++t)
+        *reinterpret_cast<uint4*>(sKV + swz(key, ch0 + t, C::ROWB)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  __syncthreads();
+  // ---- 4. S = Q K^T: warp -> (m-tile mt, key group kg of 8*MT keys) ------------
+  const int mt = warp % MT, kg = warp / MT;
+  const int kbase = kg * C::KPW;
+  float sacc[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+  {
+    const int arow = mt * 16 + (lane & 15);
+    const int mi = lane >> 3, r8 = lane & 7;
+    if constexpr (MT == 1) {
+#pragma unroll 4
+      for (int ks = 0; ks < DIM / 16; ks += 2) {
+        uint32_t a[2][4];
+        ldmatrix_x4(a[0][0], a[0][1], a[0][2], a[0][3], qs + swz(arow, 2 * ks + (lane >> 4), C::ROWB));
+        ldmatrix_x4(a[1][0], a[1][1], a[1][2], a[1][3], qs + swz(arow, 2 * ks + 2 + (lane >> 4), C::ROWB));
+        uint32_t bb[4];
+        ldmatrix_x4(bb[0], bb[1], bb[2], bb[3], kvs + swz(kbase + r8, 2 * ks + mi, C::ROWB));
+        mma_f16_16816(sacc[0], a[0][0], a[0][1], a[0][2], a[0][3], bb[0], bb[1]);
+        mma_f16_16816(sacc[0], a[1][0], a[1][1], a[1][2], a[1][3], bb[2], bb[3]);
+      }
+    } else {
+#pragma unroll 2
+      for (int ks = 0; ks < DIM / 16; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(a0, a1, a2, a3, qs + swz(arow, 2 * ks + (lane >> 4), C::ROWB));
+#pragma unroll
+        for (int np = 0; np < MT / 2; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int key = kbase + np * 16 + (mi >> 1) * 8 + r8;
+          ldmatrix_x4(b0, b1, b2, b3, kvs + swz(key, 2 * ks + (mi & 1), C::ROWB));
+          mma_f16_16816(sacc[2 * np], a0, a1, a2, a3, b0, b1);
+          mma_f16_16816(sacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+  }
+  // ---- 5. chunk-local softmax -------------------------------------------------
+  // thread holds rows r0 = mt*16+g, r1 = r0+8; keys kbase + 8t + 2c + {0,1}
+  const int r0 = mt * 16 + g, r1 = r0 + 8;
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = kbase + 8 * t + 2 * c + e;
+      const bool valid = keykind[key] != 0;
+      float v0 = valid ? sacc[t][e] * p.scale_log2 : -INFINITY;
+      float v1 = valid ? sacc[t][2 + e] * p.scale_log2 : -INFINITY;
+      sacc[t][e] = v0;
+      sacc[t][2 + e] = v1;
+      mx0 = fmaxf(mx0, v0);
+      mx1 = fmaxf(mx1, v1);
+    }
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(AFULL, mx0, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(AFULL, mx1, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(AFULL, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(AFULL, mx1, 2));
+  if (c == 0) {
+    sMax[r0 * C::KG + kg] = mx0;
+    sMax[r1 * C::KG + kg] = mx1;
+  }
+  __syncthreads();
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < C::KG; ++q) {
+    m0 = fmaxf(m0, sMax[r0 * C::KG + q]);
+    m1 = fmaxf(m1, sMax[r1 * C::KG + q]);
+  }
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int t = 0; t < MT; ++t) {
+    const int key = kbase + 8 * t + 2 * c;
+    float e00 = (m0 == -INFINITY) ? 0.f : exp2f(sacc[t][0] - m0);
+    float e01 = (m0 == -INFINITY) ? 0.f : exp2f(sacc[t][1] - m0);
+    float e10 = (m1 == -INFINITY) ? 0.f : exp2f(sacc[t][2] - m1);
+    float e11 = (m1 == -INFINITY) ? 0.f : exp2f(sacc[t][3] - m1);
+    __half2 h0 = __floats2half2_rn(e00, e01);
+    __half2 h1 = __floats2half2_rn(e10, e11);
+    l0 += __low2float(h0) + __high2float(h0);
+    l1 += __low2float(h1) + __high2float(h1);
+    // P[row][key..key+1]: chunk key/8, element offset (key%8)*2 bytes
+    *reinterpret_cast<__half2*>(sP + swz(r0, key >> 3, C::PROWB) + (key & 7) * 2) = h0;
+    *reinterpret_cast<__half2*>(sP + swz(r1, key >> 3, C::PROWB) + (key & 7) * 2) = h1;
+  }
+  l0 += __shfl_xor_sync(AFULL, l0, 1);
+  l1 += __shfl_xor_sync(AFULL, l1, 1);
+  l0 += __shfl_xor_sync(AFULL, l0, 2);
+  l1 += __shfl_xor_sync(AFULL, l1, 2);
+  if (c == 0) {
+    sSum[r0 * C::KG + kg] = l0;
+    sSum[r1 * C::KG + kg] = l1;
+  }
+  __syncthreads();
+  // ---- 6. O = P V: warp -> (m-tile mt, dims [dg*DPW, +DPW)) --------------------
+  const int dg = warp / MT;
+  const int dbase = dg * C::DPW;
+  float oacc[C::NTO][4];
+#pragma unroll
+  for (int t = 0; t < C::NTO; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
+  {
+    const int arow = mt * 16 + (lane & 15);
+    const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+    for (int ks = 0; ks < KC / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(a0, a1, a2, a3, ps + swz(arow, 2 * ks + (lane >> 4), C::PROWB));
+      if constexpr (C::NTO == 1) {
+        // two k-steps' worth is not needed: one n-tile, keys 16ks..16ks+15
+        uint32_t b0, b1, b2, b3;
+        const int key = 16 * ks + (mi & 1) * 8 + r8;
+        ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(key, dbase / 8, C::ROWB));
+        mma_f16_16816(oacc[0], a0, a1, a2, a3, b0, b1);
+      } else {
+#pragma unroll
+        for (int np = 0; np < C::NTO / 2; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int key = 16 * ks + (mi & 1) * 8 + r8;
+          ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(key, (dbase + 16 * np) / 8 + (mi >> 1), C::ROWB));
+          mma_f16_16816(oacc[2 * np], a0, a1, a2, a3, b0, b1);
+          mma_f16_16816(oacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+  }
+  // ---- 7. partial outputs -----------------------------------------------------
+  const long long pbase = ((long long)b * p.nchunk + chunk) * p.Hq;
+  if (r0 < p.Hq) {
+    float* o = p.opart + (pbase + r0) * DIM + dbase + 2 * c;
+#pragma unroll
+    for (int t = 0; t < C::NTO; ++t) *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][0], oacc[t][1]);
+  }
+  if (r1 < p.Hq) {
+    float* o = p.opart + (pbase + r1) * DIM + dbase + 2 * c;
+#pragma unroll
+    for (int t = 0; t < C::NTO; ++t) *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][2], oacc[t][3]);
+  }
+  if (dg == 0 && c == 0) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < C::KG; ++q) { s0 += sSum[r0 * C::KG + q]; s1 += sSum[r1 * C::KG + q]; }
+    if (r0 < p.Hq) p.ml[pbase + r0] = make_float2(m0, s0);
+    if (r1 < p.Hq) p.ml[pbase + r1] = make_float2(m1, s1);
+  }
+}
+
+// Merge the chunk partials of (query b, head h).  Thread -> 4 dims.
+template <int DIM>
+__global__ void __launch_bounds__(DIM / 4) k_combine(const float* __restrict__ opart, const float2* __restrict__ ml,
+                                                     int Hq, int nchunk, void* out, int out_f32, float* lse) {
+  const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
+  float M = -INFINITY;
+  for (int c = 0; c < nchunk; ++c) M = fmaxf(M, ml[((long long)b * nchunk + c) * Hq + h].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int c = 0; c < nchunk; ++c) {
+      const long long pi = ((long long)b * nchunk + c) * Hq + h;
+      float2 v = ml[pi];
+      if (v.x == -INFINITY) continue;
+      float wgt = exp2f(v.x - M);
+      L += v.y * wgt;
+      float4 o = *reinterpret_cast<const float4*>(opart + pi * DIM + 4 * t);
+      acc.x += o.x * wgt; acc.y += o.y * wgt; acc.z += o.z * wgt; acc.w += o.w * wgt;
+    }
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  const long long ob = ((long long)b * Hq + h) * DIM + 4 * t;
+  if (out_f32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + ob) = acc;
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 v = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + ob) = v;
+  }
+  if (lse && t == 0) lse[(long long)b * Hq + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+}
+
+// ---------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------
+static int attn_nchunk(const csa2_attn_args& a) { return (a.k + a.swa_max + KC - 1) / KC; }
+
+size_t attn_workspace_bytes(const csa2_attn_args& a) {
+  size_t n = (size_t)a.B * attn_nchunk(a) * a.Hq;
+  return n * a.cache.d * sizeof(float) + n * sizeof(float2);
+}
+
+template <int DIM, int MT>
+static cudaError_t run_attn(const csa2_attn_args& a, AttnParams& ap, cudaStream_t st) {
+  using C = ACfg<DIM, MT>;
+  static bool attr_set = false;   // per instantiation; harmless to repeat
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_chunk<DIM, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(ap.nchunk, a.B);
+  k_attn_chunk<DIM, MT><<<grid, ATHREADS, C::SMEM, st>>>(ap);
+  k_combine<DIM><<<dim3(a.B, a.Hq), DIM / 4, 0, st>>>(ap.opart, ap.ml, a.Hq, ap.nchunk, a.out,
+                                                     a.out_dtype == CSA2_F32, a.lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  AttnParams ap{};
+  ap.q = a.q;
+  ap.cache = a.cache;
+  ap.seq_of = a.seq_of;
+  ap.topk = a.topk;
+  ap.topk_len = a.topk_len;
+  ap.k = a.k;
+  ap.swa = a.swa;
+  ap.swa_scale = a.swa_scale;
+  ap.swa_rows = a.swa_rows;
+  ap.swa_start = a.swa_start;
+  ap.swa_len = a.swa_len;
+  ap.swa_max = a.swa_max;
+  ap.Hq = a.Hq;
+  ap.nchunk = attn_nchunk(a);
+  ap.scale_log2 = a.softmax_scale * LOG2E;
+  size_t n = (size_t)a.B * ap.nchunk * a.Hq;
+  ap.opart = static_cast<float*>(ws);
+  ap.ml = reinterpret_cast<float2*>(static_cast<float*>(ws) + n * a.cache.d);
+  const int mt = (a.Hq + 15) / 16;
+  if (a.cache.d == 512) {
+    if (mt == 4) return run_attn<512, 4>(a, ap, st);
+    if (mt == 2) return run_attn<512, 2>(a, ap, st);
+    return run_attn<512, 1>(a, ap, st);
+  }
+  if (mt == 4) return run_attn<128, 4>(a, ap, st);
+  if (mt == 2) return run_attn<128, 2>(a, ap, st);
+  return run_attn<128, 1>(a, ap, st);
+}
+
+uint32_t read_clear_error_attn() {
+  uint32_t v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_err_attn, sizeof(v));
+  cudaMemcpyToSymbol(g_err_attn, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace csa2

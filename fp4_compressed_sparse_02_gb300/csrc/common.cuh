@@ -1,0 +1,132 @@
+// Shared device helpers of the CSA2 library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+constexpr int kPage = CSA2_PAGE_SIZE;   // entries per page
+constexpr int kPageShift = 6;
+
+// Each translation unit owns one device error word; the API layer ORs them.
+// A kernel that meets an out-of-range value reported by the device (a page id, an
+// n_vis, a pool length) sets a bit here and skips the access.
+#define CSA2_DEFINE_ERROR_WORD(name) static __device__ unsigned int name = 0u
+
+__device__ __forceinline__ void raise_error(unsigned int* word, unsigned int bit) {
+  atomicOr(word, bit);
+}
+
+// Resolve entry e of sequence s to a row index in the page planes (page*64 + slot),
+// or -1 (with an error bit) when the page table points outside the planes.
+__device__ __forceinline__ long long entry_row(const csa2_cache& c, int s, long long e,
+                                               unsigned int* err) {
+  long long p = e >> kPageShift;
+  if (s < 0 || s >= c.num_seqs) { raise_error(err, CSA2_DEVERR_SEQ); return -1; }
+  if (e < 0 || p >= c.max_pages) { raise_error(err, CSA2_DEVERR_PAGE_SLOT); return -1; }
+  int page = __ldg(c.page_table + (long long)s * c.max_pages + p);
+  if (page < 0 || page >= c.num_pages) { raise_error(err, CSA2_DEVERR_PAGE_ID); return -1; }
+  return ((long long)page << kPageShift) | (e & (kPage - 1));
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+
+// --- PTX wrappers -------------------------------------------------------------
+
+// Two float32 -> packed E2M1 pair (lo nibble = a), round-to-nearest-even, satfinite.
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float a, float b) {
+  uint16_t r;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n mov.b16 %0, {t, 0};\n}"
+      : "=h"(r) : "f"(a), "f"(b));
+  return (uint32_t)(r & 0xFF);
+}
+
+// float32 -> E4M3 byte, round-to-nearest-even, satfinite.
+__device__ __forceinline__ uint32_t cvt_e4m3(float a) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(a));
+  return (uint32_t)(r & 0xFF);
+}
+
+// One byte of two E2M1 codes -> fp16x2 (lo nibble -> low half).  Exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// Two E4M3 bytes (lo byte -> low half) -> fp16x2.  Exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+  uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(byte & 0xFF));
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// mma.sync m16n8k16, fp32 accumulate.  BF16 or F16 operands.
+__device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(saddr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3, uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(saddr));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte streaming load that does not allocate in L1 (single-use HBM data).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// Order-preserving map float -> uint32 (larger float -> larger key); -0 maps like +0.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  if (f == 0.0f) f = 0.0f;   // -0 and +0 get one key
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace csa2

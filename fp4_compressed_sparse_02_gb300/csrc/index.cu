@@ -1,0 +1,488 @@
+// Hierarchical sparse indexer: Full scan with per-block top-P (the shared candidate
+// pool), Reindex re-scoring of the pool, and the exact Top-k selection.
+//
+// "DeepSeek-V4.1-Flash deep dive", section 3.1: Indexer Q x Indexer K -> score -> Top-K.
+// Section 3.3: the first Full indexer scans the whole causally visible range and keeps
+// the best positions of every block (2,048 blocks x 8 = a 16,384-entry shared pool);
+// Reindex layers score only the pool; the search range stays 16,384.
+//
+// Scoring runs on the tensor cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate):
+// M = 16 cache rows, N = 8 indexer heads, K = 16 dims.  Each thread loads its own
+// 16-byte slices of a row straight from HBM into registers (no shared-memory staging):
+// the contraction over dims is invariant under any permutation applied to both
+// operands, so the k-slots of the fragment are mapped to the dims each thread loads
+// contiguously (32j + 8c + [0, 8) for lane c of a row quad).  The indexer Q of the query
+// is loaded with the same mapping once per warp.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+CSA2_DEFINE_ERROR_WORD(g_err_index);
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+template <int DK, int NHG>
+struct QFrag {
+  uint4 v[NHG][DK / 32];
+  float w[NHG][2];
+};
+
+template <int DK, int NHG>
+__device__ __forceinline__ void load_qfrag(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                                           int H_i, QFrag<DK, NHG>& f) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int hg = 0; hg < NHG; ++hg) {
+    int head = hg * 8 + g;
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j) {
+      f.v[hg][j] = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + 32 * j + 8 * c))
+                                : make_uint4(0, 0, 0, 0);
+    }
+    int h0 = hg * 8 + 2 * c;
+    f.w[hg][0] = (h0 < H_i) ? __ldg(w + h0) : 0.f;
+    f.w[hg][1] = (h0 + 1 < H_i) ? __ldg(w + h0 + 1) : 0.f;
+  }
+}
+
+// Load the thread's slices of one cache row (zeros when row < 0).
+template <int DK>
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ idxk, long long row, uint4* a) {
+  const int c = threadIdx.x & 3;
+#pragma unroll
+  for (int j = 0; j < DK / 32; ++j)
+    a[j] = (row >= 0) ? ldg_stream_v4(idxk + row * DK + 32 * j + 8 * c) : make_uint4(0, 0, 0, 0);
+}
+
+// Scores of rows (g) and (g + 8) of a 16-row tile; identical in the 4 lanes of a quad.
+template <int DK, int NHG>
+__device__ __forceinline__ void tile_scores(const QFrag<DK, NHG>& f, const uint4* A0, const uint4* A1,
+                                            bool relu, float& s0, float& s1) {
+  float acc[NHG][4];
+#pragma unroll
+  for (int hg = 0; hg < NHG; ++hg) acc[hg][0] = acc[hg][1] = acc[hg][2] = acc[hg][3] = 0.f;
+#pragma unroll
+  for (int j = 0; j < DK / 32; ++j) {
+#pragma unroll
+    for (int hg = 0; hg < NHG; ++hg) {
+      mma_bf16_16816(acc[hg], A0[j].x, A1[j].x, A0[j].y, A1[j].y, f.v[hg][j].x, f.v[hg][j].y);
+      mma_bf16_16816(acc[hg], A0[j].z, A1[j].z, A0[j].w, A1[j].w, f.v[hg][j].z, f.v[hg][j].w);
+    }
+  }
+  float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+  for (int hg = 0; hg < NHG; ++hg) {
+    float a0 = acc[hg][0], a1 = acc[hg][1], a2 = acc[hg][2], a3 = acc[hg][3];
+    if (relu) { a0 = fmaxf(a0, 0.f); a1 = fmaxf(a1, 0.f); a2 = fmaxf(a2, 0.f); a3 = fmaxf(a3, 0.f); }
+    p0 = fmaf(f.w[hg][0], a0, p0);
+    p0 = fmaf(f.w[hg][1], a1, p0);
+    p1 = fmaf(f.w[hg][0], a2, p1);
+    p1 = fmaf(f.w[hg][1], a3, p1);
+  }
+  p0 += __shfl_xor_sync(FULL_MASK, p0, 1);
+  p1 += __shfl_xor_sync(FULL_MASK, p1, 1);
+  p0 += __shfl_xor_sync(FULL_MASK, p0, 2);
+  p1 += __shfl_xor_sync(FULL_MASK, p1, 2);
+  s0 = p0;
+  s1 = p1;
+}
+
+__device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// ---------------------------------------------------------------------------------
+// Full scan: one warp per pool block.  The warp keeps the block's best P entries in
+// lanes 0..P-1 (sorted best first) and inserts candidates that beat the P-th.
+// ---------------------------------------------------------------------------------
+struct ScanParams {
+  const uint16_t* q;      // [B][H_i][DK]
+  const float* w;         // [B][H_i]
+  csa2_cache cache;
+  const int* seq_of;
+  const int* n_vis;
+  int max_n;
+  int H_i, NB, P;
+  int relu;
+  int* pool;              // [B][NB*P]
+  float* pool_score;      // [B][NB*P]
+};
+
+template <int DK, int NHG>
+__global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int b = blockIdx.y;
+  const int j = blockIdx.x * 8 + warp;
+  if (j >= p.NB) return;
+  int n = __ldg(p.n_vis + b);
+  if (n < 0 || n > p.max_n) {
+    if (lane == 0 && j == 0) raise_error(&g_err_index, CSA2_DEVERR_N_VIS);
+    n = max(0, min(n, p.max_n));
+  }
+  const int s = __ldg(p.seq_of + b);
+  const long long lo = ((long long)j * n) / p.NB;
+  const long long hi = ((long long)(j + 1) * n) / p.NB;
+  const int P = p.P;
+
+  QFrag<DK, NHG> f;
+  load_qfrag<DK, NHG>(p.q + (long long)b * p.H_i * DK, p.w + (long long)b * p.H_i, p.H_i, f);
+
+  float tv = -INFINITY;
+  int ti = 0x7fffffff;
+  float thv = -INFINITY;
+  int thi = 0x7fffffff;
+
+  for (long long base = lo; base < hi; base += 32) {
+    long long r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
+    uint4 A[4][DK / 32];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      long long row = (r[t] < hi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
+      load_row<DK>(p.cache.idx_k, row, A[t]);
+    }
+    float sc[4];
+    tile_scores<DK, NHG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+    tile_scores<DK, NHG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int ri = (int)r[t];
+      bool cand = (c == 0) && (r[t] < hi) && better(sc[t], ri, thv, thi);
+      unsigned m = __ballot_sync(FULL_MASK, cand);
+      while (m) {
+        int src = __ffs(m) - 1;
+        m &= m - 1;
+        float cv = __shfl_sync(FULL_MASK, sc[t], src);
+        int ci = __shfl_sync(FULL_MASK, ri, src);
+        unsigned bm = __ballot_sync(FULL_MASK, lane < P && better(cv, ci, tv, ti));
+        if (bm) {
+          int at = __ffs(bm) - 1;
+          float upv = __shfl_up_sync(FULL_MASK, tv, 1);
+          int upi = __shfl_up_sync(FULL_MASK, ti, 1);
+          if (lane > at && lane < P) { tv = upv; ti = upi; }
+          if (lane == at) { tv = cv; ti = ci; }
+          thv = __shfl_sync(FULL_MASK, tv, P - 1);
+          thi = __shfl_sync(FULL_MASK, ti, P - 1);
+        }
+      }
+    }
+  }
+  const int kept = (int)((hi - lo) < (long long)P ? (hi - lo) : (long long)P);
+  int rank = 0;
+  for (int l = 0; l < P; ++l) {
+    int oi = __shfl_sync(FULL_MASK, ti, l);
+    rank += (l < kept && oi < ti) ? 1 : 0;
+  }
+  const long long off = ((long long)n >= (long long)P * p.NB) ? (long long)P * j : lo;
+  if (lane < kept) {
+    long long o = (long long)b * p.NB * P + off + rank;
+    p.pool[o] = ti;
+    p.pool_score[o] = tv;
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Reindex scoring: scores of the pool entries of each query.
+// ---------------------------------------------------------------------------------
+struct PoolScoreParams {
+  const uint16_t* q;
+  const float* w;
+  csa2_cache cache;
+  const int* seq_of;
+  const int* pool;
+  const int* pool_len;
+  int stride;
+  int H_i;
+  int relu;
+  float* score;           // [B][stride]
+};
+
+template <int DK, int NHG>
+__global__ void __launch_bounds__(256) k_pool_scores(PoolScoreParams p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int b = blockIdx.y;
+  const int pos0 = (blockIdx.x * 8 + warp) * 32;
+  if (pos0 >= p.stride) return;
+  int plen = __ldg(p.pool_len + b);
+  if (plen < 0 || plen > p.stride) {
+    if (lane == 0 && pos0 == 0) raise_error(&g_err_index, CSA2_DEVERR_POOL_ENTRY);
+    plen = max(0, min(plen, p.stride));
+  }
+  if (pos0 >= plen) return;
+  const int s = __ldg(p.seq_of + b);
+  QFrag<DK, NHG> f;
+  load_qfrag<DK, NHG>(p.q + (long long)b * p.H_i * DK, p.w + (long long)b * p.H_i, p.H_i, f);
+  int pos[4] = {pos0 + g, pos0 + g + 8, pos0 + 16 + g, pos0 + 24 + g};
+  uint4 A[4][DK / 32];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    long long row = -1;
+    if (pos[t] < plen) {
+      int e = __ldg(p.pool + (long long)b * p.stride + pos[t]);
+      row = (e >= 0) ? entry_row(p.cache, s, e, &g_err_index) : -1;
+    }
+    load_row<DK>(p.cache.idx_k, row, A[t]);
+  }
+  float sc[4];
+  tile_scores<DK, NHG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+  tile_scores<DK, NHG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+  if (c == 0) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (pos[t] < plen) p.score[(long long)b * p.stride + pos[t]] = sc[t];
+  }
+}
+
+// ---------------------------------------------------------------------------------
+// Exact Top-k of up to 16,384 scored candidates per query: 4-pass radix select of the
+// k-th largest key, then ties at that key taken in ascending position, output in
+// ascending position (= ascending entry, the pool being ascending).  One CTA per query.
+// ---------------------------------------------------------------------------------
+constexpr int SEL_THREADS = 1024;
+constexpr int SEL_PER_THREAD = 16;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(FULL_MASK, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = (lane < nw) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(FULL_MASK, t, o);
+      if (lane >= o) t += y;
+    }
+    sh[lane] = t;
+  }
+  __syncthreads();
+  int base = warp ? sh[warp - 1] : 0;
+  total = sh[nw - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+struct SelectParams {
+  const float* score;     // [B][stride]
+  const int* pool;        // [B][stride]
+  int stride;
+  // candidate count: full mode -> min(n_vis[b], stride); reindex -> pool_len[b]
+  const int* n_vis;
+  int max_n;
+  const int* pool_len_in;
+  int* pool_len_out;      // full mode: written
+  int* pool_out;          // full mode: tail filled with -1
+  int k;
+  int* topk;
+  int* topk_len;
+};
+
+__global__ void __launch_bounds__(SEL_THREADS) k_select(SelectParams p) {
+  __shared__ int hist[256];
+  __shared__ int scan_sh[32];
+  __shared__ int pick[2];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  int P;
+  if (p.n_vis) {
+    int n = __ldg(p.n_vis + b);
+    n = max(0, min(n, p.max_n));
+    P = min(n, p.stride);
+  } else {
+    P = __ldg(p.pool_len_in + b);
+    P = max(0, min(P, p.stride));
+  }
+  const long long rowb = (long long)b * p.stride;
+  if (p.pool_len_out && tid == 0) p.pool_len_out[b] = P;
+  if (p.pool_out)
+    for (int i = P + tid; i < p.stride; i += blockDim.x) p.pool_out[rowb + i] = -1;
+  const int k = p.k;
+  int* out = p.topk + (long long)b * k;
+  if (P <= k) {
+    for (int i = tid; i < k; i += blockDim.x) out[i] = (i < P) ? p.pool[rowb + i] : -1;
+    if (tid == 0) p.topk_len[b] = P;
+    return;
+  }
+  uint32_t key[SEL_PER_THREAD];
+  const int p0 = tid * SEL_PER_THREAD;
+#pragma unroll
+  for (int i = 0; i < SEL_PER_THREAD; ++i) {
+    int q = p0 + i;
+    key[i] = (q < P) ? float_key(p.score[rowb + q]) : 0u;
+  }
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < SEL_PER_THREAD; ++i)
+      if (p0 + i < P && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255], 1);
+    __syncthreads();
+    if (tid < 32) {
+      int cnt[8], local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { cnt[i] = hist[255 - 8 * tid - i]; local += cnt[i]; }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int excl = incl - local;
+      if (excl < remaining && remaining <= incl) {
+        int cum = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + cnt[i] >= remaining) {
+            pick[0] = 255 - 8 * tid - i;
+            pick[1] = remaining - cum;
+            break;
+          }
+          cum += cnt[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= ((uint32_t)pick[0]) << shift;
+    mask |= 0xFFu << shift;
+    remaining = pick[1];
+    __syncthreads();
+  }
+  // ties at the threshold key: the lowest positions first
+  int eq = 0;
+#pragma unroll
+  for (int i = 0; i < SEL_PER_THREAD; ++i) eq += (p0 + i < P && key[i] == prefix) ? 1 : 0;
+  int tot;
+  int eqrank = block_exclusive_scan(eq, scan_sh, tot);
+  unsigned selmask = 0;
+  int nsel = 0;
+#pragma unroll
+  for (int i = 0; i < SEL_PER_THREAD; ++i) {
+    bool sel = false;
+    if (p0 + i < P) {
+      if (key[i] > prefix) sel = true;
+      else if (key[i] == prefix) { sel = eqrank < remaining; ++eqrank; }
+    }
+    if (sel) { selmask |= 1u << i; ++nsel; }
+  }
+  int o = block_exclusive_scan(nsel, scan_sh, tot);
+#pragma unroll
+  for (int i = 0; i < SEL_PER_THREAD; ++i)
+    if ((selmask & (1u << i)) && o < k) out[o++] = p.pool[rowb + p0 + i];
+  for (int i = tot + tid; i < k; i += blockDim.x) out[i] = -1;
+  if (tid == 0) p.topk_len[b] = tot;
+}
+
+// ---------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------
+template <int DK>
+static void launch_scan_dk(const ScanParams& sp, int nhg, dim3 grid, cudaStream_t st) {
+  switch (nhg) {
+    case 1: k_full_scan<DK, 1><<<grid, 256, 0, st>>>(sp); break;
+    case 2: k_full_scan<DK, 2><<<grid, 256, 0, st>>>(sp); break;
+    case 3: k_full_scan<DK, 3><<<grid, 256, 0, st>>>(sp); break;
+    default: k_full_scan<DK, 4><<<grid, 256, 0, st>>>(sp); break;
+  }
+}
+
+template <int DK>
+static void launch_pool_scores_dk(const PoolScoreParams& pp, int nhg, dim3 grid, cudaStream_t st) {
+  switch (nhg) {
+    case 1: k_pool_scores<DK, 1><<<grid, 256, 0, st>>>(pp); break;
+    case 2: k_pool_scores<DK, 2><<<grid, 256, 0, st>>>(pp); break;
+    case 3: k_pool_scores<DK, 3><<<grid, 256, 0, st>>>(pp); break;
+    default: k_pool_scores<DK, 4><<<grid, 256, 0, st>>>(pp); break;
+  }
+}
+
+size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
+  return (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
+}
+
+cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  const int stride = a.num_blocks * a.per_block;
+  ScanParams sp{};
+  sp.q = a.q_idx;
+  sp.w = a.w;
+  sp.cache = a.cache;
+  sp.seq_of = a.seq_of;
+  sp.n_vis = a.n_vis;
+  sp.max_n = a.max_n;
+  sp.H_i = a.H_i;
+  sp.NB = a.num_blocks;
+  sp.P = a.per_block;
+  sp.relu = a.relu;
+  sp.pool = a.pool;
+  sp.pool_score = static_cast<float*>(ws);
+  const int nhg = (a.H_i + 7) / 8;
+  dim3 grid((a.num_blocks + 7) / 8, a.B);
+  if (a.cache.d_ik == 128) launch_scan_dk<128>(sp, nhg, grid, st);
+  else launch_scan_dk<64>(sp, nhg, grid, st);
+  SelectParams sel{};
+  sel.score = static_cast<const float*>(ws);
+  sel.pool = a.pool;
+  sel.stride = stride;
+  sel.n_vis = a.n_vis;
+  sel.max_n = a.max_n;
+  sel.pool_len_out = a.pool_len;
+  sel.pool_out = a.pool;
+  sel.k = a.k;
+  sel.topk = a.topk;
+  sel.topk_len = a.topk_len;
+  k_select<<<a.B, SEL_THREADS, 0, st>>>(sel);
+  return cudaGetLastError();
+}
+
+size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a) {
+  return (size_t)a.B * a.pool_stride * sizeof(float);
+}
+
+cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  PoolScoreParams pp{};
+  pp.q = a.q_idx;
+  pp.w = a.w;
+  pp.cache = a.cache;
+  pp.seq_of = a.seq_of;
+  pp.pool = a.pool;
+  pp.pool_len = a.pool_len;
+  pp.stride = a.pool_stride;
+  pp.H_i = a.H_i;
+  pp.relu = a.relu;
+  pp.score = static_cast<float*>(ws);
+  const int nhg = (a.H_i + 7) / 8;
+  dim3 grid((a.pool_stride + 255) / 256, a.B);
+  if (a.cache.d_ik == 128) launch_pool_scores_dk<128>(pp, nhg, grid, st);
+  else launch_pool_scores_dk<64>(pp, nhg, grid, st);
+  SelectParams sel{};
+  sel.score = static_cast<const float*>(ws);
+  sel.pool = a.pool;
+  sel.stride = a.pool_stride;
+  sel.pool_len_in = a.pool_len;
+  sel.k = a.k;
+  sel.topk = a.topk;
+  sel.topk_len = a.topk_len;
+  k_select<<<a.B, SEL_THREADS, 0, st>>>(sel);
+  return cudaGetLastError();
+}
+
+uint32_t read_clear_error_index() {
+  uint32_t v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_err_index, sizeof(v));
+  cudaMemcpyToSymbol(g_err_index, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace csa2

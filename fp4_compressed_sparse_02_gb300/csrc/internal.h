@@ -1,0 +1,29 @@
+// Launchers shared between the kernel units and the host API layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+// compress.cu
+size_t compress_workspace_bytes(const csa2_compress_args& a);
+cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t st);
+uint32_t read_clear_error_compress();
+
+// index.cu
+size_t index_full_workspace_bytes(const csa2_index_full_args& a);
+cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st);
+size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a);
+cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st);
+uint32_t read_clear_error_index();
+
+// attn.cu
+size_t attn_workspace_bytes(const csa2_attn_args& a);
+cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st);
+uint32_t read_clear_error_attn();
+
+}  // namespace csa2

@@ -1,0 +1,123 @@
+"""Seeded synthetic decode workloads built directly on the device (for sizes where a host
+round trip would dominate set-up).  Same recipes as synth.py (random bytes for FP4
+codes, E4M3 scale bytes in [0x20, 0x3F], N(0,1) bf16 for indexer K / queries / hidden
+states, weights N(0, 1/fan_in), E4M3 SWA rows with exponent field 3..13 and row scales
+in [0.005, 0.02]); no arithmetic of the method happens here."""
+import math
+
+import numpy as np
+import torch
+
+from . import csa2, synth
+from .schedule import FULL, REINDEX, REUSE, DecodeStep, decoder_schedule
+
+
+def _randn_bf16(shape, g, device, sigma=1.0):
+    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * sigma).to(torch.bfloat16)
+
+
+def _fp8_rows(rows, d, g, device):
+    sign = torch.randint(0, 2, (rows, d), generator=g, device=device, dtype=torch.int32) << 7
+    expo = torch.randint(3, 14, (rows, d), generator=g, device=device, dtype=torch.int32) << 3
+    man = torch.randint(0, 8, (rows, d), generator=g, device=device, dtype=torch.int32)
+    return (sign | expo | man).to(torch.uint8)
+
+
+def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedule=None, chunk_pages=32768):
+    """A decode step of B independent sequences with N visible entries each.
+
+    The cache holds N entries per sequence (entry N-1 is rewritten by the step's append
+    when append=True).  Pages are a random permutation.  Returns (DecodeStep, info)."""
+    B = B or cfg["B"]
+    N = N or cfg["N"]
+    d, d_ik, H_i, Hq, W, k = cfg["d"], cfg["d_ik"], cfg["H_i"], cfg["Hq"], cfg["W"], cfg["k"]
+    NB, P, d_model, d_rope = cfg["NB"], cfg["P"], cfg["d_model"], cfg["d_rope"]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    gc = torch.Generator()
+    gc.manual_seed(seed)
+    mp = (N + 63) // 64
+    num_pages = B * mp
+    page_table = torch.randperm(num_pages, generator=gc).to(torch.int32).reshape(B, mp).to(device)
+    cache = csa2.PagedCache(
+        codes=torch.empty((num_pages, 64, d // 2), dtype=torch.uint8, device=device),
+        scales=torch.empty((num_pages, 64, d // 16), dtype=torch.uint8, device=device),
+        idx_k=torch.empty((num_pages, 64, d_ik), dtype=torch.bfloat16, device=device),
+        page_table=page_table)
+    for p0 in range(0, num_pages, chunk_pages):
+        p1 = min(num_pages, p0 + chunk_pages)
+        cache.codes[p0:p1] = torch.randint(0, 256, (p1 - p0, 64, d // 2), generator=g, device=device,
+                                           dtype=torch.uint8)
+        cache.scales[p0:p1] = torch.randint(0x20, 0x40, (p1 - p0, 64, d // 16), generator=g, device=device,
+                                            dtype=torch.uint8)
+        cache.idx_k[p0:p1] = _randn_bf16((p1 - p0, 64, d_ik), g, device)
+    seq_of = torch.arange(B, dtype=torch.int32, device=device)
+    n_vis = torch.full((B,), N, dtype=torch.int32, device=device)
+    sched = schedule or decoder_schedule()
+    layers = []
+    for mode in sched:
+        L = dict(mode=mode, q=_randn_bf16((B, Hq, d), g, device),
+                 swa=_fp8_rows(B * W, d, g, device),
+                 swa_scale=(torch.rand(B * W, generator=g, device=device) * 0.015 + 0.005).float(),
+                 swa_start=torch.arange(B, dtype=torch.int32, device=device) * W,
+                 swa_len=torch.full((B,), W, dtype=torch.int32, device=device))
+        if mode in (FULL, REINDEX):
+            L["q_idx"] = _randn_bf16((B, H_i, d_ik), g, device)
+            L["w"] = torch.randn((B, H_i), generator=g, device=device) / math.sqrt(H_i)
+        layers.append(L)
+    app = None
+    rope = None
+    if append:
+        app = dict(H=_randn_bf16((B, d_model), g, device),
+                   W_kv=_randn_bf16((d_model, d), g, device, 1 / math.sqrt(d_model)),
+                   W_ik=_randn_bf16((d, d_ik), g, device, 1 / math.sqrt(d)),
+                   pos=torch.full((B,), N - 1, dtype=torch.int32, device=device),
+                   seq=torch.arange(B, dtype=torch.int32, device=device),
+                   entry=torch.full((B,), N - 1, dtype=torch.int32, device=device))
+        cos, sin = synth.rope_tables(N, d_rope)
+        rope = (torch.from_numpy(cos).to(device), torch.from_numpy(sin).to(device))
+    step = DecodeStep(cache, seq_of, n_vis, N, layers, NB, P, k, W, append=app, rope=rope)
+    info = dict(B=B, N=N, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq, W=W, k=k, NB=NB,
+                P=P, d_model=d_model, d_rope=d_rope)
+    return step, info
+
+
+def algorithmic_bytes(info):
+    """Bytes a decode step must move at minimum (each byte read or written once):
+
+    append     : H row (d_model*2) + W_kv + W_ik once (shared by the batch) + the new
+                 entry (d/2 + d/16 + 2*d_ik) per query
+    Full       : n*2*d_ik of indexer K + q_idx + w + pool (4*NB*P) + topk (4k) per query
+    Reindex    : pool*(2*d_ik) gathered indexer K + pool ids (4*NB*P) + q_idx + w + topk
+    attention  : k*(d/2 + d/16) FP4 rows + W*(d + 4) SWA rows + q (2*Hq*d)
+                 + out (2*Hq*d) + topk ids (4k) per query-layer
+    """
+    B, N, d, d_ik, H_i, Hq, W, k = (info[x] for x in ("B", "N", "d", "d_ik", "H_i", "Hq", "W", "k"))
+    pool = info["NB"] * info["P"]
+    per_q = {}
+    per_q["full"] = N * 2 * d_ik + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
+    per_q["reindex"] = min(N, pool) * 2 * d_ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
+    per_q["attn"] = k * (d // 2 + d // 16) + W * (d + 4) + 2 * Hq * d * 2 + 4 * k
+    tot = 0
+    for mode in info["schedule"]:
+        if mode == FULL:
+            tot += B * per_q["full"]
+        elif mode == REINDEX:
+            tot += B * per_q["reindex"]
+        tot += B * per_q["attn"]
+    app = 0
+    if info.get("append", True):
+        app = B * (info["d_model"] * 2 + d // 2 + d // 16 + 2 * d_ik) + info["d_model"] * d * 2 + d * d_ik * 2
+    return dict(total=tot + app, per_query=per_q, append=app)
+
+
+def host_sequence(step, b, n):
+    """Entries [0, n) of sequence b (codes, scales, idx_k bits) copied to the host."""
+    pt = step.cache.page_table[b].cpu().numpy()
+    e = np.arange(n)
+    pages = torch.from_numpy(pt[e // 64].astype(np.int64)).to(step.cache.codes.device)
+    slots = torch.from_numpy(e % 64).to(step.cache.codes.device)
+    codes = step.cache.codes[pages, slots].cpu().numpy()
+    scales = step.cache.scales[pages, slots].cpu().numpy()
+    idxk = step.cache.idx_k[pages, slots].view(torch.int16).cpu().numpy().view(np.uint16)
+    return codes, scales, idxk

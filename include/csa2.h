@@ -1,0 +1,257 @@
+/*
+ * csa2.h -- C ABI of the CSA2 attention hot path on one GB300 (sm_103a).
+ *
+ * CSA2 (Compressed Sparse Attention 2) as described for DeepSeek-V4.1-Flash:
+ *   hidden states -> non-overlapping compressor -> Main KV (FP4) -> Indexer K;
+ *   Indexer Q x Indexer K -> score -> Top-K; Main Q attends to the selected Main KV
+ *   plus the layer-local SWA KV.
+ * Sources: "DeepSeek-V4.1-Flash deep dive" (tanjunchen.github.io, 2026-09-13),
+ * sections 2, 3.1-3.4 and 6.3; "DeepSeek-V4.1-Flash paper reading" (inkeast, 2026-09-19)
+ * section 4.2.
+ *
+ * Conventions shared by every call
+ *   - Every pointer named "device" is a CUDA device pointer owned by the caller.  The
+ *     library never allocates, frees or keeps device memory between calls (except one
+ *     4-byte error word per device, see csa2_get_device_error).
+ *   - Every compute call is asynchronous on the given cudaStream_t (passed as void*;
+ *     NULL = legacy default stream) and never synchronises.
+ *   - Arguments are validated on the host before any launch; a failed check returns a
+ *     status and csa2_last_error_message() (thread-local) says why.  Nothing is
+ *     launched in that case.
+ *   - Values that only the device can see (page ids read from a page table, n_vis,
+ *     pool entries) are bounds-checked in the kernels: a bad value sets a bit in the
+ *     device error word and the access is skipped (the row reads as zeros / the entry
+ *     is ignored).  Kernels never trap.
+ *   - Argument structs begin with struct_size = sizeof(struct) for ABI versioning.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *
+ * Paged Main KV cache (one shared layout for the FP4 codes, the E4M3 scales and the
+ * bf16 indexer K): entry e of sequence s lives on page page_table[s*max_pages + e/64],
+ * slot e%64.  Each plane is an array of pages indexed by page id.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa2_status {
+  CSA2_OK = 0,
+  CSA2_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, inconsistent sizes */
+  CSA2_ERR_UNSUPPORTED_SHAPE = 2,  /* a size outside the supported set below */
+  CSA2_ERR_WORKSPACE_TOO_SMALL = 3,
+  CSA2_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
+  CSA2_ERR_DEVICE_CHECK = 5        /* the device error word was non-zero */
+} csa2_status;
+
+typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
+
+/* Device error word bits (csa2_get_device_error). */
+#define CSA2_DEVERR_PAGE_ID      0x1u  /* page id outside [0, num_pages) */
+#define CSA2_DEVERR_PAGE_SLOT    0x2u  /* entry index beyond max_pages*page_size */
+#define CSA2_DEVERR_N_VIS        0x4u  /* n_vis[b] outside [0, max_n] */
+#define CSA2_DEVERR_POOL_ENTRY   0x8u  /* pool_len[b] out of range */
+#define CSA2_DEVERR_SEQ          0x10u /* seq_of / seq index outside [0, num_seqs) */
+#define CSA2_DEVERR_SWA_RANGE    0x20u /* SWA window outside [0, swa_rows) */
+#define CSA2_DEVERR_POS          0x40u /* RoPE position outside [0, rope_max_pos) */
+
+#define CSA2_PAGE_SIZE 64
+
+/* Paged cache planes (all device).  d in {128, 512}; d_ik in {64, 128}. */
+typedef struct csa2_cache {
+  uint8_t* codes;              /* [num_pages][64][d/2]  E2M1 pairs, even channel in the low nibble */
+  uint8_t* scales;             /* [num_pages][64][d/16] E4M3 scale of each 16 channels */
+  uint16_t* idx_k;             /* [num_pages][64][d_ik] bf16 indexer K (may be NULL if unused) */
+  const int32_t* page_table;   /* [num_seqs][max_pages] page id of each 64-entry page */
+  int32_t num_pages;
+  int32_t page_size;           /* must be 64 */
+  int32_t num_seqs;
+  int32_t max_pages;
+  int32_t d;
+  int32_t d_ik;
+} csa2_cache;
+
+/* ------------------------------------------------------------------------------
+ * csa2_compress_quant -- the non-overlapping compressor and FP4 quantiser.
+ * deep dive section 2: C = H.W_KV, Z = H.W_Z; section 3.1: every m tokens become one
+ * Main KV entry (no overlap, no absolute PE) and Indexer K is projected from Main KV;
+ * section 3.4: RoPE, then FP4 E2M1 with one E4M3 scale per 16 channels.
+ *
+ * For each group g of m consecutive input rows [g*m, g*m+m):
+ *   e[c]  = sum_j softmax_j(Z[g*m+j][c]) * C[g*m+j][c]        (float32)
+ *   y     = RoPE(e) on the last d_rope channels: pair i = channels
+ *           (d-d_rope+2i, d-d_rope+2i+1), angle from rope_cos/rope_sin[pos[g]][i],
+ *           y0 = x0*c - x1*s, y1 = x0*s + x1*c, each product rounded (no FMA)
+ *   per 16 channels: s = E4M3_RNE_satfinite(amax/6); codes = E2M1_RNE_sat(y/s)
+ *           (float32 divisions, correctly rounded; s == 0 gives zero codes)
+ *   idx_k = bf16_RNE(dequant(codes, s) . W_ik)                  (if W_ik != NULL)
+ * and writes entry entry[g] of sequence seq[g] through the page table.
+ *
+ * Modes:
+ *   projection: W_kv != NULL.  H is [T][d_model] (h_dtype bf16 or f32), W_kv and W_z
+ *               are bf16 [d_model][d] (W_z may be NULL when m == 1).  C and Z are
+ *               computed in float32 into the workspace.
+ *   given:      W_kv == NULL.  C (and Z when m > 1) are float32 [T][d] device arrays.
+ * Supported: m in 1..8, d in {128, 512}, d_ik in {64, 128}, d_rope in {0, 32, 64},
+ * d_rope <= d, d_model % 32 == 0, T % m == 0.
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_compress_args {
+  size_t struct_size;
+  int32_t T;                   /* input rows */
+  int32_t m;                   /* compression ratio */
+  int32_t d_model;             /* projection mode only */
+  csa2_dtype h_dtype;          /* projection mode only */
+  const void* H;               /* device [T][d_model] */
+  const uint16_t* W_kv;        /* device bf16 [d_model][d], NULL = given mode */
+  const uint16_t* W_z;         /* device bf16 [d_model][d] */
+  const float* C;              /* device f32 [T][d] (given mode) */
+  const float* Z;              /* device f32 [T][d] (given mode, m > 1) */
+  int32_t d_rope;              /* 0 disables RoPE */
+  int32_t rope_max_pos;        /* rows of the tables */
+  const float* rope_cos;       /* device f32 [rope_max_pos][d_rope/2] */
+  const float* rope_sin;       /* device f32 [rope_max_pos][d_rope/2] */
+  const int32_t* pos;          /* device [T/m] RoPE position of each group */
+  const int32_t* seq;          /* device [T/m] destination sequence of each group */
+  const int32_t* entry;        /* device [T/m] destination entry index of each group */
+  const uint16_t* W_ik;        /* device bf16 [d][d_ik], NULL = do not write idx_k */
+  csa2_cache cache;            /* destination planes */
+  float* y_out;                /* device f32 [T/m][d] pre-quantisation rows, or NULL */
+} csa2_compress_args;
+
+csa2_status csa2_compress_quant(const csa2_compress_args* args, void* workspace,
+                                size_t workspace_bytes, void* stream);
+csa2_status csa2_compress_quant_workspace(const csa2_compress_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * csa2_index_full -- Full-mode hierarchical sparse indexer.
+ * deep dive 3.3: the first Full indexer scans the whole causally visible range, keeps
+ * the best positions of each block; 2,048 blocks x 8 = a 16,384-candidate shared pool;
+ * Top-512 per query.  deep dive 3.1: Indexer Q x Indexer K -> score -> Top-K.
+ *
+ * For query b over the visible entries [0, n = n_vis[b]) of sequence seq_of[b]:
+ *   s(e)  = sum_h w[b][h] * ReLU(q_idx[b][h] . idx_k[e])   (relu = 0: no ReLU)
+ *   block j = [floor(j*n/NB), floor((j+1)*n/NB)), keep the best min(per_block, len),
+ *   pool  = union of the kept entries, ascending; pool_len = min(n, NB*per_block);
+ *   topk  = best min(k, pool_len) entries of the pool, ascending.
+ * "Best" = larger score; equal scores go to the lower entry index.
+ * Outputs (device): pool [B][NB*per_block] and topk [B][k], -1 padded; pool_len,
+ * topk_len [B].  Scores are float32 on the device.
+ * Supported: H_i in 1..32, d_ik in {64, 128}, per_block in 1..32, NB*per_block <= 16384,
+ * k in 1..2048, max_n <= max_pages*64.
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_index_full_args {
+  size_t struct_size;
+  int32_t B;
+  int32_t H_i;
+  const uint16_t* q_idx;       /* device bf16 [B][H_i][d_ik] */
+  const float* w;              /* device f32 [B][H_i] */
+  csa2_cache cache;            /* idx_k + page_table */
+  const int32_t* seq_of;       /* device [B] */
+  const int32_t* n_vis;        /* device [B] visible entries per query */
+  int32_t max_n;               /* host bound: every n_vis[b] <= max_n */
+  int32_t num_blocks;          /* NB */
+  int32_t per_block;
+  int32_t k;
+  int32_t relu;
+  int32_t* pool;               /* device [B][NB*per_block] */
+  int32_t* pool_len;           /* device [B] */
+  int32_t* topk;               /* device [B][k] */
+  int32_t* topk_len;           /* device [B] */
+} csa2_index_full_args;
+
+csa2_status csa2_index_full(const csa2_index_full_args* args, void* workspace,
+                            size_t workspace_bytes, void* stream);
+csa2_status csa2_index_full_workspace(const csa2_index_full_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * csa2_index_reindex -- Reindex mode (deep dive 3.2, 3.3 step 3): this layer's own
+ * indexer Q re-scores only the shared pool (entries of the cache built by the Full
+ * layer) and picks its own Top-k.  Same score and ordering rules as csa2_index_full.
+ * pool: [B][pool_stride] ascending entry indices, the first pool_len[b] valid.
+ * Reuse mode (deep dive 3.2) needs no call: pass the previous topk to csa2_sparse_attn.
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_index_reindex_args {
+  size_t struct_size;
+  int32_t B;
+  int32_t H_i;
+  const uint16_t* q_idx;       /* device bf16 [B][H_i][d_ik] */
+  const float* w;              /* device f32 [B][H_i] */
+  csa2_cache cache;
+  const int32_t* seq_of;       /* device [B] */
+  const int32_t* pool;         /* device [B][pool_stride] */
+  const int32_t* pool_len;     /* device [B] */
+  int32_t pool_stride;         /* <= 16384 */
+  int32_t k;
+  int32_t relu;
+  int32_t* topk;               /* device [B][k] */
+  int32_t* topk_len;           /* device [B] */
+} csa2_index_reindex_args;
+
+csa2_status csa2_index_reindex(const csa2_index_reindex_args* args, void* workspace,
+                               size_t workspace_bytes, void* stream);
+csa2_status csa2_index_reindex_workspace(const csa2_index_reindex_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * csa2_sparse_attn -- one softmax over the selected FP4 Main KV entries plus the
+ * layer-local FP8 SWA window (deep dive 3.1; 6.3: 64 query heads x 512, n_win 128,
+ * Top-K 512).  The entry vector is both key and value (MQA over the shared entry).
+ *
+ * For query b and head h, S = { topk[b][i] : i < topk_len[b], topk[b][i] >= 0 }
+ *   U { SWA rows swa_start[b] .. swa_start[b]+swa_len[b]-1 }:
+ *   l_s = softmax_scale * q[b][h] . kv_s;  p = softmax_S(l);  out[b][h] = sum_s p_s kv_s
+ *   kv_s = dequant FP4 entry (exact) or E4M3 row * swa_scale[row].
+ *   lse[b][h] = log(sum_s exp(l_s)) (natural log); empty S gives out = 0, lse = -inf.
+ * The GPU computes the products in fp16 tensor-core MMAs with float32 accumulation
+ * (FP4 and E4M3 values are exact in fp16; the SWA row scale and q are rounded to
+ * fp16; |q| and |kv| must stay below 65504).
+ * Supported: Hq in {8, 16, 32, 64}, d in {128, 512}, k + swa_max <= 4096.
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_attn_args {
+  size_t struct_size;
+  int32_t B;
+  int32_t Hq;
+  const uint16_t* q;           /* device bf16 [B][Hq][d] */
+  csa2_cache cache;            /* codes, scales, page_table, d */
+  const int32_t* seq_of;       /* device [B] */
+  const int32_t* topk;         /* device [B][k] */
+  const int32_t* topk_len;     /* device [B], or NULL = all k slots */
+  int32_t k;
+  const uint8_t* swa;          /* device E4M3 [swa_rows][d] (may be NULL if swa_max == 0) */
+  const float* swa_scale;      /* device f32 [swa_rows] */
+  int32_t swa_rows;
+  const int32_t* swa_start;    /* device [B] */
+  const int32_t* swa_len;      /* device [B] */
+  int32_t swa_max;             /* host bound: every swa_len[b] <= swa_max */
+  float softmax_scale;
+  void* out;                   /* device [B][Hq][d] */
+  csa2_dtype out_dtype;
+  float* lse;                  /* device f32 [B][Hq], or NULL */
+} csa2_attn_args;
+
+csa2_status csa2_sparse_attn(const csa2_attn_args* args, void* workspace,
+                             size_t workspace_bytes, void* stream);
+csa2_status csa2_sparse_attn_workspace(const csa2_attn_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * Helpers
+ * -------------------------------------------------------------------------- */
+
+/* Thread-local description of the last failed call ("" if none). */
+const char* csa2_last_error_message(void);
+
+/* Synchronises the current device, returns the device error word (CSA2_DEVERR_* bits)
+ * accumulated since the last read, and clears it.  For tests and debugging: it blocks. */
+csa2_status csa2_get_device_error(uint32_t* word);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA2_H */

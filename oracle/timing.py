@@ -1,0 +1,81 @@
+"""Times the CPU oracle on a bounded sample of a decode workload (the CPU baseline).
+
+Test infrastructure (see oracle/__init__.py): run only by the benchmark's cpu_baseline
+and --impl reference legs.  Inputs come from the seeded generator on the host with the
+workload's shapes: each sampled query owns one sequence of N entries, and one "step"
+is that query's append (compressor, m = 1) plus the 20-layer decoder schedule.
+
+Usage: python -m oracle.timing --N 131072 --queries 2 [--json]
+"""
+import argparse
+import json
+import os
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from fp4_compressed_sparse_02_gb300 import synth  # noqa: E402  (input generator only)
+from oracle import compress, formats, schedule  # noqa: E402
+
+
+def make_query(r, N, cfg):
+    d, d_ik, H_i, Hq, W, d_model = (cfg[x] for x in ("d", "d_ik", "H_i", "Hq", "W", "d_model"))
+    codes = synth.fp4_codes(r, (N,), d)
+    scales = synth.fp4_scales(r, (N,), d)
+    K = formats.bf16_value(synth.bf16_normal(r, (N, d_ik)))
+    layers = []
+    for mode in schedule.decoder_schedule():
+        L = dict(mode=mode, q=formats.bf16_value(synth.bf16_normal(r, (Hq, d))),
+                 swa_rows=synth.fp8_rows(r, W, d), swa_scale=synth.fp8_row_scales(r, W), swa_start=0, swa_len=W)
+        if mode != "reuse":
+            L["q_idx"] = formats.bf16_value(synth.bf16_normal(r, (H_i, d_ik)))
+            L["w"] = synth.f32_normal(r, (H_i,), 1 / np.sqrt(H_i)).astype(np.float64)
+        layers.append(L)
+    H = formats.bf16_value(synth.bf16_normal(r, (1, d_model)))
+    Wkv = formats.bf16_value(synth.bf16_normal(r, (d_model, d), 1 / np.sqrt(d_model)))
+    Wik = formats.bf16_value(synth.bf16_normal(r, (d, d_ik), 1 / np.sqrt(d)))
+    cos, sin = synth.rope_tables(N, cfg["d_rope"])
+    return dict(codes=codes, scales=scales, K=K, layers=layers, H=H, Wkv=Wkv, Wik=Wik, cos=cos, sin=sin)
+
+
+def run_query(x, N, cfg):
+    """One query-step: append entry N-1 from H, then the 20 decoder layers."""
+    app = compress.compress_quant_from_hidden(x["H"], x["Wkv"], None, 1, np.array([N - 1]), x["cos"], x["sin"],
+                                              cfg["d_rope"], x["Wik"])
+    x["codes"][N - 1] = app["codes"][0]
+    x["scales"][N - 1] = app["scales"][0]
+    x["K"][N - 1] = formats.bf16_value(app["idx_k"][0])
+    return schedule.decode_step(x["layers"], x["K"], x["codes"], x["scales"], cfg["NB"], cfg["P"], cfg["k"],
+                                1 / np.sqrt(cfg["d"]))
+
+
+def time_sample(N, queries, cfg, seed=0):
+    r = np.random.default_rng(seed)
+    xs = [make_query(r, N, cfg) for _ in range(queries)]
+    t0 = time.perf_counter()
+    for x in xs:
+        run_query(x, N, cfg)
+    dt = time.perf_counter() - t0
+    layers = len(schedule.decoder_schedule())
+    return dict(seconds=dt, query_layers=queries * layers, value=queries * layers / dt)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--N", type=int, default=131072)
+    ap.add_argument("--queries", type=int, default=2)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--config", default="DEC128K")
+    a = ap.parse_args()
+    cfg = dict(getattr(synth, a.config))
+    res = time_sample(a.N, a.queries, cfg, a.seed)
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,107 @@
+"""Comparison rules for GPU-vs-oracle parity.
+
+  * FP4 codes / scales, given identical float32 rows: bit-exact.
+  * FP4 codes / scales from a float32 GPU pipeline vs the float64 oracle: equal except
+    where the oracle's a/6 or y/s lies within 1e-5 (relative) of a rounding midpoint.
+  * Index sets: equal except for swaps at a selection boundary between entries whose
+    oracle scores differ by <= 1e-5 relative (to the larger magnitude, with a floor of
+    1e-5 x the largest |score| among the candidates for scores near zero).
+  * Attention: relative L2 <= 2e-3 and max-abs <= 1e-2 against the float64 oracle.
+"""
+import numpy as np
+import torch
+
+from oracle import formats
+
+REL_TIE = 1e-5
+ATTN_REL_L2 = 2e-3
+ATTN_MAX_ABS = 1e-2
+
+
+def to_dev(a, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(device)
+
+
+def bf16_dev(bits, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def bf16_host_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def paged_to_logical(plane, page_table, seq, n):
+    """Entries [0, n) of sequence seq from a paged plane [pages, 64, w] (numpy)."""
+    e = np.arange(n)
+    pages = page_table[seq, e // 64]
+    return plane[pages, e % 64]
+
+
+def logical_to_paged(rows_per_seq, page_table, num_pages, width, dtype):
+    plane = np.zeros((num_pages, 64, width), dtype=dtype)
+    for s, rows in enumerate(rows_per_seq):
+        e = np.arange(len(rows))
+        plane[page_table[s, e // 64], e % 64] = rows
+    return plane
+
+
+def check_index_set(gpu, ref, score_of, what=""):
+    """gpu, ref: ascending entry arrays (no -1).  score_of: dict-like entry -> oracle
+    score.  Returns the number of tolerated swaps; raises on any other difference."""
+    gpu = np.asarray(gpu)
+    ref = np.asarray(ref)
+    assert len(gpu) == len(ref), f"{what}: size {len(gpu)} vs {len(ref)}"
+    assert len(np.unique(gpu)) == len(gpu), f"{what}: duplicate entries"
+    assert (np.diff(gpu) > 0).all(), f"{what}: not ascending"
+    only_g = np.setdiff1d(gpu, ref)
+    only_r = np.setdiff1d(ref, gpu)
+    if len(only_g) == 0:
+        return 0
+    sg = np.sort(np.array([score_of(e) for e in only_g]))[::-1]
+    sr = np.sort(np.array([score_of(e) for e in only_r]))[::-1]
+    floor = REL_TIE * max(1e-30, max(np.abs(sg).max(), np.abs(sr).max()))
+    for a, b in zip(sg, sr):
+        tol = REL_TIE * max(abs(a), abs(b)) + floor
+        assert abs(a - b) <= tol, f"{what}: swap of scores {a!r} vs {b!r} exceeds the near-tie rule"
+    return len(only_g)
+
+
+def near_midpoint(x, grid, rel=REL_TIE):
+    """True where |x| lies within rel of a midpoint of the ascending magnitude grid."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    mids = (grid[1:] + grid[:-1]) / 2
+    i = np.clip(np.searchsorted(mids, x), 1, len(mids) - 1)
+    near = np.minimum(np.abs(x - mids[i - 1]), np.abs(x - mids[np.minimum(i, len(mids) - 1)]))
+    return near <= rel * np.maximum(x, 1e-30)
+
+
+def fp4_mismatch_is_tolerated(y_oracle, codes_g, scales_g, codes_o, scales_o):
+    """Per 16-channel group: a mismatching group is tolerated only if the oracle's a/6 is
+    near an E4M3 midpoint, or (same scale) every mismatching code's y/s is near an E2M1
+    midpoint.  Returns (n_mismatched_groups, n_tolerated)."""
+    y = np.asarray(y_oracle, dtype=np.float32)
+    G, d = y.shape
+    cg = formats.fp4_unpack(codes_g).reshape(G, d // 16, 16)
+    co = formats.fp4_unpack(codes_o).reshape(G, d // 16, 16)
+    bad = (scales_g != scales_o) | (cg != co).any(-1)
+    e4 = formats.e4m3_value(np.arange(0x7F))
+    e2 = formats.e2m1_value(np.arange(8))
+    yg = y.reshape(G, d // 16, 16)
+    tol = 0
+    for gi, qi in zip(*np.nonzero(bad)):
+        a = np.abs(yg[gi, qi]).max()
+        if scales_g[gi, qi] != scales_o[gi, qi]:
+            ok = near_midpoint(np.float32(a) / np.float32(6.0), e4).item()
+        else:
+            s = np.float32(formats.e4m3_value(scales_o[gi, qi]))
+            diff = cg[gi, qi] != co[gi, qi]
+            ok = bool(near_midpoint((yg[gi, qi] / s)[diff], e2).all())
+        tol += int(ok)
+    return int(bad.sum()), tol
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)

@@ -1,0 +1,132 @@
+"""GPU parity of csa2_sparse_attn against the oracle attention, on identical FP4 caches,
+SWA rows and index sets (drawn by the input generator)."""
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_sparse_02_gb300 import csa2, synth
+from oracle import attention, formats
+from parity_utils import ATTN_MAX_ABS, ATTN_REL_L2, bf16_dev, logical_to_paged, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(r, B, Hq, d, k, W, n, ns=2, fill=0.9):
+    mp = (n + 63) // 64
+    pt = synth.page_table(r, ns, mp)
+    codes = [synth.fp4_codes(r, (n,), d) for _ in range(ns)]
+    scales = [synth.fp4_scales(r, (n,), d) for _ in range(ns)]
+    cache = csa2.PagedCache.allocate(ns, n, d, 0, "cuda", torch.from_numpy(pt))
+    cache.codes.copy_(to_dev(logical_to_paged(codes, pt, ns * mp, d // 2, np.uint8)))
+    cache.scales.copy_(to_dev(logical_to_paged(scales, pt, ns * mp, d // 16, np.uint8)))
+    seq_of = (np.arange(B) % ns).astype(np.int32)
+    topk = np.full((B, k), -1, dtype=np.int32)
+    tlen = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        cnt = min(n, max(0, int(k * fill) if b % 3 else k))
+        sel = synth.sorted_distinct(r, n, cnt)
+        topk[b, :len(sel)] = sel
+        tlen[b] = len(sel)
+    rows = B * W + 7
+    swa = synth.fp8_rows(r, rows, d)
+    swa_scale = synth.fp8_row_scales(r, rows)
+    swa_start = (np.arange(B) * W + 3).astype(np.int32)
+    swa_len = np.full(B, W, dtype=np.int32)
+    q = synth.bf16_normal(r, (B, Hq, d))
+    return dict(cache=cache, codes=codes, scales=scales, seq_of=seq_of, topk=topk, tlen=tlen, swa=swa,
+                swa_scale=swa_scale, swa_start=swa_start, swa_len=swa_len, q=q, W=W)
+
+
+def _run(c, out_dtype=torch.float32, use_tlen=True):
+    out, lse = csa2.sparse_attn(c["cache"], bf16_dev(c["q"]), to_dev(c["seq_of"]), to_dev(c["topk"]),
+                                to_dev(c["tlen"]) if use_tlen else None, to_dev(c["swa"]), to_dev(c["swa_scale"]),
+                                to_dev(c["swa_start"]), to_dev(c["swa_len"]), c["W"], out_dtype=out_dtype)
+    assert csa2.device_error() == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _oracle(c):
+    B, Hq, d = c["q"].shape
+    outs, lses = [], []
+    for b in range(B):
+        s = c["seq_of"][b]
+        o, l = attention.sparse_attention(formats.bf16_value(c["q"][b]), c["codes"][s], c["scales"][s],
+                                          c["topk"][b, :c["tlen"][b]], c["swa"], c["swa_scale"],
+                                          int(c["swa_start"][b]), int(c["swa_len"][b]), 1 / np.sqrt(d))
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def _assert_close(got, ref):
+    assert rel_l2(got, ref) <= ATTN_REL_L2, rel_l2(got, ref)
+    assert np.abs(got - ref).max() <= ATTN_MAX_ABS
+
+
+@pytest.mark.parametrize("B,Hq,d,k,W", [(5, 64, 512, 512, 128), (7, 8, 128, 64, 32), (3, 16, 512, 256, 64),
+                                        (4, 32, 128, 200, 100), (2, 64, 128, 512, 128)])
+def test_attn_parity(B, Hq, d, k, W):
+    r = np.random.default_rng(B * 1000 + Hq + d + k + W)
+    c = _case(r, B, Hq, d, k, W, n=3000)
+    out, lse = _run(c)
+    ref, rlse = _oracle(c)
+    _assert_close(out, ref)
+    np.testing.assert_allclose(lse, rlse, rtol=1e-4, atol=1e-4)
+
+
+def test_attn_bf16_output_and_determinism():
+    r = np.random.default_rng(50)
+    c = _case(r, 4, 64, 512, 512, 128, n=5000)
+    o1, _ = _run(c, torch.bfloat16)
+    o2, _ = _run(c, torch.bfloat16)
+    np.testing.assert_array_equal(o1, o2)          # Reuse = the same call again: identical
+    ref, _ = _oracle(c)
+    assert rel_l2(o1, ref) <= ATTN_REL_L2 + 4e-3     # bf16 output rounding (2^-9) on top
+    assert np.abs(o1 - ref).max() <= ATTN_MAX_ABS + 1e-2
+
+
+def test_attn_empty_and_one_sided():
+    r = np.random.default_rng(51)
+    c = _case(r, 4, 64, 512, 512, 128, n=2000)
+    c["tlen"][0] = 0
+    c["swa_len"][0] = 0            # nothing to attend: out 0, lse -inf
+    c["tlen"][1] = 0               # window only
+    c["swa_len"][2] = 0            # selection only
+    c["topk"][3, ::3] = -1         # holes inside the valid prefix are skipped
+    out, lse = _run(c)
+    ref, rlse = _oracle(c)
+    assert (out[0] == 0).all() and np.isneginf(lse[0]).all()
+    _assert_close(out[1:], ref[1:])
+    np.testing.assert_allclose(lse[1:], rlse[1:], rtol=1e-4, atol=1e-4)
+
+
+def test_attn_without_topk_len_reads_all_slots():
+    r = np.random.default_rng(52)
+    c = _case(r, 3, 64, 512, 512, 128, n=4000, fill=0.5)
+    out, _ = _run(c, use_tlen=False)
+    ref, _ = _oracle(c)
+    _assert_close(out, ref)
+
+
+def test_attn_single_key_returns_its_row():
+    r = np.random.default_rng(53)
+    c = _case(r, 2, 64, 512, 512, 128, n=1000)
+    c["topk"][:] = -1
+    c["topk"][:, 0] = [17, 900]
+    c["tlen"][:] = 1
+    c["swa_len"][:] = 0
+    out, lse = _run(c)
+    for b in range(2):
+        row = formats.fp4_dequantize(c["codes"][c["seq_of"][b]][c["topk"][b, 0]],
+                                     c["scales"][c["seq_of"][b]][c["topk"][b, 0]])
+        np.testing.assert_allclose(out[b], np.tile(row, (64, 1)), rtol=1e-6, atol=1e-6)
+
+
+def test_swa_window_outside_rows_is_flagged():
+    r = np.random.default_rng(54)
+    c = _case(r, 2, 8, 128, 64, 32, n=500)
+    c["swa_start"][1] = c["swa"].shape[0] - 5       # window runs past the last row
+    _run_noerr = csa2.sparse_attn(c["cache"], bf16_dev(c["q"]), to_dev(c["seq_of"]), to_dev(c["topk"]),
+                                  to_dev(c["tlen"]), to_dev(c["swa"]), to_dev(c["swa_scale"]),
+                                  to_dev(c["swa_start"]), to_dev(c["swa_len"]), c["W"])
+    assert csa2.device_error() & 0x20

@@ -1,0 +1,174 @@
+"""GPU parity of csa2_index_full / csa2_index_reindex against the oracle indexer, on
+identical indexer-K caches (drawn by the input generator)."""
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_sparse_02_gb300 import csa2, synth
+from oracle import formats, indexer
+from parity_utils import bf16_dev, check_index_set, logical_to_paged, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(r, ns, n_max, d_ik, H_i, B, sigma=1.0):
+    """ns sequences of n_max entries of random bf16 indexer K, paged through a random
+    page table; B queries with random q / w."""
+    mp = (n_max + 63) // 64
+    pt = synth.page_table(r, ns, mp)
+    K = [synth.bf16_normal(r, (n_max, d_ik), sigma) for _ in range(ns)]
+    plane = logical_to_paged(K, pt, ns * mp, d_ik, np.uint16)
+    cache = csa2.PagedCache.allocate(ns, n_max, 512, d_ik, "cuda", torch.from_numpy(pt))
+    cache.idx_k.copy_(bf16_dev(plane))
+    q = synth.bf16_normal(r, (B, H_i, d_ik))
+    w = synth.f32_normal(r, (B, H_i), 1 / np.sqrt(H_i))
+    return cache, K, q, w
+
+
+def _run_full(cache, q, w, seq_of, n_vis, NB, P, k, relu=True):
+    pool, plen, topk, tlen = csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(n_vis),
+                                             int(n_vis.max()), NB, P, k, relu)
+    assert csa2.device_error() == 0
+    return pool.cpu().numpy(), plen.cpu().numpy(), topk.cpu().numpy(), tlen.cpu().numpy()
+
+
+def _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got, relu=True):
+    pool, plen, topk, tlen = got
+    swaps = 0
+    for b in range(len(n_vis)):
+        n = int(n_vis[b])
+        Kb = formats.bf16_value(K[seq_of[b]][:n])
+        rpool, rtopk, s = indexer.full(formats.bf16_value(q[b]), w[b], Kb, NB, P, k, relu)
+        assert plen[b] == len(rpool)
+        assert tlen[b] == len(rtopk)
+        assert (pool[b, plen[b]:] == -1).all() and (topk[b, tlen[b]:] == -1).all()
+        gp = pool[b, :plen[b]]
+        bb = indexer.block_bounds(n, NB)
+        score = lambda e: s[e]
+        if n >= NB * P:
+            for j in range(NB):
+                seg = gp[P * j:P * j + P]
+                assert ((seg >= bb[j]) & (seg < bb[j + 1])).all(), f"query {b} block {j} out of range"
+                rseg = rpool[P * j:P * j + P]
+                swaps += check_index_set(seg, rseg, score, f"q{b} block {j}")
+        else:
+            np.testing.assert_array_equal(gp, rpool)
+        swaps += check_index_set(topk[b, :tlen[b]], rtopk, score, f"q{b} topk")
+    return swaps
+
+
+@pytest.mark.parametrize("relu", [True, False])
+def test_full_tiny_geometry_ragged(relu):
+    r = np.random.default_rng(1 + relu)
+    NB, P, k, d_ik, H_i = 64, 8, 64, 64, 4
+    n_vis = np.array([0, 1, 5, 63, 64, 300, 512, 513, 4096, 4097, 9001, 20011], dtype=np.int32)
+    B = len(n_vis)
+    cache, K, q, w = _setup(r, 3, int(n_vis.max()), d_ik, H_i, B)
+    seq_of = (np.arange(B) % 3).astype(np.int32)
+    got = _run_full(cache, q, w, seq_of, n_vis, NB, P, k, relu)
+    swaps = _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got, relu)
+    assert swaps <= 4
+
+
+def test_full_pages_geometry():
+    r = np.random.default_rng(3)
+    NB, P, k, d_ik, H_i = 2048, 8, 512, 128, 8
+    n_vis = np.array([16384, 20000, 50001, 1000, 131072 // 2 + 7, 16383, 600, 100000], dtype=np.int32)
+    B = len(n_vis)
+    cache, K, q, w = _setup(r, 2, int(n_vis.max()), d_ik, H_i, B)
+    seq_of = (np.arange(B) % 2).astype(np.int32)
+    got = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    swaps = _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got)
+    assert swaps <= 8
+    assert (got[1][n_vis >= NB * P] == NB * P).all()        # pool fixed at 16,384
+
+
+@pytest.mark.parametrize("H_i", [1, 8, 12, 32])
+def test_full_head_counts(H_i):
+    r = np.random.default_rng(10 + H_i)
+    NB, P, k = 256, 8, 128
+    n_vis = np.array([5000, 2048, 777], dtype=np.int32)
+    cache, K, q, w = _setup(r, 1, 5000, 128, H_i, 3)
+    seq_of = np.zeros(3, np.int32)
+    got = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 4
+
+
+def test_exact_ties_break_to_lower_index():
+    # a cache of only three distinct rows: scores tie exactly in large groups, so the
+    # selection must follow the lower-index rule bit for bit.
+    r = np.random.default_rng(20)
+    NB, P, k, d_ik, H_i = 128, 8, 200, 128, 8
+    n = 5000
+    cache, _, q, w = _setup(r, 1, n, d_ik, H_i, 2)
+    rows = synth.bf16_normal(r, (3, d_ik))
+    K = rows[r.integers(0, 3, n)]
+    pt = cache.page_table.cpu().numpy()
+    cache.idx_k.copy_(bf16_dev(logical_to_paged([K], pt, cache.num_pages, d_ik, np.uint16)))
+    n_vis = np.array([n, 3000], dtype=np.int32)
+    seq_of = np.zeros(2, np.int32)
+    pool, plen, topk, tlen = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    for b in range(2):
+        rpool, rtopk, s = indexer.full(formats.bf16_value(q[b]), w[b], formats.bf16_value(K[:n_vis[b]]), NB, P, k)
+        np.testing.assert_array_equal(pool[b, :plen[b]], rpool)
+        np.testing.assert_array_equal(topk[b, :tlen[b]], rtopk)
+
+
+def test_reindex_matches_oracle():
+    r = np.random.default_rng(30)
+    NB, P, k, d_ik, H_i = 2048, 8, 512, 128, 8
+    n_vis = np.array([40000, 16384, 9000, 70000], dtype=np.int32)
+    B = len(n_vis)
+    cache, K, q_full, w_full = _setup(r, 4, int(n_vis.max()), d_ik, H_i, B)
+    seq_of = np.arange(B, dtype=np.int32)
+    stride = NB * P
+    pools = np.full((B, stride), -1, dtype=np.int32)
+    plen = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        rp, _, _ = indexer.full(formats.bf16_value(q_full[b]), w_full[b], formats.bf16_value(K[b][:n_vis[b]]),
+                                NB, P, k)
+        pools[b, :len(rp)] = rp
+        plen[b] = len(rp)
+    q = synth.bf16_normal(r, (B, H_i, d_ik))
+    w = synth.f32_normal(r, (B, H_i), 1 / np.sqrt(H_i))
+    topk, tlen = csa2.index_reindex(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(pools), to_dev(plen), k)
+    assert csa2.device_error() == 0
+    topk, tlen = topk.cpu().numpy(), tlen.cpu().numpy()
+    swaps = 0
+    for b in range(B):
+        Kb = formats.bf16_value(K[b])
+        rt, rs = indexer.reindex(formats.bf16_value(q[b]), w[b], Kb, pools[b, :plen[b]], k)
+        assert tlen[b] == len(rt)
+        s_all = indexer.scores(formats.bf16_value(q[b]), w[b], Kb[pools[b, :plen[b]]])
+        smap = dict(zip(pools[b, :plen[b]].tolist(), s_all.tolist()))
+        swaps += check_index_set(topk[b, :tlen[b]], rt, lambda e: smap[e], f"reindex q{b}")
+        assert set(topk[b, :tlen[b]].tolist()) <= set(pools[b, :plen[b]].tolist())
+    assert swaps <= 4
+
+
+def test_reindex_short_pools():
+    r = np.random.default_rng(31)
+    d_ik, H_i, k = 64, 4, 64
+    cache, K, q, w = _setup(r, 1, 3000, d_ik, H_i, 3)
+    pools = np.full((3, 512), -1, dtype=np.int32)
+    plen = np.array([0, 40, 512], dtype=np.int32)
+    pools[1, :40] = synth.sorted_distinct(r, 3000, 40)
+    pools[2] = synth.sorted_distinct(r, 3000, 512)
+    seq_of = np.zeros(3, np.int32)
+    topk, tlen = csa2.index_reindex(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(pools), to_dev(plen), k)
+    topk, tlen = topk.cpu().numpy(), tlen.cpu().numpy()
+    assert tlen.tolist() == [0, 40, 64]
+    assert (topk[0] == -1).all()
+    np.testing.assert_array_equal(topk[1, :40], pools[1, :40])
+    Kb = formats.bf16_value(K[0])
+    rt, _ = indexer.reindex(formats.bf16_value(q[2]), w[2], Kb, pools[2], k)
+    s_all = indexer.scores(formats.bf16_value(q[2]), w[2], Kb)
+    check_index_set(topk[2], rt, lambda e: s_all[e], "short pool")
+
+
+def test_n_vis_beyond_max_n_is_flagged():
+    r = np.random.default_rng(40)
+    cache, K, q, w = _setup(r, 1, 1000, 64, 4, 1)
+    n_vis = np.array([1000], dtype=np.int32)
+    csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(np.zeros(1, np.int32)), to_dev(n_vis), 900, 64, 8, 64)
+    assert csa2.device_error() & 0x4
