@@ -181,6 +181,21 @@ csa2_status csa2_index_full(const csa2_index_full_args* a, void* ws, size_t ws_b
   return cuda_status(csa2::launch_index_full(*a, ws, static_cast<cudaStream_t>(stream)), "csa2_index_full");
 }
 
+csa2_status csa2_index_full_noalloc(const csa2_index_full_args* a, void* stream) {
+  csa2_status s = check_full(a);
+  if (s != CSA2_OK) return s;
+  const long long need = (long long)a->B * a->num_blocks * a->per_block;
+  REQUIRE(need <= CSA2_NOALLOC_MAX_SCORES, CSA2_ERR_UNSUPPORTED_SHAPE,
+          "csa2_index_full_noalloc: B*num_blocks*per_block = %lld exceeds the fixed scratch of %d scores",
+          need, CSA2_NOALLOC_MAX_SCORES);
+  void* scratch = nullptr;
+  size_t have = 0;
+  cudaError_t e = csa2::index_noalloc_scratch(&scratch, &have);
+  if (e != cudaSuccess) return cuda_status(e, "csa2_index_full_noalloc: scratch address lookup");
+  return cuda_status(csa2::launch_index_full(*a, scratch, static_cast<cudaStream_t>(stream)),
+                     "csa2_index_full_noalloc");
+}
+
 csa2_status csa2_index_reindex_workspace(const csa2_index_reindex_args* a, size_t* bytes) {
   csa2_status s = check_reindex(a);
   if (s != CSA2_OK) return s;

@@ -13,6 +13,8 @@
 // operands, so the k-slots of the fragment are mapped to the dims each thread loads
 // contiguously (32j + 8c + [0, 8) for lane c of a row quad).  The indexer Q of the query
 // is loaded with the same mapping once per warp.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -476,6 +478,36 @@ cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cud
   sel.topk_len = a.topk_len;
   k_select<<<a.B, SEL_THREADS, 0, st>>>(sel);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// Fixed scratch for csa2_index_full_noalloc: the pool scores live in this array
+// instead of a caller workspace.  Host code cannot use the symbol as a device address,
+// so the address is looked up once per device with that device current.
+// ---------------------------------------------------------------------------------
+static __device__ __align__(256) float g_noalloc_scores[CSA2_NOALLOC_MAX_SCORES];
+
+namespace {
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t index_noalloc_scratch(void** ptr, size_t* bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = p;
+  }
+  *ptr = g_noalloc_addr[dev];
+  *bytes = sizeof(g_noalloc_scores);
+  return cudaSuccess;
 }
 
 uint32_t read_clear_error_index() {

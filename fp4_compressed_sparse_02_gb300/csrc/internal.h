@@ -20,6 +20,9 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
 size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a);
 cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st);
 uint32_t read_clear_error_index();
+// device address of the fixed score array used by csa2_index_full_noalloc on the
+// current device (looked up once per device)
+cudaError_t index_noalloc_scratch(void** ptr, size_t* bytes);
 
 // attn.cu
 size_t attn_workspace_bytes(const csa2_attn_args& a);

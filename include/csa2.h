@@ -12,7 +12,8 @@
  * Conventions shared by every call
  *   - Every pointer named "device" is a CUDA device pointer owned by the caller.  The
  *     library never allocates, frees or keeps device memory between calls (except one
- *     4-byte error word per device, see csa2_get_device_error).
+ *     4-byte error word per device, see csa2_get_device_error, and the fixed score
+ *     array of csa2_index_full_noalloc).
  *   - Every compute call is asynchronous on the given cudaStream_t (passed as void*;
  *     NULL = legacy default stream) and never synchronises.
  *   - Arguments are validated on the host before any launch; a failed check returns a
@@ -166,6 +167,36 @@ typedef struct csa2_index_full_args {
 csa2_status csa2_index_full(const csa2_index_full_args* args, void* workspace,
                             size_t workspace_bytes, void* stream);
 csa2_status csa2_index_full_workspace(const csa2_index_full_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * csa2_index_full_noalloc -- csa2_index_full for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this call: it is a convenience of the
+ * library, not a step of the method.
+ *
+ * Some callers cannot hand the library a workspace: a serving process that carved all
+ * of HBM into KV pages at start-up and has no allocator left, a host runtime that talks
+ * to the library through this C ABI without any CUDA allocator of its own, or code
+ * that must not call cudaMalloc on its hot path (an allocation can synchronise the
+ * device and stall every stream).  This entry point needs no workspace: the candidate
+ * scores it needs between its two kernels live in one fixed device array compiled into
+ * the library, CSA2_NOALLOC_MAX_SCORES floats (4 MiB).  Every GPU that loads the
+ * library holds that array until the process exits.  The call itself allocates nothing.
+ *
+ * Arguments, outputs and results are exactly those of csa2_index_full.  Limits and
+ * rules of the shared array:
+ *   - B * num_blocks * per_block must not exceed CSA2_NOALLOC_MAX_SCORES (with the
+ *     16,384-candidate pool that is B <= 64); larger calls return
+ *     CSA2_ERR_UNSUPPORTED_SHAPE and launch nothing.
+ *   - The first call on a device looks up the array's device address for that device
+ *     (the device must be current); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous call's
+ *     contents.  Nothing in it needs to start at zero (every score is written before it
+ *     is read), but calls that overlap on the GPU -- on two streams, or from two host
+ *     threads -- race on it and must be serialised by the caller.
+ * -------------------------------------------------------------------------- */
+#define CSA2_NOALLOC_MAX_SCORES (1 << 20)
+
+csa2_status csa2_index_full_noalloc(const csa2_index_full_args* args, void* stream);
 
 /* ------------------------------------------------------------------------------
  * csa2_index_reindex -- Reindex mode (deep dive 3.2, 3.3 step 3): this layer's own

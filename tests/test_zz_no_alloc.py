@@ -1,0 +1,88 @@
+"""csa2_index_full_noalloc: the Full indexer for callers that cannot allocate device
+memory (for example a server whose HBM is already carved into KV pages, or a host
+runtime that reaches the library only through the C ABI and has no CUDA allocator).
+Its candidate scores live in a fixed array inside the library instead of a caller
+workspace.  Through the C ABI, two calls in a row must give exactly what the
+workspace-based csa2_index_full gives on the same inputs.
+
+This file is named to be collected last, so that a run stopping at the first failure
+has already run every other test."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from fp4_compressed_sparse_02_gb300 import _lib, csa2, synth
+from parity_utils import bf16_dev, logical_to_paged, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _args(cache, q, w, seq_of, n_vis, max_n, NB, P, k, outs):
+    a = _lib.IndexFullArgs()
+    a.struct_size = ctypes.sizeof(_lib.IndexFullArgs)
+    a.B, a.H_i = q.shape[0], q.shape[1]
+    a.q_idx, a.w = q.data_ptr(), w.data_ptr()
+    a.cache = cache.c_struct()
+    a.seq_of, a.n_vis, a.max_n = seq_of.data_ptr(), n_vis.data_ptr(), max_n
+    a.num_blocks, a.per_block, a.k, a.relu = NB, P, k, 1
+    a.pool, a.pool_len, a.topk, a.topk_len = (t.data_ptr() for t in outs)
+    return a
+
+
+def _outs(B, NB, P, k):
+    return [torch.full((B, NB * P), -7, dtype=torch.int32, device="cuda"),
+            torch.full((B,), -7, dtype=torch.int32, device="cuda"),
+            torch.full((B, k), -7, dtype=torch.int32, device="cuda"),
+            torch.full((B,), -7, dtype=torch.int32, device="cuda")]
+
+
+def _problem(seed, B, n_max, NB, P, k):
+    r = np.random.default_rng(seed)
+    d_ik, H_i = 128, 8
+    mp = (n_max + 63) // 64
+    pt = synth.page_table(r, 2, mp)
+    K = [synth.bf16_normal(r, (n_max, d_ik)) for _ in range(2)]
+    cache = csa2.PagedCache.allocate(2, n_max, 128, d_ik, "cuda", torch.from_numpy(pt))
+    cache.idx_k.copy_(bf16_dev(logical_to_paged(K, pt, 2 * mp, d_ik, np.uint16)))
+    q = bf16_dev(synth.bf16_normal(r, (B, H_i, d_ik)))
+    w = to_dev(synth.f32_normal(r, (B, H_i), 0.35))
+    seq_of = to_dev((np.arange(B) % 2).astype(np.int32))
+    n_vis = to_dev(r.integers(1, n_max + 1, size=B).astype(np.int32))
+    return cache, q, w, seq_of, n_vis
+
+
+def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
+    L = _lib.lib()
+    NB, P, k = 2048, 8, 512
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for call, (seed, B, n_max) in enumerate([(1, 6, 60000), (2, 3, 20000)]):
+        cache, q, w, seq_of, n_vis = _problem(seed, B, n_max, NB, P, k)
+        ref = _outs(B, NB, P, k)
+        a = _args(cache, q, w, seq_of, n_vis, n_max, NB, P, k, ref)
+        need = ctypes.c_size_t(0)
+        _lib.check(L.csa2_index_full_workspace(ctypes.byref(a), ctypes.byref(need)))
+        ws = torch.empty(need.value, dtype=torch.uint8, device="cuda")
+        _lib.check(L.csa2_index_full(ctypes.byref(a), ctypes.c_void_p(ws.data_ptr()), need.value, stream))
+        got = _outs(B, NB, P, k)
+        b = _args(cache, q, w, seq_of, n_vis, n_max, NB, P, k, got)
+        _lib.check(L.csa2_index_full_noalloc(ctypes.byref(b), stream))
+        torch.cuda.synchronize()
+        for x, y in zip(got, ref):
+            assert torch.equal(x, y), f"call {call}: allocation-free result differs"
+        assert (got[1] > 0).all() and (got[3] > 0).all()
+
+
+def test_noalloc_rejects_sizes_beyond_its_fixed_scratch():
+    L = _lib.lib()
+    NB, P, k = 2048, 8, 512
+    B = (1 << 20) // (NB * P) + 1            # one query more than the array holds
+    cache, q, w, seq_of, n_vis = _problem(3, B, 4096, NB, P, k)
+    outs = _outs(B, NB, P, k)
+    a = _args(cache, q, w, seq_of, n_vis, 4096, NB, P, k, outs)
+    st = L.csa2_index_full_noalloc(ctypes.byref(a), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 2
+    assert b"fixed scratch" in L.csa2_last_error_message()
+    torch.cuda.synchronize()
+    assert (outs[3] == -7).all()                           # nothing was launched
