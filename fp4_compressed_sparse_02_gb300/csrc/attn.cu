@@ -13,6 +13,9 @@
 // tile serves both products (row-major for S, transposed ldmatrix for O).
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
+
+#include <cstdlib>
 
 namespace csa2 {
 
@@ -335,6 +338,312 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------------
+// tcgen05 path for d = 512, Hq = 64 (the model's shape).  CTA (chunk, query), 256 threads.
+//   shared: KV tile 128 keys x 512 dims fp16 (128 KB), Q 64 heads x 512 fp16 (64 KB),
+//           P^T 128 keys x 64 heads fp16 (16 KB); 128-byte-swizzled canonical layouts.
+//   MMA1  S^T[128 keys x 64 heads] = KV . Q^T      (A, B K-major)       -> TMEM cols 0..63
+//   MMA2  O^T[512 dims x 64 heads] = KV^T . P^T    (A, B MN-major; the same KV tile read
+//         along the other axis)                                          -> TMEM cols 64..319
+// Keys sit in TMEM lanes after MMA1, so the per-head softmax max / sum reduce across
+// lanes with a warp transpose-reduce (each lane ends with heads 2l, 2l+1) and a
+// 4-warp shared-memory step.
+// ---------------------------------------------------------------------------------
+namespace tca {
+constexpr int THREADS = 256;
+constexpr int HQ = 64;
+constexpr int DIM = 512;
+constexpr int SM_KV = KC * DIM * 2;           // 131072
+constexpr int SM_Q = HQ * DIM * 2;            // 65536
+constexpr int SM_P = KC * HQ * 2;             // 16384
+constexpr int SMEM = SM_KV + SM_Q + SM_P + 1024;   // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t MAX_POLL = 1u << 22;
+
+// byte offset of 16-byte chunk ch (8 fp16) of row r in a K-major tile of `rows` rows x
+// 512 dims: 8 K-atoms of (rows/8) 1024-byte atoms each.
+__device__ __forceinline__ uint32_t kmaj(int r, int ch, int rows) {
+  return (uint32_t)((ch >> 3) * (rows / 8) * 1024 + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+template <int N>
+__device__ __forceinline__ void xreduce_max(float* v, int lane) {
+  constexpr int H = N / 2;
+  constexpr int o = N / 4;   // 64 -> offset 16, 32 -> 8, ...
+  const bool up = lane & o;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    float keep = up ? v[H + i] : v[i];
+    float send = up ? v[i] : v[H + i];
+    float recv = __shfl_xor_sync(AFULL, send, o);
+    v[i] = fmaxf(keep, recv);
+  }
+  if constexpr (N > 4) xreduce_max<H>(v, lane);
+}
+
+template <int N>
+__device__ __forceinline__ void xreduce_sum(float* v, int lane) {
+  constexpr int H = N / 2;
+  constexpr int o = N / 4;
+  const bool up = lane & o;
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    float keep = up ? v[H + i] : v[i];
+    float send = up ? v[i] : v[H + i];
+    float recv = __shfl_xor_sync(AFULL, send, o);
+    v[i] = keep + recv;
+  }
+  if constexpr (N > 4) xreduce_sum<H>(v, lane);
+}
+}  // namespace tca
+
+__global__ void __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
+  using namespace tca;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sKV = base;
+  uint8_t* sQ = sKV + SM_KV;
+  uint8_t* sP = sQ + SM_Q;
+  __shared__ long long keyrow[KC];
+  __shared__ float keyscale[KC];
+  __shared__ int keykind[KC];
+  __shared__ float redA[4][HQ];
+  __shared__ float redB[4][HQ];
+  __shared__ float mrow[HQ];
+  __shared__ uint32_t tslot;
+  __shared__ int ok_flag;
+  __shared__ __align__(8) uint64_t mbar[2];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.y, chunk = blockIdx.x;
+  const uint32_t kv_a = smem_u32(sKV), q_a = smem_u32(sQ), p_a = smem_u32(sP);
+
+  if (warp == 0) tc::tmem_alloc(&tslot, TMEM_COLS);
+  if (tid == 32) {
+    tc::mbar_init(&mbar[0], 1);
+    tc::mbar_init(&mbar[1], 1);
+  }
+  // ---- Q: bf16 -> fp16, K-major rows = heads ---------------------------------------
+  {
+    const uint4* qg = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
+#pragma unroll 4
+    for (int i = tid; i < HQ * DIM / 8; i += THREADS) {
+      const int h = i >> 6, ch = i & 63;
+      uint4 v = __ldg(qg + i);
+      uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+      *reinterpret_cast<uint4*>(sQ + kmaj(h, ch, HQ)) = o;
+    }
+  }
+  // ---- resolve the chunk's key slots ---------------------------------------------------
+  if (tid < KC) {
+    const int j = chunk * KC + tid;
+    int kind = 0;
+    long long row = -1;
+    float sc = 0.f;
+    if (j < p.k) {
+      int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
+      if (j < tl) {
+        int e = __ldg(p.topk + (long long)b * p.k + j);
+        if (e >= 0) {
+          row = entry_row(p.cache, __ldg(p.seq_of + b), e, &g_err_attn);
+          kind = row >= 0 ? 1 : 0;
+        }
+      }
+    } else if (j - p.k < p.swa_max) {
+      int w = j - p.k;
+      if (w < __ldg(p.swa_len + b)) {
+        long long r = (long long)__ldg(p.swa_start + b) + w;
+        if (r >= 0 && r < p.swa_rows) {
+          row = r;
+          kind = 2;
+          sc = __ldg(p.swa_scale + r);
+        } else {
+          raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
+        }
+      }
+    }
+    keyrow[tid] = row;
+    keykind[tid] = kind;
+    keyscale[tid] = sc;
+  }
+  __syncthreads();
+  // ---- gather + dequantise: 2 threads per key, 256 dims each -------------------------
+  {
+    const int key = tid >> 1, half = tid & 1;
+    const int kind = keykind[key];
+    const long long row = keyrow[key];
+    if (kind == 1) {
+      const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + row * (DIM / 2) + half * 128);
+      const uint4 sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + row * (DIM / 16) + half * 16));
+      uint4 cw[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {             // 16 code bytes = 32 dims = scale groups 2i, 2i+1
+        uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sw[i >> 1] >> (16 * (i & 1))));
+        const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
+        const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+        uint32_t o[16];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int bi = 0; bi < 4; ++bi)
+            o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
+        const int ch0 = half * 32 + i * 4;
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0 + t, KC)) =
+              make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+      }
+    } else if (kind == 2) {
+      const uint4* rp = reinterpret_cast<const uint4*>(p.swa + row * DIM + half * 256);
+      const float sc = keyscale[key];
+      uint4 v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = __ldg(rp + i);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {             // 16 bytes = 16 dims = 2 chunks
+        const uint32_t words[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t o[8];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
+            __half2 hv = *reinterpret_cast<__half2*>(&h2);
+            __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
+            o[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
+          }
+        const int ch0 = half * 32 + i * 2;
+        *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0 + 1, KC)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        *reinterpret_cast<uint4*>(sKV + kmaj(key, half * 32 + t, KC)) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = tslot;
+  // ---- MMA1 ------------------------------------------------------------------------
+  if (tid == 0) {
+    constexpr uint32_t id1 = tc::idesc_f16(128, HQ, 0, 0, 0);
+#pragma unroll 4
+    for (int ks = 0; ks < DIM / 16; ++ks) {
+      const uint64_t a = tc::smem_desc_sw128(kv_a + (ks >> 2) * (KC * 128) + (ks & 3) * 32, 16, 1024);
+      const uint64_t bd = tc::smem_desc_sw128(q_a + (ks >> 2) * (HQ * 128) + (ks & 3) * 32, 16, 1024);
+      tc::mma_f16_ss(tbase, a, bd, id1, ks > 0);
+    }
+    tc::mma_commit(&mbar[0]);
+    ok_flag = tc::mbar_wait(&mbar[0], 0, MAX_POLL) ? 1 : 0;
+    if (!ok_flag) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const bool ok = ok_flag != 0;
+  // ---- softmax over this chunk's keys (warps 0-3: thread = key lane) ---------------
+  if (ok && warp < 4) {
+    const int key = warp * 32 + lane;
+    uint32_t r[64];
+    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16), r);
+    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + 32, r + 32);
+    tc::tmem_ld_wait();
+    const bool valid = keykind[key] != 0;
+    float v[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) v[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
+    float t[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) t[h] = v[h];
+    xreduce_max<64>(t, lane);
+    redA[warp][2 * lane] = t[0];
+    redA[warp][2 * lane + 1] = t[1];
+  }
+  __syncthreads();
+  if (tid < HQ) mrow[tid] = fmaxf(fmaxf(redA[0][tid], redA[1][tid]), fmaxf(redA[2][tid], redA[3][tid]));
+  __syncthreads();
+  if (ok && warp < 4) {
+    const int key = warp * 32 + lane;
+    uint32_t r[64];
+    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16), r);
+    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + 32, r + 32);
+    tc::tmem_ld_wait();
+    const bool valid = keykind[key] != 0;
+    float e[64];
+    uint32_t pk[32];
+#pragma unroll
+    for (int h = 0; h < 64; h += 2) {
+      const float m0 = mrow[h], m1 = mrow[h + 1];
+      float x0 = (valid && m0 != -INFINITY) ? exp2f(__uint_as_float(r[h]) * p.scale_log2 - m0) : 0.f;
+      float x1 = (valid && m1 != -INFINITY) ? exp2f(__uint_as_float(r[h + 1]) * p.scale_log2 - m1) : 0.f;
+      __half2 hp = __floats2half2_rn(x0, x1);
+      pk[h >> 1] = *reinterpret_cast<uint32_t*>(&hp);
+      e[h] = __low2float(hp);
+      e[h + 1] = __high2float(hp);
+    }
+    // P^T row = this key: 64 heads, MN-major (heads contiguous), 8 chunks of 16 bytes
+#pragma unroll
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(sP + (key >> 3) * 1024 + (key & 7) * 128 + ((c8 ^ (key & 7)) << 4)) =
+          make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+    xreduce_sum<64>(e, lane);
+    redB[warp][2 * lane] = e[0];
+    redB[warp][2 * lane + 1] = e[1];
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  // ---- MMA2 ------------------------------------------------------------------------
+  if (tid == 0 && ok) {
+    constexpr uint32_t id2 = tc::idesc_f16(128, HQ, 0, 1, 1);
+#pragma unroll
+    for (int mt = 0; mt < DIM / 128; ++mt)
+#pragma unroll
+      for (int ks = 0; ks < KC / 16; ++ks) {
+        const uint64_t a = tc::smem_desc_sw128(kv_a + (2 * mt) * (KC * 128) + (2 * ks) * 1024, KC * 128, 1024);
+        const uint64_t bd = tc::smem_desc_sw128(p_a + (2 * ks) * 1024, 8192, 1024);
+        tc::mma_f16_ss(tbase + 64 + 64 * mt, a, bd, id2, ks > 0);
+      }
+    tc::mma_commit(&mbar[1]);
+    ok_flag = tc::mbar_wait(&mbar[1], 0, MAX_POLL) ? 1 : 0;
+    if (!ok_flag) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+  }
+  __syncthreads();
+  tc::fence_after_sync();
+  const long long pbase = ((long long)b * p.nchunk + chunk) * HQ;
+  if (ok_flag) {
+    // ---- epilogue: O^T tiles -> unnormalised partial O[head][dim] ---------------------
+    const int q4 = warp & 3;
+#pragma unroll 1
+    for (int tt = 0; tt < 2; ++tt) {
+      const int mt = (warp >> 2) * 2 + tt;
+      const int dim = mt * 128 + q4 * 32 + lane;
+      uint32_t r[64];
+      tc::tmem_ld32(tbase + ((uint32_t)(q4 * 32) << 16) + 64 + 64 * mt, r);
+      tc::tmem_ld32(tbase + ((uint32_t)(q4 * 32) << 16) + 64 + 64 * mt + 32, r + 32);
+      tc::tmem_ld_wait();
+      float* o = p.opart + pbase * DIM + dim;
+#pragma unroll
+      for (int h = 0; h < 64; ++h) o[(long long)h * DIM] = __uint_as_float(r[h]);
+    }
+    if (tid < HQ) {
+      const float l = redB[0][tid] + redB[1][tid] + redB[2][tid] + redB[3][tid];
+      p.ml[pbase + tid] = make_float2(mrow[tid], l);
+    }
+  } else if (tid < HQ) {
+    p.ml[pbase + tid] = make_float2(-INFINITY, 0.f);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
 // Merge the chunk partials of (query b, head h).  Thread -> 4 dims.
 template <int DIM>
 __global__ void __launch_bounds__(DIM / 4) k_combine(const float* __restrict__ opart, const float2* __restrict__ ml,
@@ -371,6 +680,17 @@ __global__ void __launch_bounds__(DIM / 4) k_combine(const float* __restrict__ o
 // ---------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------
+// CSA2_ATTN_LEGACY=1 selects the mma.sync kernel for every shape (kept for comparison
+// measurements of the two tensor-core paths).
+static bool attn_force_legacy() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CSA2_ATTN_LEGACY");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 static int attn_nchunk(const csa2_attn_args& a) { return (a.k + a.swa_max + KC - 1) / KC; }
 
 size_t attn_workspace_bytes(const csa2_attn_args& a) {
@@ -391,6 +711,19 @@ static cudaError_t run_attn(const csa2_attn_args& a, AttnParams& ap, cudaStream_
   k_attn_chunk<DIM, MT><<<grid, ATHREADS, C::SMEM, st>>>(ap);
   k_combine<DIM><<<dim3(a.B, a.Hq), DIM / 4, 0, st>>>(ap.opart, ap.ml, a.Hq, ap.nchunk, a.out,
                                                      a.out_dtype == CSA2_F32, a.lse);
+  return cudaGetLastError();
+}
+
+static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tca::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  k_attn_tc<<<dim3(ap.nchunk, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
+  k_combine<512><<<dim3(a.B, a.Hq), 128, 0, st>>>(ap.opart, ap.ml, a.Hq, ap.nchunk, a.out, a.out_dtype == CSA2_F32,
+                                                 a.lse);
   return cudaGetLastError();
 }
 
@@ -416,6 +749,7 @@ cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   ap.opart = static_cast<float*>(ws);
   ap.ml = reinterpret_cast<float2*>(static_cast<float*>(ws) + n * a.cache.d);
   const int mt = (a.Hq + 15) / 16;
+  if (a.cache.d == 512 && a.Hq == 64 && !attn_force_legacy()) return run_attn_tc(a, ap, st);
   if (a.cache.d == 512) {
     if (mt == 4) return run_attn<512, 4>(a, ap, st);
     if (mt == 2) return run_attn<512, 2>(a, ap, st);
