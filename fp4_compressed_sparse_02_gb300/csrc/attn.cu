@@ -44,6 +44,12 @@ struct AttnParams {
   float scale_log2;               // softmax_scale * log2(e)
   float* opart;                   // [B][nchunk][Hq][DIM]
   float2* ml;                     // [B][nchunk][Hq]  (row max in log2 units, row sum)
+  // tcgen05 path: normalised fp16 partials, per-query arrival counters, final outputs
+  __half* opart16;                // [B][nchunk][Hq][DIM]
+  int* counter;                   // [B], zero on entry
+  void* out;
+  int out_f32;
+  float* lse;
 };
 
 // byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile of `rowbytes`
@@ -339,309 +345,382 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 }
 
 // ---------------------------------------------------------------------------------
-// tcgen05 path for d = 512, Hq = 64 (the model's shape).  CTA (chunk, query), 256 threads.
-//   shared: KV tile 128 keys x 512 dims fp16 (128 KB), Q 64 heads x 512 fp16 (64 KB),
-//           P^T 128 keys x 64 heads fp16 (16 KB); 128-byte-swizzled canonical layouts.
-//   MMA1  S^T[128 keys x 64 heads] = KV . Q^T      (A, B K-major)       -> TMEM cols 0..63
-//   MMA2  O^T[512 dims x 64 heads] = KV^T . P^T    (A, B MN-major; the same KV tile read
-//         along the other axis)                                          -> TMEM cols 64..319
-// Keys sit in TMEM lanes after MMA1, so the per-head softmax max / sum reduce across
-// lanes with a warp transpose-reduce (each lane ends with heads 2l, 2l+1) and a
-// 4-warp shared-memory step.
+// tcgen05 path for d = 512, Hq = 64, k <= 512, swa_max <= 128 (the model's shape).
+// CTA (chunk c of 4, query b), 256 threads.  The chunk's keys are the selected-entry
+// slots [128c, 128c+128) and the window rows [32c, 32c+32): 160 keys, so a query needs
+// 4 CTAs and a decode batch of 32 fills the GPU in one wave.
+//   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle), 160 KB
+//   TMEM   : Q (A operand, heads in lanes 0..63, two fp16 per column)   cols   0..255
+//            S = Q K^T (fp32, 160 columns)                              cols 256..415
+//            P = softmax numerators (fp16 pairs, A operand)             cols 256..335
+//            O half = P V (fp32, 256 dims)                              cols   0..255
+//   MMA1  S[128 x 160] = Q[tmem] . KV^T        (B K-major)
+//   MMA2  O[128 x 256] = P[tmem] . KV[:, half] (B MN-major: the same tile read along
+//         the other axis), once per half of the 512 dims
+// Rows 64..127 of the 128-row MMAs are padding: whatever they hold only reaches rows of
+// S, P and O that are never read.  Heads sit in TMEM lanes, so the softmax of a head is
+// a row of one thread (two threads split the 160 keys and exchange max and sum).
+// The chunk writes o = O / l in fp16 plus (max, l) per head; the last of the 4 CTAs of
+// a query to finish (a global counter) merges the chunks into the output.
 // ---------------------------------------------------------------------------------
 namespace tca {
 constexpr int THREADS = 256;
 constexpr int HQ = 64;
 constexpr int DIM = 512;
-constexpr int SM_KV = KC * DIM * 2;           // 131072
-constexpr int SM_Q = HQ * DIM * 2;            // 65536
-constexpr int SM_P = KC * HQ * 2;             // 16384
-constexpr int SMEM = SM_KV + SM_Q + SM_P + 1024;   // + alignment slack
+constexpr int NCH = 4;                          // chunks per query
+constexpr int KT = 128;                         // selected-entry slots per chunk
+constexpr int KW = 32;                          // window rows per chunk
+constexpr int NK = KT + KW;                     // keys per chunk
+constexpr int ATOM = NK / 8 * 1024;             // bytes per 64-dim K-atom of the KV tile
+constexpr int SM_KV = NK * DIM * 2;             // 163840
+constexpr int SMEM = SM_KV + 1024;              // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_S = 256;
 constexpr uint32_t MAX_POLL = 1u << 22;
 
-// byte offset of 16-byte chunk ch (8 fp16) of row r in a K-major tile of `rows` rows x
-// 512 dims: 8 K-atoms of (rows/8) 1024-byte atoms each.
-__device__ __forceinline__ uint32_t kmaj(int r, int ch, int rows) {
-  return (uint32_t)((ch >> 3) * (rows / 8) * 1024 + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
+// byte offset of 16-byte chunk ch (8 fp16) of row r in the K-major KV tile
+__device__ __forceinline__ uint32_t kvoff(int r, int ch) {
+  return (uint32_t)((ch >> 3) * ATOM + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
-template <int N>
-__device__ __forceinline__ void xreduce_max(float* v, int lane) {
-  constexpr int H = N / 2;
-  constexpr int o = N / 4;   // 64 -> offset 16, 32 -> 8, ...
-  const bool up = lane & o;
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    float keep = up ? v[H + i] : v[i];
-    float send = up ? v[i] : v[H + i];
-    float recv = __shfl_xor_sync(AFULL, send, o);
-    v[i] = fmaxf(keep, recv);
-  }
-  if constexpr (N > 4) xreduce_max<H>(v, lane);
-}
-
-template <int N>
-__device__ __forceinline__ void xreduce_sum(float* v, int lane) {
-  constexpr int H = N / 2;
-  constexpr int o = N / 4;
-  const bool up = lane & o;
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    float keep = up ? v[H + i] : v[i];
-    float send = up ? v[i] : v[H + i];
-    float recv = __shfl_xor_sync(AFULL, send, o);
-    v[i] = keep + recv;
-  }
-  if constexpr (N > 4) xreduce_sum<H>(v, lane);
+__device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
+  const bool ok = tc::mbar_wait(mbar, parity, MAX_POLL);
+  if (!ok) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+  return ok;
 }
 }  // namespace tca
 
-__global__ void __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
+__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
   using namespace tca;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t* sKV = base;
-  uint8_t* sQ = sKV + SM_KV;
-  uint8_t* sP = sQ + SM_Q;
-  __shared__ long long keyrow[KC];
-  __shared__ float keyscale[KC];
-  __shared__ int keykind[KC];
-  __shared__ float redA[4][HQ];
-  __shared__ float redB[4][HQ];
-  __shared__ float mrow[HQ];
+  uint8_t* sKV = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ long long keyrow[NK];
+  __shared__ float keyscale[NK];
+  __shared__ int keyok[NK];
+  __shared__ float pmax[2][HQ];
+  __shared__ float psum[2][HQ];
+  __shared__ float linv[HQ];
+  __shared__ float2 mlx[HQ];                 // this chunk's (row max in log2 units, row sum)
   __shared__ uint32_t tslot;
   __shared__ int ok_flag;
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t mbar[3];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y, chunk = blockIdx.x;
-  const uint32_t kv_a = smem_u32(sKV), q_a = smem_u32(sQ), p_a = smem_u32(sP);
+  const uint32_t kv_a = smem_u32(sKV);
+  // warps 0, 1, 4, 5 own TMEM lanes 0..63 = the 64 heads; warp >> 2 picks a half of the
+  // columns they work on
+  const bool hw = (warp & 2) == 0;
+  const int head = (warp & 1) * 32 + lane;
+  const int kh = warp >> 2;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
   if (warp == 0) tc::tmem_alloc(&tslot, TMEM_COLS);
   if (tid == 32) {
     tc::mbar_init(&mbar[0], 1);
     tc::mbar_init(&mbar[1], 1);
+    tc::mbar_init(&mbar[2], 1);
   }
-  // ---- Q: bf16 -> fp16, K-major rows = heads ---------------------------------------
-  {
-    const uint4* qg = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
-#pragma unroll 4
-    for (int i = tid; i < HQ * DIM / 8; i += THREADS) {
-      const int h = i >> 6, ch = i & 63;
-      uint4 v = __ldg(qg + i);
-      uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-      *reinterpret_cast<uint4*>(sQ + kmaj(h, ch, HQ)) = o;
-    }
-  }
-  // ---- resolve the chunk's key slots ---------------------------------------------------
-  if (tid < KC) {
-    const int j = chunk * KC + tid;
-    int kind = 0;
+  // ---- Q loads in flight first (16 x 16 B per thread), then resolve the 160 keys ----
+  const uint4* qg = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
+  uint4 qv[HQ * DIM / 8 / THREADS];
+#pragma unroll
+  for (int i = 0; i < HQ * DIM / 8 / THREADS; ++i) qv[i] = __ldg(qg + tid + i * THREADS);
+  if (tid < NK) {
     long long row = -1;
     float sc = 0.f;
-    if (j < p.k) {
-      int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
-      if (j < tl) {
-        int e = __ldg(p.topk + (long long)b * p.k + j);
-        if (e >= 0) {
-          row = entry_row(p.cache, __ldg(p.seq_of + b), e, &g_err_attn);
-          kind = row >= 0 ? 1 : 0;
+    int ok = 0;
+    if (tid < KT) {
+      const int j = chunk * KT + tid;
+      if (j < p.k) {
+        const int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
+        const int e = __ldg(p.topk + (long long)b * p.k + j);
+        const int sq = __ldg(p.seq_of + b);
+        if (j < tl && e >= 0) {
+          row = entry_row(p.cache, sq, e, &g_err_attn);
+          ok = row >= 0;
         }
       }
-    } else if (j - p.k < p.swa_max) {
-      int w = j - p.k;
-      if (w < __ldg(p.swa_len + b)) {
-        long long r = (long long)__ldg(p.swa_start + b) + w;
-        if (r >= 0 && r < p.swa_rows) {
-          row = r;
-          kind = 2;
-          sc = __ldg(p.swa_scale + r);
-        } else {
-          raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
+    } else {
+      const int w = chunk * KW + (tid - KT);
+      if (w < p.swa_max) {
+        const int wl = __ldg(p.swa_len + b);
+        const long long r = (long long)__ldg(p.swa_start + b) + w;
+        if (w < wl) {
+          if (r >= 0 && r < p.swa_rows) {
+            row = r;
+            ok = 1;
+            sc = __ldg(p.swa_scale + r);
+          } else {
+            raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
+          }
         }
       }
     }
     keyrow[tid] = row;
-    keykind[tid] = kind;
     keyscale[tid] = sc;
+    keyok[tid] = ok;
   }
+  // ---- Q -> fp16 staging rows in shared memory (16-byte chunk c of head h stored at
+  //      chunk c ^ (h % 8), so both the row-wise writes and the per-head reads spread
+  //      over all banks) -------------------------------------------------------------
+#pragma unroll
+  for (int i = 0; i < HQ * DIM / 8 / THREADS; ++i) {
+    const int idx = tid + i * THREADS;
+    const int h = idx >> 6, ch = idx & 63;
+    const uint4 v = qv[i];
+    *reinterpret_cast<uint4*>(sKV + h * 1024 + ((ch ^ (h & 7)) << 4)) =
+        make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+  }
+  tc::fence_before_sync();
   __syncthreads();
-  // ---- gather + dequantise: 2 threads per key, 256 dims each -------------------------
-  {
-    const int key = tid >> 1, half = tid & 1;
-    const int kind = keykind[key];
-    const long long row = keyrow[key];
-    if (kind == 1) {
-      const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + row * (DIM / 2) + half * 128);
-      const uint4 sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + row * (DIM / 16) + half * 16));
-      uint4 cw[8];
+  tc::fence_after_sync();
+  const uint32_t tb = tslot;
+  // ---- gather loads (FP4 rows 0..127: 2 threads each; SWA rows 128..159: 8 threads each)
+  const int fkey = tid >> 1, half = tid & 1;
+  const int skey = KT + (tid >> 3), part = tid & 7;
+  const bool fok = keyok[fkey] != 0;
+  const bool sok = keyok[skey] != 0;
+  uint4 cw[8], sv = make_uint4(0, 0, 0, 0), wv[4];
+  if (fok) {
+    const long long row = keyrow[fkey];
+    const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + row * (DIM / 2) + half * 128);
+    sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + row * (DIM / 16) + half * 16));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
-      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+    for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
+  }
+  if (sok) {
+    const uint4* rp = reinterpret_cast<const uint4*>(p.swa + keyrow[skey] * DIM + part * 64);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {             // 16 code bytes = 32 dims = scale groups 2i, 2i+1
-        uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sw[i >> 1] >> (16 * (i & 1))));
-        const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
-        const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-        uint32_t o[16];
+    for (int i = 0; i < 4; ++i) wv[i] = __ldg(rp + i);
+  }
+  // ---- staged Q rows -> TMEM (A operand, two fp16 per column) while the gather flies ---
+  if (hw) {
 #pragma unroll
-        for (int wi = 0; wi < 4; ++wi)
+    for (int r = 0; r < 4; ++r) {               // 8 chunks = 64 dims = 32 columns per round
+      uint32_t w[32];
 #pragma unroll
-          for (int bi = 0; bi < 4; ++bi)
-            o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
-        const int ch0 = half * 32 + i * 4;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0 + t, KC)) =
-              make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+      for (int j = 0; j < 8; ++j) {
+        const int ch = kh * 32 + r * 8 + j;
+        const uint4 v = *reinterpret_cast<const uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4));
+        w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
       }
-    } else if (kind == 2) {
-      const uint4* rp = reinterpret_cast<const uint4*>(p.swa + row * DIM + half * 256);
-      const float sc = keyscale[key];
-      uint4 v[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = __ldg(rp + i);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {             // 16 bytes = 16 dims = 2 chunks
-        const uint32_t words[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint32_t o[8];
-#pragma unroll
-        for (int wi = 0; wi < 4; ++wi)
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
-            __half2 hv = *reinterpret_cast<__half2*>(&h2);
-            __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
-            o[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
-          }
-        const int ch0 = half * 32 + i * 2;
-        *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(sKV + kmaj(key, ch0 + 1, KC)) = make_uint4(o[4], o[5], o[6], o[7]);
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        *reinterpret_cast<uint4*>(sKV + kmaj(key, half * 32 + t, KC)) = make_uint4(0, 0, 0, 0);
+      tc::tmem_st32(tb + lane_base + kh * 128 + r * 32, w);
     }
+    tc::tmem_st_wait();
+  }
+  tc::fence_before_sync();
+  __syncthreads();                              // staging reads done: the tile may be overwritten
+  // ---- dequantise into the K-major KV tile ----------------------------------------------
+  if (fok) {
+    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {               // 16 code bytes = 32 dims = scale groups 2i, 2i+1
+      const uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sw[i >> 1] >> (16 * (i & 1))));
+      const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
+      const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+      uint32_t o[16];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+        for (int bi = 0; bi < 4; ++bi)
+          o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
+      const int ch0 = half * 32 + i * 4;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        *reinterpret_cast<uint4*>(sKV + kvoff(fkey, ch0 + t)) = make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 32; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(fkey, half * 32 + t)) = make_uint4(0, 0, 0, 0);
+  }
+  if (sok) {
+    const float sc = keyscale[skey];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {               // 16 bytes = 16 dims = 2 chunks
+      const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
+          const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+          __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
+          o[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
+        }
+      const int ch0 = part * 8 + i * 2;
+      *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(skey, part * 8 + t)) = make_uint4(0, 0, 0, 0);
   }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tbase = tslot;
-  // ---- MMA1 ------------------------------------------------------------------------
+  // ---- MMA1: S = Q K^T -----------------------------------------------------------------
   if (tid == 0) {
-    constexpr uint32_t id1 = tc::idesc_f16(128, HQ, 0, 0, 0);
+    constexpr uint32_t id1 = tc::idesc_f16(128, NK, 0, 0, 0);
 #pragma unroll 4
     for (int ks = 0; ks < DIM / 16; ++ks) {
-      const uint64_t a = tc::smem_desc_sw128(kv_a + (ks >> 2) * (KC * 128) + (ks & 3) * 32, 16, 1024);
-      const uint64_t bd = tc::smem_desc_sw128(q_a + (ks >> 2) * (HQ * 128) + (ks & 3) * 32, 16, 1024);
-      tc::mma_f16_ss(tbase, a, bd, id1, ks > 0);
+      const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
+      tc::mma_f16_ts(tb + COL_S, tb + ks * 8, bd, id1, ks > 0);
     }
     tc::mma_commit(&mbar[0]);
-    ok_flag = tc::mbar_wait(&mbar[0], 0, MAX_POLL) ? 1 : 0;
-    if (!ok_flag) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+    ok_flag = wait_mma(&mbar[0], 0) ? 1 : 0;
   }
   __syncthreads();
   tc::fence_after_sync();
-  const bool ok = ok_flag != 0;
-  // ---- softmax over this chunk's keys (warps 0-3: thread = key lane) ---------------
-  if (ok && warp < 4) {
-    const int key = warp * 32 + lane;
-    uint32_t r[64];
-    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16), r);
-    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + 32, r + 32);
+  // ---- softmax: head = lane row; two threads split the 160 keys ([80 kh, 80 kh + 80)) -
+  float e[80];
+  if (ok_flag && hw) {
+    uint32_t r[96];
+    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh, r);
+    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 32, r + 32);
+    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 64, r + 64);
     tc::tmem_ld_wait();
-    const bool valid = keykind[key] != 0;
-    float v[64];
+    float mx = -INFINITY;
 #pragma unroll
-    for (int h = 0; h < 64; ++h) v[h] = valid ? __uint_as_float(r[h]) * p.scale_log2 : -INFINITY;
-    float t[64];
-#pragma unroll
-    for (int h = 0; h < 64; ++h) t[h] = v[h];
-    xreduce_max<64>(t, lane);
-    redA[warp][2 * lane] = t[0];
-    redA[warp][2 * lane + 1] = t[1];
-  }
-  __syncthreads();
-  if (tid < HQ) mrow[tid] = fmaxf(fmaxf(redA[0][tid], redA[1][tid]), fmaxf(redA[2][tid], redA[3][tid]));
-  __syncthreads();
-  if (ok && warp < 4) {
-    const int key = warp * 32 + lane;
-    uint32_t r[64];
-    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16), r);
-    tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + 32, r + 32);
-    tc::tmem_ld_wait();
-    const bool valid = keykind[key] != 0;
-    float e[64];
-    uint32_t pk[32];
-#pragma unroll
-    for (int h = 0; h < 64; h += 2) {
-      const float m0 = mrow[h], m1 = mrow[h + 1];
-      float x0 = (valid && m0 != -INFINITY) ? exp2f(__uint_as_float(r[h]) * p.scale_log2 - m0) : 0.f;
-      float x1 = (valid && m1 != -INFINITY) ? exp2f(__uint_as_float(r[h + 1]) * p.scale_log2 - m1) : 0.f;
-      __half2 hp = __floats2half2_rn(x0, x1);
-      pk[h >> 1] = *reinterpret_cast<uint32_t*>(&hp);
-      e[h] = __low2float(hp);
-      e[h + 1] = __high2float(hp);
+    for (int j = 0; j < 80; ++j) {
+      e[j] = keyok[80 * kh + j] ? __uint_as_float(r[j]) * p.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, e[j]);
     }
-    // P^T row = this key: 64 heads, MN-major (heads contiguous), 8 chunks of 16 bytes
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-      *reinterpret_cast<uint4*>(sP + (key >> 3) * 1024 + (key & 7) * 128 + ((c8 ^ (key & 7)) << 4)) =
-          make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-    xreduce_sum<64>(e, lane);
-    redB[warp][2 * lane] = e[0];
-    redB[warp][2 * lane + 1] = e[1];
+    pmax[kh][head] = mx;
   }
-  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (ok_flag && hw) {
+    const float m = fmaxf(pmax[0][head], pmax[1][head]);
+    float l = 0.f;
+    uint32_t pk[40];
+#pragma unroll
+    for (int j = 0; j < 80; j += 2) {
+      const float x0 = (m == -INFINITY) ? 0.f : exp2f(e[j] - m);
+      const float x1 = (m == -INFINITY) ? 0.f : exp2f(e[j + 1] - m);
+      const __half2 hp = __floats2half2_rn(x0, x1);
+      pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
+      l += __low2float(hp) + __high2float(hp);
+    }
+    tc::tmem_st32(tb + lane_base + COL_S + 40 * kh, pk);
+    tc::tmem_st8(tb + lane_base + COL_S + 40 * kh + 32, pk + 32);
+    tc::tmem_st_wait();
+    psum[kh][head] = l;
+    if (kh == 0) linv[head] = m;                 // row max, consumed just below
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // ---- MMA2 ------------------------------------------------------------------------
-  if (tid == 0 && ok) {
-    constexpr uint32_t id2 = tc::idesc_f16(128, HQ, 0, 1, 1);
-#pragma unroll
-    for (int mt = 0; mt < DIM / 128; ++mt)
-#pragma unroll
-      for (int ks = 0; ks < KC / 16; ++ks) {
-        const uint64_t a = tc::smem_desc_sw128(kv_a + (2 * mt) * (KC * 128) + (2 * ks) * 1024, KC * 128, 1024);
-        const uint64_t bd = tc::smem_desc_sw128(p_a + (2 * ks) * 1024, 8192, 1024);
-        tc::mma_f16_ss(tbase + 64 + 64 * mt, a, bd, id2, ks > 0);
-      }
-    tc::mma_commit(&mbar[1]);
-    ok_flag = tc::mbar_wait(&mbar[1], 0, MAX_POLL) ? 1 : 0;
-    if (!ok_flag) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+  if (tid < HQ) {
+    const float l = psum[0][tid] + psum[1][tid];
+    const bool any = ok_flag && l > 0.f;
+    mlx[tid] = any ? make_float2(linv[tid], l) : make_float2(-INFINITY, 0.f);
+    linv[tid] = any ? 1.f / l : 0.f;
   }
-  __syncthreads();
-  tc::fence_after_sync();
-  const long long pbase = ((long long)b * p.nchunk + chunk) * HQ;
-  if (ok_flag) {
-    // ---- epilogue: O^T tiles -> unnormalised partial O[head][dim] ---------------------
-    const int q4 = warp & 3;
+  // ---- MMA2 in two halves of 256 dims; each epilogue writes o = O / l (fp16) into this
+  //      CTA's shared memory: row h (1 KB), 16-byte chunk c at c ^ (h % 8).  Half 0 lands
+  //      in K-atoms 0..3 of the tile, which half 1 of MMA2 no longer reads. -------------
 #pragma unroll 1
-    for (int tt = 0; tt < 2; ++tt) {
-      const int mt = (warp >> 2) * 2 + tt;
-      const int dim = mt * 128 + q4 * 32 + lane;
-      uint32_t r[64];
-      tc::tmem_ld32(tbase + ((uint32_t)(q4 * 32) << 16) + 64 + 64 * mt, r);
-      tc::tmem_ld32(tbase + ((uint32_t)(q4 * 32) << 16) + 64 + 64 * mt + 32, r + 32);
-      tc::tmem_ld_wait();
-      float* o = p.opart + pbase * DIM + dim;
+  for (int hf = 0; hf < 2; ++hf) {
+    if (tid == 0 && ok_flag) {
+      constexpr uint32_t id2 = tc::idesc_f16(128, 256, 0, 0, 1);
 #pragma unroll
-      for (int h = 0; h < 64; ++h) o[(long long)h * DIM] = __uint_as_float(r[h]);
+      for (int ks = 0; ks < NK / 16; ++ks) {
+        const uint64_t bd = tc::smem_desc_sw128(kv_a + (4 * hf) * ATOM + (2 * ks) * 1024, ATOM, 1024);
+        tc::mma_f16_ts(tb, tb + COL_S + ks * 8, bd, id2, ks > 0);
+      }
+      tc::mma_commit(&mbar[1 + hf]);
+      ok_flag = wait_mma(&mbar[1 + hf], 0) ? 1 : 0;
     }
-    if (tid < HQ) {
-      const float l = redB[0][tid] + redB[1][tid] + redB[2][tid] + redB[3][tid];
-      p.ml[pbase + tid] = make_float2(mrow[tid], l);
+    __syncthreads();
+    tc::fence_after_sync();
+    if (ok_flag && hw) {
+      const float li = linv[head];
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {            // 32 columns = 32 dims = 4 chunks
+        uint32_t r[32];
+        tc::tmem_ld32(tb + lane_base + 128 * kh + 32 * c4, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
+                                                 __uint_as_float(r[8 * i + 2 * t + 1]) * li);
+            pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          const int ch = 32 * hf + 16 * kh + 4 * c4 + i;
+          *reinterpret_cast<uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
     }
-  } else if (tid < HQ) {
-    p.ml[pbase + tid] = make_float2(-INFINITY, 0.f);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
   }
+  // ---- merge across the cluster: CTA r combines heads [16 r, 16 r + 16) of the 4 chunks --
+  tc::cluster_sync();
+  {
+    const uint32_t rank = tc::cluster_ctarank();
+    const int h = 16 * (int)rank + (tid >> 4), dc = tid & 15;   // dims [32 dc, 32 dc + 32)
+    float w4[NCH], M = -INFINITY, L = 0.f;
+    const uint32_t ml_a = smem_u32(&mlx[h]);
+    float2 mv[NCH];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      mv[c] = tc::ld_dsmem_f2(tc::mapa(ml_a, c));
+      M = fmaxf(M, mv[c].x);
+    }
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      w4[c] = (mv[c].x == -INFINITY) ? 0.f : mv[c].y * exp2f(mv[c].x - M);
+      L += w4[c];
+    }
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const float wgt = w4[c] * inv;
+      if (wgt == 0.f) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int ch = 4 * dc + j;
+        const uint4 u = tc::ld_dsmem_v4(tc::mapa(kv_a + h * 1024 + ((ch ^ (h & 7)) << 4), c));
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&uw[t]));
+          acc[8 * j + 2 * t] = fmaf(wgt, f.x, acc[8 * j + 2 * t]);
+          acc[8 * j + 2 * t + 1] = fmaf(wgt, f.y, acc[8 * j + 2 * t + 1]);
+        }
+      }
+    }
+    const long long ob = ((long long)b * HQ + h) * DIM + 32 * dc;
+    if (p.out_f32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+    } else {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        pk[i] = *reinterpret_cast<uint32_t*>(&v2);
+      }
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + ob);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+    if (p.lse && dc == 0) p.lse[(long long)b * HQ + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+  }
+  tc::cluster_sync();                            // no CTA leaves while others read its memory
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+  if (warp == 0) tc::tmem_dealloc(tb, TMEM_COLS);
 }
 
 // Merge the chunk partials of (query b, head h).  Thread -> 4 dims.
@@ -693,9 +772,18 @@ static bool attn_force_legacy() {
 
 static int attn_nchunk(const csa2_attn_args& a) { return (a.k + a.swa_max + KC - 1) / KC; }
 
+// chunks the workspace is laid out for: enough for either kernel
+static int ws_chunks(const csa2_attn_args& a) { return attn_nchunk(a) > tca::NCH ? attn_nchunk(a) : tca::NCH; }
+
+// partials (float32 for the mma.sync path; the tcgen05 path uses the first half as
+// fp16), then (m, l) per chunk and head, then one arrival counter per query.
+static size_t attn_counter_offset(const csa2_attn_args& a) {
+  size_t n = (size_t)a.B * ws_chunks(a) * a.Hq;
+  return ((n * a.cache.d * sizeof(float) + n * sizeof(float2)) + 255) & ~(size_t)255;
+}
+
 size_t attn_workspace_bytes(const csa2_attn_args& a) {
-  size_t n = (size_t)a.B * attn_nchunk(a) * a.Hq;
-  return n * a.cache.d * sizeof(float) + n * sizeof(float2);
+  return attn_counter_offset(a) + (size_t)a.B * sizeof(int);
 }
 
 template <int DIM, int MT>
@@ -721,9 +809,8 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  k_attn_tc<<<dim3(ap.nchunk, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
-  k_combine<512><<<dim3(a.B, a.Hq), 128, 0, st>>>(ap.opart, ap.ml, a.Hq, ap.nchunk, a.out, a.out_dtype == CSA2_F32,
-                                                 a.lse);
+  ap.nchunk = tca::NCH;
+  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
   return cudaGetLastError();
 }
 
@@ -745,11 +832,18 @@ cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   ap.Hq = a.Hq;
   ap.nchunk = attn_nchunk(a);
   ap.scale_log2 = a.softmax_scale * LOG2E;
-  size_t n = (size_t)a.B * ap.nchunk * a.Hq;
+  size_t n = (size_t)a.B * ws_chunks(a) * a.Hq;
   ap.opart = static_cast<float*>(ws);
   ap.ml = reinterpret_cast<float2*>(static_cast<float*>(ws) + n * a.cache.d);
+  ap.opart16 = static_cast<__half*>(ws);
+  ap.counter = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + attn_counter_offset(a));
+  ap.out = a.out;
+  ap.out_f32 = a.out_dtype == CSA2_F32;
+  ap.lse = a.lse;
   const int mt = (a.Hq + 15) / 16;
-  if (a.cache.d == 512 && a.Hq == 64 && !attn_force_legacy()) return run_attn_tc(a, ap, st);
+  if (a.cache.d == 512 && a.Hq == 64 && a.k <= tca::NCH * tca::KT && a.swa_max <= tca::NCH * tca::KW &&
+      !attn_force_legacy())
+    return run_attn_tc(a, ap, st);
   if (a.cache.d == 512) {
     if (mt == 4) return run_attn<512, 4>(a, ap, st);
     if (mt == 2) return run_attn<512, 2>(a, ap, st);

@@ -90,6 +90,69 @@ __global__ void __launch_bounds__(256) k_project(const HT* __restrict__ H,
 }
 
 // ---------------------------------------------------------------------------------
+// Projection for few rows (decode append, T <= 64): CTA = (64 output columns, one K
+// slice of ks rows).  The whole W slice and H slice are loaded with 16-byte loads in
+// one go (no K loop), then each thread accumulates T/4 rows of one column.
+// ---------------------------------------------------------------------------------
+constexpr int SMALL_T = 64;
+
+template <typename HT>
+__device__ __forceinline__ void load_h8(const HT* p, float* v);
+template <>
+__device__ __forceinline__ void load_h8<uint16_t>(const uint16_t* p, float* v) {
+  uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { v[2 * i] = __uint_as_float(w[i] << 16); v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u); }
+}
+template <>
+__device__ __forceinline__ void load_h8<float>(const float* p, float* v) {
+  float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+template <typename HT>
+__global__ void __launch_bounds__(256) k_project_small(const HT* __restrict__ H, const uint16_t* __restrict__ Wkv,
+                                                       const uint16_t* __restrict__ Wz, float* __restrict__ out,
+                                                       int T, int d_model, int d, int N, int ks) {
+  extern __shared__ __align__(16) uint8_t psm[];
+  uint16_t* Ws = reinterpret_cast<uint16_t*>(psm);                 // [ks][64] bf16
+  float* Hs = reinterpret_cast<float*>(psm + (size_t)ks * 128);      // [T][ks]
+  const int tid = threadIdx.x;
+  const int n0 = blockIdx.x * 64, s = blockIdx.y;
+  const int k0 = s * ks;
+  const uint16_t* W = (n0 < d) ? Wkv : Wz;
+  const int wn0 = (n0 < d) ? n0 : n0 - d;
+  for (int i = tid; i < ks * 8; i += 256) {
+    const int r = i >> 3, c8 = i & 7;
+    *reinterpret_cast<uint4*>(Ws + r * 64 + c8 * 8) =
+        __ldg(reinterpret_cast<const uint4*>(W + (long long)(k0 + r) * d + wn0 + c8 * 8));
+  }
+  for (int i = tid; i < T * (ks / 8); i += 256) {
+    const int t = i / (ks / 8), c8 = i % (ks / 8);
+    float v[8];
+    load_h8<HT>(H + (long long)t * d_model + k0 + c8 * 8, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) Hs[t * ks + c8 * 8 + j] = v[j];
+  }
+  __syncthreads();
+  const int c = tid & 63, rg = tid >> 6;
+  float acc[SMALL_T / 4];
+#pragma unroll
+  for (int i = 0; i < SMALL_T / 4; ++i) acc[i] = 0.f;
+  for (int k = 0; k < ks; ++k) {
+    const float w = bf16_bits_to_f32(Ws[k * 64 + c]);
+#pragma unroll
+    for (int i = 0; i < SMALL_T / 4; ++i)
+      if (rg + 4 * i < T) acc[i] = fmaf(Hs[(rg + 4 * i) * ks + k], w, acc[i]);
+  }
+  float* o = out + (long long)s * T * N + n0 + c;
+#pragma unroll
+  for (int i = 0; i < SMALL_T / 4; ++i)
+    if (rg + 4 * i < T) o[(long long)(rg + 4 * i) * N] = acc[i];
+}
+
+// ---------------------------------------------------------------------------------
 // Pool + RoPE + quantise.  One thread per 16-channel group of one entry.
 //   C row t, channel c: sum_{s < nsplit} Cp[s*split_stride + t*ldc + c]
 //   Z likewise from Zp (m > 1 only).
@@ -122,7 +185,17 @@ __device__ __forceinline__ void load16(const float* p, float* v) {
 
 __device__ __forceinline__ void load16_sum(const float* p, long long stride, int nsplit, float* v) {
   load16(p, v);
-  for (int s = 1; s < nsplit; ++s) {
+  int s = 1;
+  for (; s + 3 < nsplit; s += 4) {   // four partial rows in flight
+    float w0[16], w1[16], w2[16], w3[16];
+    load16(p + s * stride, w0);
+    load16(p + (s + 1) * stride, w1);
+    load16(p + (s + 2) * stride, w2);
+    load16(p + (s + 3) * stride, w3);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = (((v[i] + w0[i]) + w1[i]) + w2[i]) + w3[i];
+  }
+  for (; s < nsplit; ++s) {
     float w[16];
     load16(p + s * stride, w);
 #pragma unroll
@@ -211,63 +284,116 @@ __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Indexer K: idx_k[e][j] = bf16( sum_c dequant(e)[c] * W_ik[c][j] ), float32 FMA in
-// ascending c.  16 entries per CTA, one thread per output column.
+// Indexer K: idx_k[e][j] = bf16( sum_c dequant(e)[c] * W_ik[c][j] ).  CTA = E entries,
+// 8 warps; warp w owns rows c in [w*d/8, (w+1)*d/8) of W_ik (loaded once, 16 rows at a
+// time, for all E entries), lane l owns columns [l*cpl, l*cpl + cpl).  The 8 warp
+// partials are summed in warp order, so the result does not depend on scheduling.
 // ---------------------------------------------------------------------------------
-constexpr int IK_E = 16;
-
-__global__ void __launch_bounds__(128) k_index_k(csa2_cache cache, const int* __restrict__ seq,
+template <int E, int DIK>
+__global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __restrict__ seq,
                                                  const int* __restrict__ entry, int G,
                                                  const uint16_t* __restrict__ Wik) {
-  extern __shared__ float deq[];                 // [IK_E][d]
-  __shared__ long long rows[IK_E];
-  const int d = cache.d, dik = cache.d_ik;
-  const int g0 = blockIdx.x * IK_E;
-  if (threadIdx.x < IK_E) {
-    int g = g0 + threadIdx.x;
-    rows[threadIdx.x] = (g < G) ? entry_row(cache, __ldg(seq + g), __ldg(entry + g), &g_err_compress) : -1;
+  constexpr int CPL = DIK / 32;                  // columns per lane: 4 or 2
+  extern __shared__ float ik_sm[];
+  const int d = cache.d;
+  float* deq = ik_sm;                            // [E][d]
+  float* part = ik_sm + E * d;                   // [8][E][DIK]
+  __shared__ long long rows[E];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g0 = blockIdx.x * E;
+  if (tid < E) {
+    const int g = g0 + tid;
+    rows[tid] = (g < G) ? entry_row(cache, __ldg(seq + g), __ldg(entry + g), &g_err_compress) : -1;
   }
   __syncthreads();
-  // dequantise: each thread handles one code byte (2 channels) at a time
-  for (int i = threadIdx.x; i < IK_E * d / 2; i += blockDim.x) {
-    int e = i / (d / 2), cb = i % (d / 2);
-    long long r = rows[e];
+  for (int i = tid; i < E * d / 2; i += 256) {
+    const int e = i / (d / 2), cb = i % (d / 2);
+    const long long r = rows[e];
     float v0 = 0.f, v1 = 0.f;
     if (r >= 0) {
-      uint32_t byte = cache.codes[r * (d / 2) + cb];
-      float s = e4m3_to_f32(cache.scales[r * (d / 16) + (2 * cb) / 16]);
-      uint32_t h2 = e2m1x2_to_f16x2(byte);
-      __half2 hv = *reinterpret_cast<__half2*>(&h2);
-      v0 = __low2float(hv) * s;
-      v1 = __high2float(hv) * s;
+      const uint32_t byte = cache.codes[r * (d / 2) + cb];
+      const float sc = e4m3_to_f32(cache.scales[r * (d / 16) + (2 * cb) / 16]);
+      const uint32_t h2 = e2m1x2_to_f16x2(byte);
+      const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+      v0 = __low2float(hv) * sc;
+      v1 = __high2float(hv) * sc;
     }
     deq[e * d + 2 * cb] = v0;
     deq[e * d + 2 * cb + 1] = v1;
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < dik; j += blockDim.x) {
-    float acc[IK_E];
+  float acc[E][CPL];
 #pragma unroll
-    for (int e = 0; e < IK_E; ++e) acc[e] = 0.f;
-    for (int c = 0; c < d; ++c) {
-      float w = bf16_bits_to_f32(__ldg(Wik + (long long)c * dik + j));
+  for (int e = 0; e < E; ++e)
 #pragma unroll
-      for (int e = 0; e < IK_E; ++e) acc[e] = fmaf(deq[e * d + c], w, acc[e]);
-    }
+    for (int j = 0; j < CPL; ++j) acc[e][j] = 0.f;
+  const int rows_per_warp = d / 8;
+  const int cbase = warp * rows_per_warp;
+  for (int c0 = 0; c0 < rows_per_warp; c0 += 16) {
+    float w[16][CPL];
 #pragma unroll
-    for (int e = 0; e < IK_E; ++e) {
-      long long r = rows[e];
-      if (r >= 0) {
-        __nv_bfloat16 hb = __float2bfloat16_rn(acc[e]);
-        cache.idx_k[r * dik + j] = *reinterpret_cast<uint16_t*>(&hb);
+    for (int rr = 0; rr < 16; ++rr) {
+      const uint16_t* wp = Wik + (long long)(cbase + c0 + rr) * DIK + lane * CPL;
+      if constexpr (CPL == 4) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(wp));
+        w[rr][0] = __uint_as_float(u.x << 16); w[rr][1] = __uint_as_float(u.x & 0xffff0000u);
+        w[rr][2] = __uint_as_float(u.y << 16); w[rr][3] = __uint_as_float(u.y & 0xffff0000u);
+      } else {
+        const uint32_t u = __ldg(reinterpret_cast<const uint32_t*>(wp));
+        w[rr][0] = __uint_as_float(u << 16); w[rr][1] = __uint_as_float(u & 0xffff0000u);
       }
     }
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float x = deq[e * d + cbase + c0 + rr];
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) acc[e][j] = fmaf(x, w[rr][j], acc[e][j]);
+      }
   }
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) part[(warp * E + e) * DIK + lane * CPL + j] = acc[e][j];
+  __syncthreads();
+  for (int i = tid; i < E * DIK; i += 256) {
+    const int e = i / DIK, j = i % DIK;
+    const long long r = rows[e];
+    if (r < 0) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) sum += part[(w8 * E + e) * DIK + j];
+    const __nv_bfloat16 hb = __float2bfloat16_rn(sum);
+    cache.idx_k[r * DIK + j] = *reinterpret_cast<const uint16_t*>(&hb);
+  }
+}
+
+template <int E, int DIK>
+static void launch_index_k(const csa2_compress_args& a, int G, cudaStream_t st) {
+  const size_t sm = ((size_t)E * a.cache.d + 8 * E * DIK) * sizeof(float);
+  k_index_k<E, DIK><<<(G + E - 1) / E, 256, sm, st>>>(a.cache, a.seq, a.entry, G, a.W_ik);
 }
 
 // ---------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------
+// K slices for the few-row projection: aim at ~128 CTAs with slices that are a multiple of
+// 8 rows and small enough for shared memory (ks * (128 + 4*T) bytes).
+static int small_splits(int T, int d_model, int N) {
+  int best = 1;
+  for (int s = 1; s <= 64; ++s) {
+    if (d_model % s || (d_model / s) % 8) continue;
+    const size_t smem = (size_t)(d_model / s) * (128 + 4 * T);
+    if (smem > 160 * 1024) continue;
+    best = s;
+    if ((N / 64) * s >= 128) break;
+  }
+  return best;
+}
+
+static bool use_small(const csa2_compress_args& a) { return a.T <= SMALL_T; }
+
 static int pick_splits(int T, int d_model, int N) {
   // enough CTAs to cover the GPU when T is small (decode append): split K so that
   // (tiles x splits) >= ~2 waves of 152 SMs, keeping each split >= 128 deep.
@@ -280,7 +406,7 @@ static int pick_splits(int T, int d_model, int N) {
 size_t compress_workspace_bytes(const csa2_compress_args& a) {
   if (!a.W_kv) return 0;
   int N = a.cache.d * (a.m > 1 ? 2 : 1);
-  int s = pick_splits(a.T, a.d_model, N);
+  int s = use_small(a) ? small_splits(a.T, a.d_model, N) : pick_splits(a.T, a.d_model, N);
   return (size_t)s * a.T * N * sizeof(float);
 }
 
@@ -290,16 +416,35 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   QuantParams qp{};
   if (a.W_kv) {
     int N = d * (a.m > 1 ? 2 : 1);
-    int s = pick_splits(a.T, a.d_model, N);
+    float* out = static_cast<float*>(ws);
+    int s;
+    if (use_small(a)) {
+      s = small_splits(a.T, a.d_model, N);
+      const int ks = a.d_model / s;
+      const size_t sm = (size_t)ks * (128 + 4 * a.T);
+      cudaError_t e;
+      if (a.h_dtype == CSA2_F32) {
+        e = cudaFuncSetAttribute(k_project_small<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        k_project_small<float><<<dim3(N / 64, s), 256, sm, st>>>(static_cast<const float*>(a.H), a.W_kv, a.W_z,
+                                                                 out, a.T, a.d_model, d, N, ks);
+      } else {
+        e = cudaFuncSetAttribute(k_project_small<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        k_project_small<uint16_t><<<dim3(N / 64, s), 256, sm, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv,
+                                                                    a.W_z, out, a.T, a.d_model, d, N, ks);
+      }
+    } else {
+    s = pick_splits(a.T, a.d_model, N);
     int kps = ((a.d_model / s + PBK - 1) / PBK) * PBK;
     dim3 grid(N / PBN, (a.T + PBM - 1) / PBM, s);
-    float* out = static_cast<float*>(ws);
     if (a.h_dtype == CSA2_F32)
       k_project<float><<<grid, 256, 0, st>>>(static_cast<const float*>(a.H), a.W_kv, a.W_z, out,
                                              a.T, a.d_model, d, N, kps);
     else
       k_project<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z,
                                                 out, a.T, a.d_model, d, N, kps);
+    }
     qp.Cp = out;
     qp.Zp = out + d;
     qp.split_stride = (long long)a.T * N;
@@ -327,8 +472,12 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   long long threads = (long long)G * (d / 16);
   if (threads > 0) k_quant<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(qp);
   if (a.W_ik && G > 0) {
-    size_t sm = (size_t)IK_E * d * sizeof(float);
-    k_index_k<<<(G + IK_E - 1) / IK_E, 128, sm, st>>>(a.cache, a.seq, a.entry, G, a.W_ik);
+    const bool many = G >= 2048;
+    if (a.cache.d_ik == 128) {
+      if (many) launch_index_k<8, 128>(a, G, st); else launch_index_k<1, 128>(a, G, st);
+    } else {
+      if (many) launch_index_k<8, 64>(a, G, st); else launch_index_k<1, 64>(a, G, st);
+    }
   }
   return cudaGetLastError();
 }
