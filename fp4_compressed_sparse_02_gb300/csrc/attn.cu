@@ -350,18 +350,19 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // slots [128c, 128c+128) and the window rows [32c, 32c+32): 160 keys, so a query needs
 // 4 CTAs and a decode batch of 32 fills the GPU in one wave.
 //   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle), 160 KB
-//   TMEM   : Q (A operand, heads in lanes 0..63, two fp16 per column)   cols   0..255
+//   TMEM   : Q (A operand, two fp16 per column)                         cols   0..255
 //            S = Q K^T (fp32, 160 columns)                              cols 256..415
 //            P = softmax numerators (fp16 pairs, A operand)             cols 256..335
 //            O half = P V (fp32, 256 dims)                              cols   0..255
-//   MMA1  S[128 x 160] = Q[tmem] . KV^T        (B K-major)
-//   MMA2  O[128 x 256] = P[tmem] . KV[:, half] (B MN-major: the same tile read along
+//   MMA1  S[64 x 160] = Q[tmem] . KV^T        (B K-major)
+//   MMA2  O[64 x 256] = P[tmem] . KV[:, half] (B MN-major: the same tile read along
 //         the other axis), once per half of the 512 dims
-// Rows 64..127 of the 128-row MMAs are padding: whatever they hold only reaches rows of
-// S, P and O that are never read.  Heads sit in TMEM lanes, so the softmax of a head is
-// a row of one thread (two threads split the 160 keys and exchange max and sum).
-// The chunk writes o = O / l in fp16 plus (max, l) per head; the last of the 4 CTAs of
-// a query to finish (a global counter) merges the chunks into the output.
+// With M = 64 the 64 heads occupy lanes 0..15 of each of the four lane quarters, so all
+// eight warps (two per quarter, each taking half of the keys or dims) share the
+// softmax, the Q transfer and the epilogue.  A head's softmax is a row of one thread.
+// The 4 chunk CTAs of a query form a thread-block cluster: each writes o = O / l (fp16)
+// and (max, l) per head into its own shared memory, and after a cluster barrier CTA r
+// merges heads [16 r, 16 r + 16) of all four chunks through distributed shared memory.
 // ---------------------------------------------------------------------------------
 namespace tca {
 constexpr int THREADS = 256;
@@ -394,8 +395,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   using namespace tca;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sKV = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ long long keyrow[NK];
-  __shared__ float keyscale[NK];
   __shared__ int keyok[NK];
   __shared__ float pmax[2][HQ];
   __shared__ float psum[2][HQ];
@@ -408,10 +407,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y, chunk = blockIdx.x;
   const uint32_t kv_a = smem_u32(sKV);
-  // warps 0, 1, 4, 5 own TMEM lanes 0..63 = the 64 heads; warp >> 2 picks a half of the
-  // columns they work on
-  const bool hw = (warp & 2) == 0;
-  const int head = (warp & 1) * 32 + lane;
+  // M = 64 tensor-memory layout: head h sits in lane 32 * (h / 16) + h % 16, so warp w
+  // (lane quarter w % 4) owns heads [16 (w % 4), 16 (w % 4) + 16) in its lanes 0..15 and
+  // warp >> 2 picks a half of the columns; lanes 16..31 mirror lanes 0..15 and write
+  // nothing that is read.
+  const bool hw = true;
+  const bool lv = lane < 16;
+  const int head = 16 * (warp & 3) + (lane & 15);
   const int kh = warp >> 2;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
@@ -421,46 +423,54 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     tc::mbar_init(&mbar[1], 1);
     tc::mbar_init(&mbar[2], 1);
   }
-  // ---- Q loads in flight first (16 x 16 B per thread), then resolve the 160 keys ----
+  // ---- Q loads in flight first (16 x 16 B per thread) ------------------------------------
   const uint4* qg = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
   uint4 qv[HQ * DIM / 8 / THREADS];
 #pragma unroll
   for (int i = 0; i < HQ * DIM / 8 / THREADS; ++i) qv[i] = __ldg(qg + tid + i * THREADS);
-  if (tid < NK) {
-    long long row = -1;
-    float sc = 0.f;
-    int ok = 0;
-    if (tid < KT) {
-      const int j = chunk * KT + tid;
-      if (j < p.k) {
-        const int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
-        const int e = __ldg(p.topk + (long long)b * p.k + j);
-        const int sq = __ldg(p.seq_of + b);
-        if (j < tl && e >= 0) {
-          row = entry_row(p.cache, sq, e, &g_err_attn);
-          ok = row >= 0;
-        }
-      }
-    } else {
-      const int w = chunk * KW + (tid - KT);
-      if (w < p.swa_max) {
-        const int wl = __ldg(p.swa_len + b);
-        const long long r = (long long)__ldg(p.swa_start + b) + w;
-        if (w < wl) {
-          if (r >= 0 && r < p.swa_rows) {
-            row = r;
-            ok = 1;
-            sc = __ldg(p.swa_scale + r);
-          } else {
-            raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
-          }
+  // ---- each thread resolves the keys it gathers: FP4 slot fkey (2 threads per key) and
+  //      window row skey (8 threads per key), then issues those loads at once -------------
+  const int fkey = tid >> 1, half = tid & 1;
+  const int skey = KT + (tid >> 3), part = tid & 7;
+  long long frow = -1, srow = -1;
+  float ssc = 0.f;
+  {
+    const int j = chunk * KT + fkey;
+    if (j < p.k) {
+      const int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
+      const int e = __ldg(p.topk + (long long)b * p.k + j);
+      const int sq = __ldg(p.seq_of + b);
+      if (j < tl && e >= 0) frow = entry_row(p.cache, sq, e, &g_err_attn);
+    }
+    const int w = chunk * KW + (tid >> 3);
+    if (w < p.swa_max) {
+      const int wl = __ldg(p.swa_len + b);
+      const long long r = (long long)__ldg(p.swa_start + b) + w;
+      if (w < wl) {
+        if (r >= 0 && r < p.swa_rows) {
+          srow = r;
+          ssc = __ldg(p.swa_scale + r);
+        } else if (part == 0) {
+          raise_error(&g_err_attn, CSA2_DEVERR_SWA_RANGE);
         }
       }
     }
-    keyrow[tid] = row;
-    keyscale[tid] = sc;
-    keyok[tid] = ok;
   }
+  const bool fok = frow >= 0, sok = srow >= 0;
+  uint4 cw[8], sv = make_uint4(0, 0, 0, 0), wv[4];
+  if (fok) {
+    const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + frow * (DIM / 2) + half * 128);
+    sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + frow * (DIM / 16) + half * 16));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
+  }
+  if (sok) {
+    const uint4* rp = reinterpret_cast<const uint4*>(p.swa + srow * DIM + part * 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wv[i] = __ldg(rp + i);
+  }
+  if (half == 0) keyok[fkey] = fok;
+  if (part == 0) keyok[skey] = sok;
   // ---- Q -> fp16 staging rows in shared memory (16-byte chunk c of head h stored at
   //      chunk c ^ (h % 8), so both the row-wise writes and the per-head reads spread
   //      over all banks) -------------------------------------------------------------
@@ -476,24 +486,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = tslot;
-  // ---- gather loads (FP4 rows 0..127: 2 threads each; SWA rows 128..159: 8 threads each)
-  const int fkey = tid >> 1, half = tid & 1;
-  const int skey = KT + (tid >> 3), part = tid & 7;
-  const bool fok = keyok[fkey] != 0;
-  const bool sok = keyok[skey] != 0;
-  uint4 cw[8], sv = make_uint4(0, 0, 0, 0), wv[4];
-  if (fok) {
-    const long long row = keyrow[fkey];
-    const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + row * (DIM / 2) + half * 128);
-    sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + row * (DIM / 16) + half * 16));
-#pragma unroll
-    for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
-  }
-  if (sok) {
-    const uint4* rp = reinterpret_cast<const uint4*>(p.swa + keyrow[skey] * DIM + part * 64);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) wv[i] = __ldg(rp + i);
-  }
   // ---- staged Q rows -> TMEM (A operand, two fp16 per column) while the gather flies ---
   if (hw) {
 #pragma unroll
@@ -535,7 +527,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     for (int t = 0; t < 32; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(fkey, half * 32 + t)) = make_uint4(0, 0, 0, 0);
   }
   if (sok) {
-    const float sc = keyscale[skey];
+    const float sc = ssc;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {               // 16 bytes = 16 dims = 2 chunks
       const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
@@ -563,7 +555,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   tc::fence_after_sync();
   // ---- MMA1: S = Q K^T -----------------------------------------------------------------
   if (tid == 0) {
-    constexpr uint32_t id1 = tc::idesc_f16(128, NK, 0, 0, 0);
+    constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
 #pragma unroll 4
     for (int ks = 0; ks < DIM / 16; ++ks) {
       const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
@@ -588,7 +580,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       e[j] = keyok[80 * kh + j] ? __uint_as_float(r[j]) * p.scale_log2 : -INFINITY;
       mx = fmaxf(mx, e[j]);
     }
-    pmax[kh][head] = mx;
+    if (lv) pmax[kh][head] = mx;
   }
   __syncthreads();
   if (ok_flag && hw) {
@@ -606,8 +598,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     tc::tmem_st32(tb + lane_base + COL_S + 40 * kh, pk);
     tc::tmem_st8(tb + lane_base + COL_S + 40 * kh + 32, pk + 32);
     tc::tmem_st_wait();
-    psum[kh][head] = l;
-    if (kh == 0) linv[head] = m;                 // row max, consumed just below
+    if (lv) psum[kh][head] = l;
+    if (lv && kh == 0) linv[head] = m;           // row max, consumed just below
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -624,7 +616,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll 1
   for (int hf = 0; hf < 2; ++hf) {
     if (tid == 0 && ok_flag) {
-      constexpr uint32_t id2 = tc::idesc_f16(128, 256, 0, 0, 1);
+      constexpr uint32_t id2 = tc::idesc_f16(64, 256, 0, 0, 1);
 #pragma unroll
       for (int ks = 0; ks < NK / 16; ++ks) {
         const uint64_t bd = tc::smem_desc_sw128(kv_a + (4 * hf) * ATOM + (2 * ks) * 1024, ATOM, 1024);
@@ -635,7 +627,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
     __syncthreads();
     tc::fence_after_sync();
-    if (ok_flag && hw) {
+    if (ok_flag) {                                 // tcgen05.ld is warp-wide; only lanes 0..15 store
       const float li = linv[head];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {            // 32 columns = 32 dims = 4 chunks
@@ -652,7 +644,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
             pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           const int ch = 32 * hf + 16 * kh + 4 * c4 + i;
-          *reinterpret_cast<uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          if (lv)
+            *reinterpret_cast<uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
     }
@@ -664,58 +657,74 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   tc::cluster_sync();
   {
     const uint32_t rank = tc::cluster_ctarank();
-    const int h = 16 * (int)rank + (tid >> 4), dc = tid & 15;   // dims [32 dc, 32 dc + 32)
-    float w4[NCH], M = -INFINITY, L = 0.f;
-    const uint32_t ml_a = smem_u32(&mlx[h]);
-    float2 mv[NCH];
+    float* wts = reinterpret_cast<float*>(&pmax[0][0]);       // [16][NCH] merge weights
+    if (tid < 16) {
+      const int h = 16 * (int)rank + tid;
+      const uint32_t ml_a = smem_u32(&mlx[h]);
+      float2 mv[NCH];
+      float M = -INFINITY, L = 0.f;
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      mv[c] = tc::ld_dsmem_f2(tc::mapa(ml_a, c));
-      M = fmaxf(M, mv[c].x);
+      for (int c = 0; c < NCH; ++c) {
+        mv[c] = tc::ld_dsmem_f2(tc::mapa(ml_a, c));
+        M = fmaxf(M, mv[c].x);
+      }
+      float w4[NCH];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        w4[c] = (mv[c].x == -INFINITY) ? 0.f : mv[c].y * exp2f(mv[c].x - M);
+        L += w4[c];
+      }
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) wts[tid * NCH + c] = w4[c] * inv;
+      if (p.lse) p.lse[(long long)b * HQ + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    // item = (head, 16-byte chunk); a warp covers 32 consecutive chunks of one head row,
+    // which the c ^ (h % 8) placement spreads over every bank
+    uint4 u[4][NCH];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int idx = tid + it * THREADS;
+      const int hh = idx >> 6, ch = idx & 63;
+      const int h = 16 * (int)rank + hh;
+      const uint32_t la = kv_a + h * 1024 + ((ch ^ (h & 7)) << 4);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+        u[it][c] = (wts[hh * NCH + c] != 0.f) ? tc::ld_dsmem_v4(tc::mapa(la, c)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      w4[c] = (mv[c].x == -INFINITY) ? 0.f : mv[c].y * exp2f(mv[c].x - M);
-      L += w4[c];
-    }
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    float acc[32];
+    for (int it = 0; it < 4; ++it) {
+      const int idx = tid + it * THREADS;
+      const int hh = idx >> 6, ch = idx & 63;
+      const int h = 16 * (int)rank + hh;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const float wgt = w4[c] * inv;
-      if (wgt == 0.f) continue;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int ch = 4 * dc + j;
-        const uint4 u = tc::ld_dsmem_v4(tc::mapa(kv_a + h * 1024 + ((ch ^ (h & 7)) << 4), c));
-        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+      for (int c = 0; c < NCH; ++c) {
+        const float wgt = wts[hh * NCH + c];
+        const uint32_t uw[4] = {u[it][c].x, u[it][c].y, u[it][c].z, u[it][c].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&uw[t]));
-          acc[8 * j + 2 * t] = fmaf(wgt, f.x, acc[8 * j + 2 * t]);
-          acc[8 * j + 2 * t + 1] = fmaf(wgt, f.y, acc[8 * j + 2 * t + 1]);
+          acc[2 * t] = fmaf(wgt, f.x, acc[2 * t]);
+          acc[2 * t + 1] = fmaf(wgt, f.y, acc[2 * t + 1]);
         }
       }
-    }
-    const long long ob = ((long long)b * HQ + h) * DIM + 32 * dc;
-    if (p.out_f32) {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob);
+      const long long ob = ((long long)b * HQ + h) * DIM + 8 * ch;
+      if (p.out_f32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      } else {
+        uint32_t pk[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) o[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
-    } else {
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-        pk[i] = *reinterpret_cast<uint32_t*>(&v2);
+        for (int t = 0; t < 4; ++t) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(acc[2 * t], acc[2 * t + 1]);
+          pk[t] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + ob) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + ob);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
-    if (p.lse && dc == 0) p.lse[(long long)b * HQ + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
   tc::cluster_sync();                            // no CTA leaves while others read its memory
   tc::fence_before_sync();

@@ -152,6 +152,73 @@ __global__ void __launch_bounds__(256) k_project_small(const HT* __restrict__ H,
     if (rg + 4 * i < T) o[(long long)(rg + 4 * i) * N] = acc[i];
 }
 
+// Few-row projection on the tensor cores (bf16 H): mma.sync m16n8k16, fp32 accumulate.
+// CTA = (64 output columns, one K slice of ks rows, ks % 16 == 0), 4 warps; warp w owns
+// rows [16w, 16w + 16).  Shared rows are padded to an odd number of 16-byte chunks so the
+// ldmatrix row addresses fall in distinct banks.
+__global__ void __launch_bounds__(128) k_project_mma(const uint16_t* __restrict__ H, const uint16_t* __restrict__ Wkv,
+                                                     const uint16_t* __restrict__ Wz, float* __restrict__ out, int T,
+                                                     int d_model, int d, int N, int ks) {
+  extern __shared__ __align__(16) uint8_t psm[];
+  const int HS = ks * 2 + 16, WS = 64 * 2 + 16;
+  uint8_t* Hs = psm;                       // [64][HS]
+  uint8_t* Ws = psm + 64 * HS;             // [ks][WS]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n0 = blockIdx.x * 64, s = blockIdx.y, k0 = s * ks;
+  const uint16_t* W = (n0 < d) ? Wkv : Wz;
+  const int wn0 = (n0 < d) ? n0 : n0 - d;
+  for (int i = tid; i < ks * 8; i += 128) {
+    const int r = i >> 3, c8 = i & 7;
+    *reinterpret_cast<uint4*>(Ws + r * WS + c8 * 16) =
+        __ldg(reinterpret_cast<const uint4*>(W + (long long)(k0 + r) * d + wn0 + c8 * 8));
+  }
+  const int kc = ks / 8;
+  for (int i = tid; i < 64 * kc; i += 128) {
+    const int t = i / kc, c8 = i % kc;
+    *reinterpret_cast<uint4*>(Hs + t * HS + c8 * 16) =
+        (t < T) ? __ldg(reinterpret_cast<const uint4*>(H + (long long)t * d_model + k0 + c8 * 8)) : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  if (16 * warp >= T) return;
+  float acc[8][4];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  const int mi = lane >> 3, r8 = lane & 7;
+  const uint32_t hs = smem_u32(Hs), ws = smem_u32(Ws);
+  for (int kk = 0; kk < ks; kk += 16) {
+    uint32_t a0, a1, a2, a3;
+    ldmatrix_x4(a0, a1, a2, a3, hs + (16 * warp + (lane & 15)) * HS + (kk + (lane >> 4) * 8) * 2);
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(b0, b1, b2, b3, ws + (kk + (mi & 1) * 8 + r8) * WS + (np * 16 + (mi >> 1) * 8) * 2);
+      mma_bf16_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+      mma_bf16_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+    }
+  }
+  const int g = lane >> 2, c = lane & 3;
+  const int r0 = 16 * warp + g, r1 = r0 + 8;
+  float* o = out + (long long)s * T * N + n0 + 2 * c;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    if (r0 < T) *reinterpret_cast<float2*>(o + (long long)r0 * N + 8 * t) = make_float2(acc[t][0], acc[t][1]);
+    if (r1 < T) *reinterpret_cast<float2*>(o + (long long)r1 * N + 8 * t) = make_float2(acc[t][2], acc[t][3]);
+  }
+}
+
+// K slices for the tensor-core few-row projection: multiples of 16 rows, ~128 CTAs.
+static int mma_splits(int d_model, int N) {
+  int best = 1;
+  for (int s = 1; s <= 64; ++s) {
+    if (d_model % s || (d_model / s) % 16) continue;
+    const size_t smem = (size_t)64 * ((d_model / s) * 2 + 16) + (size_t)(d_model / s) * 144;
+    if (smem > 160 * 1024) continue;
+    best = s;
+    if ((N / 64) * s >= 128) break;
+  }
+  return best;
+}
+
 // ---------------------------------------------------------------------------------
 // Pool + RoPE + quantise.  One thread per 16-channel group of one entry.
 //   C row t, channel c: sum_{s < nsplit} Cp[s*split_stride + t*ldc + c]
@@ -406,7 +473,8 @@ static int pick_splits(int T, int d_model, int N) {
 size_t compress_workspace_bytes(const csa2_compress_args& a) {
   if (!a.W_kv) return 0;
   int N = a.cache.d * (a.m > 1 ? 2 : 1);
-  int s = use_small(a) ? small_splits(a.T, a.d_model, N) : pick_splits(a.T, a.d_model, N);
+  int s = !use_small(a) ? pick_splits(a.T, a.d_model, N)
+          : (a.h_dtype == CSA2_BF16 ? mma_splits(a.d_model, N) : small_splits(a.T, a.d_model, N));
   return (size_t)s * a.T * N * sizeof(float);
 }
 
@@ -418,7 +486,15 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
     int N = d * (a.m > 1 ? 2 : 1);
     float* out = static_cast<float*>(ws);
     int s;
-    if (use_small(a)) {
+    if (use_small(a) && a.h_dtype == CSA2_BF16) {
+      s = mma_splits(a.d_model, N);
+      const int ks = a.d_model / s;
+      const size_t sm = (size_t)64 * (ks * 2 + 16) + (size_t)ks * 144;
+      cudaError_t e = cudaFuncSetAttribute(k_project_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      if (e != cudaSuccess) return e;
+      k_project_mma<<<dim3(N / 64, s), 128, sm, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z, out, a.T,
+                                                      a.d_model, d, N, ks);
+    } else if (use_small(a)) {
       s = small_splits(a.T, a.d_model, N);
       const int ks = a.d_model / s;
       const size_t sm = (size_t)ks * (128 + 4 * a.T);

@@ -151,14 +151,13 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
 
 __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t caddr) {
   uint4 v;
-  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(caddr)
-               : "memory");
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(caddr));
   return v;
 }
 
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t caddr) {
   float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr));
   return v;
 }
 
