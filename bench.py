@@ -40,6 +40,32 @@ def peaks():
     return 6800.0, "fallback"
 
 
+PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
+            ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu")}
+
+
+def profiled_traffic(kernel, workload_name):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and workload,
+    or None when there is none or the kernel source changed since it was captured."""
+    import hashlib
+    key = PROFILES.get((kernel, workload_name))
+    if key is None:
+        return None
+    prof = os.path.join(ROOT, "profiles", key[0])
+    src = os.path.join(ROOT, "fp4_compressed_sparse_02_gb300", "csrc", key[1])
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    fields = {}
+    for ln in open(prof):
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            fields[k.strip()] = v.strip()
+    sha = hashlib.sha1(open(src, "rb").read()).hexdigest()
+    if fields.get(f"source_sha1 ({key[1]})") != sha:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -135,7 +161,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="decode128k", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--cpu-queries", type=int, default=24)
+    ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     a.warmup = max(a.warmup, 3)
@@ -161,26 +187,31 @@ def main():
     with torch.cuda.stream(stream):
         step.run()
     torch.cuda.synchronize()
+    # the step as four graphs so that the Full indexer call and one attention call (the
+    # dominant kernel) are timed with events inside every timed step
     graphs = []
-    parts = [lambda: step.run_append(), lambda: step.run_layer(0),
+    parts = [lambda: step.run_append(), lambda: step.run_index(0), lambda: step.run_attn(0),
              lambda: [step.run_layer(i) for i in range(1, len(step.layers))]]
     for fn in parts:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             fn()
         graphs.append(g)
-    ga, gf, gr = graphs
+    ga, gf, gat, gr = graphs
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
+    def replay_step():
+        ga.replay(); gf.replay(); gat.replay(); gr.replay()
+
     with torch.cuda.stream(stream):
         for _ in range(a.warmup):
-            ga.replay(); gf.replay(); gr.replay()
+            replay_step()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -195,13 +226,16 @@ def main():
             ev[i][0].record(stream)
             gf.replay()
             ev[i][1].record(stream)
+            gat.replay()
+            ev[i][2].record(stream)
             gr.replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    full_ms = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    full_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    attn_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     if world > 1:
         t = torch.tensor([ms_total], device=f"cuda:{local}")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -233,7 +267,7 @@ def main():
         for _ in range(e2e_steps):
             for dev_t, host_t in host_in:
                 dev_t.copy_(host_t, non_blocking=True)
-            ga.replay(); gf.replay(); gr.replay()
+            replay_step()
             host_out.copy_(step.out[-1], non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
@@ -246,9 +280,12 @@ def main():
 
     if rank == 0:
         peak, peak_kind = peaks()
+        attn_bytes = B * nbytes["per_query"]["attn"]
+        attn_gbs = attn_bytes / (attn_ms / 1000.0) / 1e9
         full_bytes = B * nbytes["per_query"]["full"]
-        achieved = full_bytes / (full_ms / 1000.0) / 1e9
+        full_gbs = full_bytes / (full_ms / 1000.0) / 1e9
         step_gbs = nbytes["total"] / (ms_step / 1000.0) / 1e9
+        n_index = sum(1 for m in info["schedule"] if m in ("full", "reindex"))
         line = {
             "metric": METRIC, "value": value, "unit": "query-layers/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -259,12 +296,17 @@ def main():
                        "N": info["N"], "B": B, "layers": info["layers"], "d_kv": info["d"], "Hq": info["Hq"],
                        "indexer": f"{info['H_i']}x{info['d_ik']}", "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB algorithmic bytes per step"},
-            "roofline": {"bound": "hbm", "kernel": "csa2_index_full (scan + pool Top-k)", "achieved": achieved,
-                         "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
-                         "peak_source": peak_kind},
+            "roofline": {"bound": "hbm", "kernel": "k_attn_tc (csa2_sparse_attn, one layer)",
+                         "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                         "traffic": profiled_traffic("k_attn_tc", a.workload), "peak_source": peak_kind,
+                         "algorithmic_bytes": attn_bytes, "ms": attn_ms},
+            "roofline_index_full": {"bound": "hbm", "kernel": "k_full_scan + k_select (csa2_index_full)",
+                                    "achieved": full_gbs, "peak": peak, "unit": "GB/s", "frac": full_gbs / peak,
+                                    "traffic": profiled_traffic("k_full_scan", a.workload),
+                                    "algorithmic_bytes": full_bytes, "ms": full_ms},
             "step_hbm": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": step_gbs, "frac": step_gbs / peak},
             "clocks": clk,
-            "gpu_launches": a.steps * (3 + 2 + 2 * info["schedule"].count("reindex") + 2 * info["layers"]),
+            "gpu_launches": a.steps * (3 + 2 * n_index + info["layers"]),
             "e2e": {"value": e2e_val, "unit": "query-layers/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
         }

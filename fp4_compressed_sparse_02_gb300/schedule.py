@@ -59,19 +59,25 @@ class DecodeStep:
                             rope_cos=cos, rope_sin=sin, W_ik=a["W_ik"], ws=self.ws)
 
     def run_layer(self, i):
+        self.run_index(i)
+        self.run_attn(i)
+
+    def run_index(self, i):
+        """The index step of layer i (nothing for a Reuse layer)."""
         L = self.layers[i]
         mode = L["mode"]
         if mode == FULL:
             csa2.index_full(self.cache, L["q_idx"], L["w"], self.seq_of, self.n_vis, self.max_n, self.NB,
                             self.P, self.k, out=(self.pool, self.pool_len, self.topk[i], self.topk_len[i]),
                             ws=self.ws)
-            tk, tl = self.topk[i], self.topk_len[i]
         elif mode == REINDEX:
             csa2.index_reindex(self.cache, L["q_idx"], L["w"], self.seq_of, self.pool, self.pool_len, self.k,
                                out=(self.topk[i], self.topk_len[i]), ws=self.ws)
-            tk, tl = self.topk[i], self.topk_len[i]
-        else:
-            tk, tl = self._last_topk(i)
+
+    def run_attn(self, i):
+        """The sparse attention of layer i over its own (or the reused) index set."""
+        L = self.layers[i]
+        tk, tl = self.result_topk(i)
         csa2.sparse_attn(self.cache, L["q"], self.seq_of, tk, tl, L["swa"], L["swa_scale"], L["swa_start"],
                          L["swa_len"], self.swa_max, out=self.out[i], lse=self.lse[i], ws=self.ws)
 
