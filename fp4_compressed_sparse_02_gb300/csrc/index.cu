@@ -147,28 +147,63 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
     float sc[4];
     tile_scores<DK, NHG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
     tile_scores<DK, NHG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+    // lane (g, c) owns candidate row r[c] = base + g + 8c (a permutation of the 32 rows)
+    float cv = sc[0];
+    int ci = (int)r[0];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int ri = (int)r[t];
-      bool cand = (c == 0) && (r[t] < hi) && better(sc[t], ri, thv, thi);
-      unsigned m = __ballot_sync(FULL_MASK, cand);
-      while (m) {
-        int src = __ffs(m) - 1;
-        m &= m - 1;
-        float cv = __shfl_sync(FULL_MASK, sc[t], src);
-        int ci = __shfl_sync(FULL_MASK, ri, src);
-        unsigned bm = __ballot_sync(FULL_MASK, lane < P && better(cv, ci, tv, ti));
+    for (int t = 1; t < 4; ++t)
+      if (c == t) { cv = sc[t]; ci = (int)r[t]; }
+    if ((long long)ci >= hi) { cv = -INFINITY; ci = 0x7fffffff; }
+    const unsigned m = __ballot_sync(FULL_MASK, better(cv, ci, thv, thi));
+    if (m == 0) continue;
+    if (__popc(m) <= 3 || P > 16) {
+      // few candidates (or a long list): insert them one by one
+      unsigned mm = m;
+      while (mm) {
+        const int src = __ffs(mm) - 1;
+        mm &= mm - 1;
+        const float xv = __shfl_sync(FULL_MASK, cv, src);
+        const int xi = __shfl_sync(FULL_MASK, ci, src);
+        const unsigned bm = __ballot_sync(FULL_MASK, lane < P && better(xv, xi, tv, ti));
         if (bm) {
-          int at = __ffs(bm) - 1;
-          float upv = __shfl_up_sync(FULL_MASK, tv, 1);
-          int upi = __shfl_up_sync(FULL_MASK, ti, 1);
+          const int at = __ffs(bm) - 1;
+          const float upv = __shfl_up_sync(FULL_MASK, tv, 1);
+          const int upi = __shfl_up_sync(FULL_MASK, ti, 1);
           if (lane > at && lane < P) { tv = upv; ti = upi; }
-          if (lane == at) { tv = cv; ti = ci; }
-          thv = __shfl_sync(FULL_MASK, tv, P - 1);
-          thi = __shfl_sync(FULL_MASK, ti, P - 1);
+          if (lane == at) { tv = xv; ti = xi; }
         }
       }
+    } else {
+      // many candidates: bitonic sort of the 32 (best first), then a bitonic merge of
+      // the best Pp of them with the list (Pp = P rounded up to a power of two <= 16)
+#pragma unroll
+      for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          const float ov = __shfl_xor_sync(FULL_MASK, cv, jj);
+          const int oi = __shfl_xor_sync(FULL_MASK, ci, jj);
+          const bool want_better = (((lane & jj) == 0) == ((lane & kk) == 0));
+          const bool ob = better(ov, oi, cv, ci);
+          if (want_better == ob) { cv = ov; ci = oi; }
+        }
+      }
+      int Pp = 1;
+      while (Pp < P) Pp <<= 1;
+      const float nv = __shfl_sync(FULL_MASK, cv, (2 * Pp - 1 - lane) & 31);
+      const int ni = __shfl_sync(FULL_MASK, ci, (2 * Pp - 1 - lane) & 31);
+      float mv = (lane < Pp) ? tv : nv;
+      int mi = (lane < Pp) ? ti : ni;
+      for (int jj = Pp; jj > 0; jj >>= 1) {
+        const float ov = __shfl_xor_sync(FULL_MASK, mv, jj);
+        const int oi = __shfl_xor_sync(FULL_MASK, mi, jj);
+        const bool want_better = (lane & jj) == 0;
+        const bool ob = better(ov, oi, mv, mi);
+        if (want_better == ob) { mv = ov; mi = oi; }
+      }
+      if (lane < P) { tv = mv; ti = mi; }
     }
+    thv = __shfl_sync(FULL_MASK, tv, P - 1);
+    thi = __shfl_sync(FULL_MASK, ti, P - 1);
   }
   const int kept = (int)((hi - lo) < (long long)P ? (hi - lo) : (long long)P);
   int rank = 0;
