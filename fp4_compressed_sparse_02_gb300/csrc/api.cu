@@ -40,6 +40,8 @@ csa2_status check_cache(const csa2_cache& c, bool need_codes, bool need_idx) {
           c.page_size);
   REQUIRE(c.num_pages > 0 && c.num_seqs > 0 && c.max_pages > 0, CSA2_ERR_INVALID_ARG,
           "cache.num_pages/num_seqs/max_pages must be positive");
+  REQUIRE(c.num_pages <= (1 << 25), CSA2_ERR_UNSUPPORTED_SHAPE,
+          "cache.num_pages must be <= 2^25 (row indices are 31-bit)");
   REQUIRE(c.d == 128 || c.d == 512, CSA2_ERR_UNSUPPORTED_SHAPE, "cache.d must be 128 or 512 (got %d)", c.d);
   if (need_codes) REQUIRE(c.codes && c.scales, CSA2_ERR_INVALID_ARG, "cache.codes/scales is NULL");
   if (need_idx) {

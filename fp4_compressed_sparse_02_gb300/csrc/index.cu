@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace csa2 {
 
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
 }
 
 // ---------------------------------------------------------------------------------
-// Reindex scoring: scores of the pool entries of each query.
+// Reindex scoring parameters (the scoring itself runs inside k_select_cl).
 // ---------------------------------------------------------------------------------
 struct PoolScoreParams {
   const uint16_t* q;
@@ -235,51 +236,11 @@ struct PoolScoreParams {
   float* score;           // [B][stride]
 };
 
-template <int DK, int NHG>
-__global__ void __launch_bounds__(256) k_pool_scores(PoolScoreParams p) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int b = blockIdx.y;
-  const int pos0 = (blockIdx.x * 8 + warp) * 32;
-  if (pos0 >= p.stride) return;
-  int plen = __ldg(p.pool_len + b);
-  if (plen < 0 || plen > p.stride) {
-    if (lane == 0 && pos0 == 0) raise_error(&g_err_index, CSA2_DEVERR_POOL_ENTRY);
-    plen = max(0, min(plen, p.stride));
-  }
-  if (pos0 >= plen) return;
-  const int s = __ldg(p.seq_of + b);
-  QFrag<DK, NHG> f;
-  load_qfrag<DK, NHG>(p.q + (long long)b * p.H_i * DK, p.w + (long long)b * p.H_i, p.H_i, f);
-  int pos[4] = {pos0 + g, pos0 + g + 8, pos0 + 16 + g, pos0 + 24 + g};
-  uint4 A[4][DK / 32];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    long long row = -1;
-    if (pos[t] < plen) {
-      int e = __ldg(p.pool + (long long)b * p.stride + pos[t]);
-      row = (e >= 0) ? entry_row(p.cache, s, e, &g_err_index) : -1;
-    }
-    load_row<DK>(p.cache.idx_k, row, A[t]);
-  }
-  float sc[4];
-  tile_scores<DK, NHG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
-  tile_scores<DK, NHG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
-  if (c == 0) {
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-      if (pos[t] < plen) p.score[(long long)b * p.stride + pos[t]] = sc[t];
-  }
-}
-
 // ---------------------------------------------------------------------------------
 // Exact Top-k of up to 16,384 scored candidates per query: 4-pass radix select of the
 // k-th largest key, then ties at that key taken in ascending position, output in
-// ascending position (= ascending entry, the pool being ascending).  One CTA per query.
+// ascending position (= ascending entry, the pool being ascending).
 // ---------------------------------------------------------------------------------
-constexpr int SEL_THREADS = 1024;
-constexpr int SEL_PER_THREAD = 16;
-
 __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int x = v;
@@ -321,12 +282,30 @@ struct SelectParams {
   int* topk_len;
 };
 
-__global__ void __launch_bounds__(SEL_THREADS) k_select(SelectParams p) {
-  __shared__ int hist[256];
+// ---------------------------------------------------------------------------------
+// Cluster Top-k: the candidates of one query are split over a cluster of NCL CTAs
+// (2,048 each at most).  Radix-select histograms and the compaction offsets are
+// combined through distributed shared memory, so every pass runs on NCL SMs at once.
+// With SCORE the CTAs first score their slice of the pool (Reindex) into shared
+// memory; otherwise they read the scores the Full scan wrote (and finish the pool).
+// ---------------------------------------------------------------------------------
+constexpr int NCL = 8;
+constexpr int CL_THREADS = 256;
+constexpr int CL_SLICE = 16384 / NCL;                 // 2048
+constexpr int CL_PER_T = CL_SLICE / CL_THREADS;       // 8
+
+template <int DK, int NHG, bool SCORE>
+__global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_select_cl(SelectParams p, PoolScoreParams sp) {
+  __shared__ float sscore[SCORE ? CL_SLICE : 1];
+  __shared__ int hist[2][256];
+  __shared__ int total[256];
   __shared__ int scan_sh[32];
   __shared__ int pick[2];
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x;
+  __shared__ int xfer[2];
+  __shared__ int base_sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.y;
+  const int rank = (int)tc::cluster_ctarank();
   int P;
   if (p.n_vis) {
     int n = __ldg(p.n_vis + b);
@@ -334,48 +313,114 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(SelectParams p) {
     P = min(n, p.stride);
   } else {
     P = __ldg(p.pool_len_in + b);
-    P = max(0, min(P, p.stride));
+    if (P < 0 || P > p.stride) {
+      if (tid == 0 && rank == 0) raise_error(&g_err_index, CSA2_DEVERR_POOL_ENTRY);
+      P = max(0, min(P, p.stride));
+    }
   }
   const long long rowb = (long long)b * p.stride;
-  if (p.pool_len_out && tid == 0) p.pool_len_out[b] = P;
-  if (p.pool_out)
-    for (int i = P + tid; i < p.stride; i += blockDim.x) p.pool_out[rowb + i] = -1;
+  const int S = (p.stride + NCL - 1) / NCL;
+  const int s0 = rank * S, s1 = min(p.stride, s0 + S);
   const int k = p.k;
   int* out = p.topk + (long long)b * k;
-  if (P <= k) {
-    for (int i = tid; i < k; i += blockDim.x) out[i] = (i < P) ? p.pool[rowb + i] : -1;
-    if (tid == 0) p.topk_len[b] = P;
+  if (p.pool_len_out && tid == 0 && rank == 0) p.pool_len_out[b] = P;
+  if (p.pool_out)
+    for (int i = max(P, s0) + tid; i < s1; i += CL_THREADS) p.pool_out[rowb + i] = -1;
+  if (P <= k) {                                           // every candidate is selected
+    for (int i = s0 + tid; i < min(s1, P); i += CL_THREADS) out[i] = p.pool[rowb + i];
+    for (int i = P + rank * CL_THREADS + tid; i < k; i += NCL * CL_THREADS) out[i] = -1;
+    if (tid == 0 && rank == 0) p.topk_len[b] = P;
     return;
   }
-  uint32_t key[SEL_PER_THREAD];
-  const int p0 = tid * SEL_PER_THREAD;
+  const int e1 = min(s1, P);                              // valid positions [s0, e1)
+  if constexpr (SCORE) {
+    // ---- score this CTA's slice of the pool (Reindex).  Warp w owns tiles w, w+8, ...
+    //      of 32 positions (at most 8).  All of its rows are resolved first (pool id ->
+    //      page table), then tiles stream two at a time so 16 KB per warp are in flight.
+    constexpr int NT = CL_SLICE / 32 / (CL_THREADS / 32);   // tiles per warp: 8
+    const int g = lane >> 2, c = lane & 3;
+    const int sq = __ldg(sp.seq_of + b);
+    QFrag<DK, NHG> f;
+    load_qfrag<DK, NHG>(sp.q + (long long)b * sp.H_i * DK, sp.w + (long long)b * sp.H_i, sp.H_i, f);
+    int ent[NT][4];
 #pragma unroll
-  for (int i = 0; i < SEL_PER_THREAD; ++i) {
-    int q = p0 + i;
-    key[i] = (q < P) ? float_key(p.score[rowb + q]) : 0u;
+    for (int it = 0; it < NT; ++it)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int pos = s0 + 32 * (warp + 8 * it) + g + 8 * t;
+        ent[it][t] = (pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
+      }
+    int rw[NT][4];
+#pragma unroll
+    for (int it = 0; it < NT; ++it)
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        rw[it][t] = (ent[it][t] >= 0) ? (int)entry_row(sp.cache, sq, ent[it][t], &g_err_index) : -1;
+#pragma unroll
+    for (int it = 0; it < NT; it += 2) {
+      if (s0 + 32 * (warp + 8 * it) >= e1) break;
+      uint4 A[2][4][DK / 32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) load_row<DK>(sp.cache.idx_k, rw[it + u][t], A[u][t]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float sc[4];
+        tile_scores<DK, NHG>(f, A[u][0], A[u][1], sp.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, NHG>(f, A[u][2], A[u][3], sp.relu != 0, sc[2], sc[3]);
+        if (c == 0) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int pos = s0 + 32 * (warp + 8 * (it + u)) + g + 8 * t;
+            if (pos < e1) sscore[pos - s0] = sc[t];
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // ---- keys: 8 consecutive positions per thread ----------------------------------------
+  uint32_t key[CL_PER_T];
+  const int q0 = s0 + tid * CL_PER_T;
+#pragma unroll
+  for (int i = 0; i < CL_PER_T; ++i) {
+    const int q = q0 + i;
+    float sv = 0.f;
+    if (q < e1) sv = SCORE ? sscore[q - s0] : p.score[rowb + q];
+    key[i] = (q < e1) ? float_key(sv) : 0u;
   }
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (tid < 256) hist[tid] = 0;
+    int* hb = hist[pass & 1];
+    hb[tid] = 0;
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < SEL_PER_THREAD; ++i)
-      if (p0 + i < P && (key[i] & mask) == prefix) atomicAdd(&hist[(key[i] >> shift) & 255], 1);
+    for (int i = 0; i < CL_PER_T; ++i)
+      if (q0 + i < e1 && (key[i] & mask) == prefix) atomicAdd(&hb[(key[i] >> shift) & 255], 1);
+    tc::cluster_sync();
+    {
+      const uint32_t ha = smem_u32(&hb[tid]);
+      int tsum = 0;
+#pragma unroll
+      for (int cc = 0; cc < NCL; ++cc) tsum += tc::ld_dsmem_s32(tc::mapa(ha, cc));
+      total[tid] = tsum;
+    }
     __syncthreads();
     if (tid < 32) {
       int cnt[8], local = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { cnt[i] = hist[255 - 8 * tid - i]; local += cnt[i]; }
+      for (int i = 0; i < 8; ++i) { cnt[i] = total[255 - 8 * tid - i]; local += cnt[i]; }
       int incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(FULL_MASK, incl, o);
+        const int y = __shfl_up_sync(FULL_MASK, incl, o);
         if (tid >= o) incl += y;
       }
-      int excl = incl - local;
+      const int excl = incl - local;
       if (excl < remaining && remaining <= incl) {
         int cum = excl;
 #pragma unroll
@@ -393,31 +438,49 @@ __global__ void __launch_bounds__(SEL_THREADS) k_select(SelectParams p) {
     prefix |= ((uint32_t)pick[0]) << shift;
     mask |= 0xFFu << shift;
     remaining = pick[1];
-    __syncthreads();
   }
-  // ties at the threshold key: the lowest positions first
+  // ---- ties at the threshold key go to the lowest positions, cluster-wide ---------------
   int eq = 0;
 #pragma unroll
-  for (int i = 0; i < SEL_PER_THREAD; ++i) eq += (p0 + i < P && key[i] == prefix) ? 1 : 0;
-  int tot;
-  int eqrank = block_exclusive_scan(eq, scan_sh, tot);
+  for (int i = 0; i < CL_PER_T; ++i) eq += (q0 + i < e1 && key[i] == prefix) ? 1 : 0;
+  int eq_tot;
+  int eqrank = block_exclusive_scan(eq, scan_sh, eq_tot);
+  if (tid == 0) xfer[0] = eq_tot;
+  tc::cluster_sync();
+  if (tid == 0) {
+    int bsum = 0;
+    for (int cc = 0; cc < rank; ++cc) bsum += tc::ld_dsmem_s32(tc::mapa(smem_u32(&xfer[0]), cc));
+    base_sh = bsum;
+  }
+  __syncthreads();
+  eqrank += base_sh;
   unsigned selmask = 0;
   int nsel = 0;
 #pragma unroll
-  for (int i = 0; i < SEL_PER_THREAD; ++i) {
+  for (int i = 0; i < CL_PER_T; ++i) {
     bool sel = false;
-    if (p0 + i < P) {
+    if (q0 + i < e1) {
       if (key[i] > prefix) sel = true;
       else if (key[i] == prefix) { sel = eqrank < remaining; ++eqrank; }
     }
     if (sel) { selmask |= 1u << i; ++nsel; }
   }
-  int o = block_exclusive_scan(nsel, scan_sh, tot);
+  int sel_tot;
+  int o = block_exclusive_scan(nsel, scan_sh, sel_tot);
+  if (tid == 0) xfer[1] = sel_tot;
+  tc::cluster_sync();
+  if (tid == 0) {
+    int bsum = 0;
+    for (int cc = 0; cc < rank; ++cc) bsum += tc::ld_dsmem_s32(tc::mapa(smem_u32(&xfer[1]), cc));
+    base_sh = bsum;
+  }
+  __syncthreads();
+  o += base_sh;
 #pragma unroll
-  for (int i = 0; i < SEL_PER_THREAD; ++i)
-    if ((selmask & (1u << i)) && o < k) out[o++] = p.pool[rowb + p0 + i];
-  for (int i = tot + tid; i < k; i += blockDim.x) out[i] = -1;
-  if (tid == 0) p.topk_len[b] = tot;
+  for (int i = 0; i < CL_PER_T; ++i)
+    if ((selmask & (1u << i)) && o < k) out[o++] = p.pool[rowb + q0 + i];
+  if (tid == 0 && rank == 0) p.topk_len[b] = k;
+  tc::cluster_sync();                                   // no CTA leaves while others read it
 }
 
 // ---------------------------------------------------------------------------------
@@ -430,16 +493,6 @@ static void launch_scan_dk(const ScanParams& sp, int nhg, dim3 grid, cudaStream_
     case 2: k_full_scan<DK, 2><<<grid, 256, 0, st>>>(sp); break;
     case 3: k_full_scan<DK, 3><<<grid, 256, 0, st>>>(sp); break;
     default: k_full_scan<DK, 4><<<grid, 256, 0, st>>>(sp); break;
-  }
-}
-
-template <int DK>
-static void launch_pool_scores_dk(const PoolScoreParams& pp, int nhg, dim3 grid, cudaStream_t st) {
-  switch (nhg) {
-    case 1: k_pool_scores<DK, 1><<<grid, 256, 0, st>>>(pp); break;
-    case 2: k_pool_scores<DK, 2><<<grid, 256, 0, st>>>(pp); break;
-    case 3: k_pool_scores<DK, 3><<<grid, 256, 0, st>>>(pp); break;
-    default: k_pool_scores<DK, 4><<<grid, 256, 0, st>>>(pp); break;
   }
 }
 
@@ -478,7 +531,8 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sel.k = a.k;
   sel.topk = a.topk;
   sel.topk_len = a.topk_len;
-  k_select<<<a.B, SEL_THREADS, 0, st>>>(sel);
+  PoolScoreParams none{};
+  k_select_cl<128, 1, false><<<dim3(NCL, a.B), CL_THREADS, 0, st>>>(sel, none);
   return cudaGetLastError();
 }
 
@@ -486,7 +540,19 @@ size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a) {
   return (size_t)a.B * a.pool_stride * sizeof(float);
 }
 
+template <int DK>
+static void launch_reindex_dk(const SelectParams& sel, const PoolScoreParams& pp, int nhg, int B, cudaStream_t st) {
+  const dim3 grid(NCL, B);
+  switch (nhg) {
+    case 1: k_select_cl<DK, 1, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
+    case 2: k_select_cl<DK, 2, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
+    case 3: k_select_cl<DK, 3, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
+    default: k_select_cl<DK, 4, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
+  }
+}
+
 cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st) {
+  (void)ws;
   if (a.B == 0) return cudaSuccess;
   PoolScoreParams pp{};
   pp.q = a.q_idx;
@@ -498,20 +564,16 @@ cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cud
   pp.stride = a.pool_stride;
   pp.H_i = a.H_i;
   pp.relu = a.relu;
-  pp.score = static_cast<float*>(ws);
-  const int nhg = (a.H_i + 7) / 8;
-  dim3 grid((a.pool_stride + 255) / 256, a.B);
-  if (a.cache.d_ik == 128) launch_pool_scores_dk<128>(pp, nhg, grid, st);
-  else launch_pool_scores_dk<64>(pp, nhg, grid, st);
   SelectParams sel{};
-  sel.score = static_cast<const float*>(ws);
   sel.pool = a.pool;
   sel.stride = a.pool_stride;
   sel.pool_len_in = a.pool_len;
   sel.k = a.k;
   sel.topk = a.topk;
   sel.topk_len = a.topk_len;
-  k_select<<<a.B, SEL_THREADS, 0, st>>>(sel);
+  const int nhg = (a.H_i + 7) / 8;
+  if (a.cache.d_ik == 128) launch_reindex_dk<128>(sel, pp, nhg, a.B, st);
+  else launch_reindex_dk<64>(sel, pp, nhg, a.B, st);
   return cudaGetLastError();
 }
 

@@ -155,6 +155,12 @@ __device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ int ld_dsmem_s32(uint32_t caddr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(caddr));
+  return v;
+}
+
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t caddr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr));

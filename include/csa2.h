@@ -63,7 +63,8 @@ typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 
 #define CSA2_PAGE_SIZE 64
 
-/* Paged cache planes (all device).  d in {128, 512}; d_ik in {64, 128}. */
+/* Paged cache planes (all device).  d in {128, 512}; d_ik in {64, 128};
+ * num_pages <= 2^25 (2^31 entries). */
 typedef struct csa2_cache {
   uint8_t* codes;              /* [num_pages][64][d/2]  E2M1 pairs, even channel in the low nibble */
   uint8_t* scales;             /* [num_pages][64][d/16] E4M3 scale of each 16 channels */
