@@ -132,6 +132,7 @@ csa2_status check_attn(const csa2_attn_args* a) {
   REQUIRE(a->out_dtype == CSA2_BF16 || a->out_dtype == CSA2_F32, CSA2_ERR_INVALID_ARG, "bad out_dtype");
   if (a->B > 0) {
     REQUIRE(a->q && a->seq_of && a->out, CSA2_ERR_INVALID_ARG, "q/seq_of/out is NULL");
+    REQUIRE(((uintptr_t)a->q & 15) == 0, CSA2_ERR_INVALID_ARG, "q must be 16-byte aligned");
     if (a->k > 0) REQUIRE(a->topk, CSA2_ERR_INVALID_ARG, "topk is NULL");
     if (a->swa_max > 0)
       REQUIRE(a->swa && a->swa_scale && a->swa_start && a->swa_len && a->swa_rows > 0, CSA2_ERR_INVALID_ARG,

@@ -15,6 +15,8 @@
 #include "internal.h"
 #include "tc.cuh"
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cstdlib>
 
 namespace csa2 {
@@ -348,21 +350,26 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // tcgen05 path for d = 512, Hq = 64, k <= 512, swa_max <= 128 (the model's shape).
 // CTA (chunk c of 4, query b), 256 threads.  The chunk's keys are the selected-entry
 // slots [128c, 128c+128) and the window rows [32c, 32c+32): 160 keys, so a query needs
-// 4 CTAs and a decode batch of 32 fills the GPU in one wave.
-//   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle), 160 KB
-//   TMEM   : Q (A operand, two fp16 per column)                         cols   0..255
-//            S = Q K^T (fp32, 160 columns)                              cols 256..415
-//            P = softmax numerators (fp16 pairs, A operand)             cols 256..335
-//            O half = P V (fp32, 256 dims)                              cols   0..255
-//   MMA1  S[64 x 160] = Q[tmem] . KV^T        (B K-major)
+// 4 CTAs and a decode batch of 32 fills the GPU in one wave.  The 4 CTAs of a query form
+// a thread-block cluster.
+//   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle)      160 KB
+//            Q 64 heads x 512 dims (K-major, 128-byte swizzle)                    64 KB
+//            Q arrives by TMA: each CTA of the cluster loads two 64-dim boxes and
+//            multicasts them to all four, so Q is read from memory once per query;
+//            it is converted bf16 -> fp16 in place.
+//   TMEM   : S = Q K^T (fp32, 160 columns)                              cols   0..159
+//            P = softmax numerators (fp16 pairs, A operand)             cols   0..79
+//            O half = P V (fp32, 256 dims)                              cols 256..511
+//   MMA1  S[64 x 160] = Q[smem] . KV^T        (A, B K-major)
 //   MMA2  O[64 x 256] = P[tmem] . KV[:, half] (B MN-major: the same tile read along
 //         the other axis), once per half of the 512 dims
-// With M = 64 the 64 heads occupy lanes 0..15 of each of the four lane quarters, so all
-// eight warps (two per quarter, each taking half of the keys or dims) share the
-// softmax, the Q transfer and the epilogue.  A head's softmax is a row of one thread.
-// The 4 chunk CTAs of a query form a thread-block cluster: each writes o = O / l (fp16)
-// and (max, l) per head into its own shared memory, and after a cluster barrier CTA r
-// merges heads [16 r, 16 r + 16) of all four chunks through distributed shared memory.
+// With M = 64 the 64 heads occupy lanes 0..15 of each of the four TMEM lane quarters, so
+// all eight warps (two per quarter, each taking half of the keys or dims) share the
+// softmax and the epilogue.  A head's softmax is a row of one thread.
+// Each CTA computes o = O / l (fp16) and (max, l) per head of its chunk; CTA r owns the
+// merge of heads [16 r, 16 r + 16): the others send it their blocks of those heads with
+// shared-to-shared bulk copies (into its Q space, free after its first product), and it
+// combines the 4 chunks from its own shared memory.
 // ---------------------------------------------------------------------------------
 namespace tca {
 constexpr int THREADS = 256;
@@ -374,10 +381,25 @@ constexpr int KW = 32;                          // window rows per chunk
 constexpr int NK = KT + KW;                     // keys per chunk
 constexpr int ATOM = NK / 8 * 1024;             // bytes per 64-dim K-atom of the KV tile
 constexpr int SM_KV = NK * DIM * 2;             // 163840
-constexpr int SMEM = SM_KV + 1024;              // + alignment slack
+constexpr int SM_Q = HQ * DIM * 2;             // 65536
+struct Misc {                                   // small per-CTA state, after the tiles
+  int keyok[NK];
+  float pmax[2][HQ];
+  float psum[2][HQ];
+  float linv[HQ];
+  alignas(16) float2 mlx[HQ];     // this chunk's (row max in log2 units, row sum) per head
+  alignas(16) float2 rml[NCH - 1][HQ / NCH];   // received (max, sum) of the other chunks
+  uint64_t mbar[5];
+  uint32_t tslot;
+  int ok_flag;
+};
+constexpr int SMEM = SM_KV + SM_Q + (int)sizeof(Misc);   // no static shared memory
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 256;
+constexpr uint32_t COL_S = 0;               // S, then P over its first 80 columns
+constexpr uint32_t COL_O = 256;               // one half of O
 constexpr uint32_t MAX_POLL = 1u << 22;
+constexpr int BLK = HQ / NCH * DIM * 2;         // one CTA's merge block: 16 heads x 512 dims fp16
+constexpr uint32_t RECV_BYTES = (NCH - 1) * (BLK + HQ / NCH * 8);
 
 // byte offset of 16-byte chunk ch (8 fp16) of row r in the K-major KV tile
 __device__ __forceinline__ uint32_t kvoff(int r, int ch) {
@@ -391,43 +413,47 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 }
 }  // namespace tca
 
-__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
+__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1)
+    k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap) {
   using namespace tca;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sKV = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ int keyok[NK];
-  __shared__ float pmax[2][HQ];
-  __shared__ float psum[2][HQ];
-  __shared__ float linv[HQ];
-  __shared__ float2 mlx[HQ];                 // this chunk's (row max in log2 units, row sum)
-  __shared__ uint32_t tslot;
-  __shared__ int ok_flag;
-  __shared__ __align__(8) uint64_t mbar[3];
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* sKV = smem;
+  uint8_t* sQ = smem + SM_KV;
+  Misc& ms = *reinterpret_cast<Misc*>(smem + SM_KV + SM_Q);
+  int* keyok = ms.keyok;
+  float (*pmax)[HQ] = ms.pmax;
+  float (*psum)[HQ] = ms.psum;
+  float* linv = ms.linv;
+  float2* mlx = ms.mlx;
+  uint64_t* mbar = ms.mbar;
+  int& ok_flag = ms.ok_flag;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y, chunk = blockIdx.x;
-  const uint32_t kv_a = smem_u32(sKV);
+  if ((smem_u32(smem) & 1023) != 0) {           // the same in every CTA: all return together
+    if (tid == 0) raise_error(&g_err_attn, CSA2_DEVERR_SMEM_ALIGN);
+    return;
+  }
+  const uint32_t kv_a = smem_u32(sKV), q_a = smem_u32(sQ);
   // M = 64 tensor-memory layout: head h sits in lane 32 * (h / 16) + h % 16, so warp w
   // (lane quarter w % 4) owns heads [16 (w % 4), 16 (w % 4) + 16) in its lanes 0..15 and
   // warp >> 2 picks a half of the columns; lanes 16..31 mirror lanes 0..15 and write
   // nothing that is read.
-  const bool hw = true;
   const bool lv = lane < 16;
   const int head = 16 * (warp & 3) + (lane & 15);
   const int kh = warp >> 2;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (warp == 0) tc::tmem_alloc(&tslot, TMEM_COLS);
+  if (warp == 0) tc::tmem_alloc(&ms.tslot, TMEM_COLS);
   if (tid == 32) {
     tc::mbar_init(&mbar[0], 1);
     tc::mbar_init(&mbar[1], 1);
     tc::mbar_init(&mbar[2], 1);
+    tc::mbar_init(&mbar[3], 1);
+    tc::mbar_init(&mbar[4], 1);
+    tc::mbar_arrive_expect_tx(&mbar[3], SM_Q);   // the four multicast halves of Q
+    tc::mbar_arrive_expect_tx(&mbar[4], RECV_BYTES);   // the other chunks' merge blocks
   }
-  // ---- Q loads in flight first (16 x 16 B per thread) ------------------------------------
-  const uint4* qg = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
-  uint4 qv[HQ * DIM / 8 / THREADS];
-#pragma unroll
-  for (int i = 0; i < HQ * DIM / 8 / THREADS; ++i) qv[i] = __ldg(qg + tid + i * THREADS);
   // ---- each thread resolves the keys it gathers: FP4 slot fkey (2 threads per key) and
   //      window row skey (8 threads per key), then issues those loads at once -------------
   const int fkey = tid >> 1, half = tid & 1;
@@ -471,39 +497,21 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   if (half == 0) keyok[fkey] = fok;
   if (part == 0) keyok[skey] = sok;
-  // ---- Q -> fp16 staging rows in shared memory (16-byte chunk c of head h stored at
-  //      chunk c ^ (h % 8), so both the row-wise writes and the per-head reads spread
-  //      over all banks) -------------------------------------------------------------
-#pragma unroll
-  for (int i = 0; i < HQ * DIM / 8 / THREADS; ++i) {
-    const int idx = tid + i * THREADS;
-    const int h = idx >> 6, ch = idx & 63;
-    const uint4 v = qv[i];
-    *reinterpret_cast<uint4*>(sKV + h * 1024 + ((ch ^ (h & 7)) << 4)) =
-        make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-  }
+  // ---- Q: every CTA's barrier is initialised and expecting its bytes before any CTA
+  //      multicasts; CTA r loads the 64-dim boxes 2r and 2r + 1 for the whole cluster --------
   tc::fence_before_sync();
+  tc::cluster_arrive_relaxed();
+  tc::cluster_wait();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tb = tslot;
-  // ---- staged Q rows -> TMEM (A operand, two fp16 per column) while the gather flies ---
-  if (hw) {
+  const uint32_t tb = ms.tslot;
+  if (tid == 0) {
+    const int rank = (int)tc::cluster_ctarank();
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {               // 8 chunks = 64 dims = 32 columns per round
-      uint32_t w[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ch = kh * 32 + r * 8 + j;
-        const uint4 v = *reinterpret_cast<const uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4));
-        w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-      }
-      tc::tmem_st32(tb + lane_base + kh * 128 + r * 32, w);
-    }
-    tc::tmem_st_wait();
+    for (int kb = 2 * rank; kb < 2 * rank + 2; ++kb)
+      tc::tma_load_2d_multicast(sQ + kb * 8192, &qmap, 64 * kb, HQ * b, &mbar[3], (uint16_t)((1u << NCH) - 1));
   }
-  tc::fence_before_sync();
-  __syncthreads();                              // staging reads done: the tile may be overwritten
-  // ---- dequantise into the K-major KV tile ----------------------------------------------
+  // ---- dequantise the gathered rows into the K-major KV tile ----------------------------
   if (fok) {
     const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
@@ -549,48 +557,80 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
     for (int t = 0; t < 8; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(skey, part * 8 + t)) = make_uint4(0, 0, 0, 0);
   }
+  // ---- Q arrived: bf16 -> fp16 in place (the swizzled layout is kept element for element)
+  if (tid == 0) {
+    ok_flag = wait_mma(&mbar[3], 0) ? 1 : 0;
+  }
+  __syncthreads();
+  if (ok_flag) {
+#pragma unroll
+    for (int i = 0; i < SM_Q / 16 / THREADS; ++i) {
+      uint4* qp = reinterpret_cast<uint4*>(sQ) + tid + i * THREADS;
+      const uint4 v = *qp;
+      *qp = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    }
+  }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   // ---- MMA1: S = Q K^T -----------------------------------------------------------------
-  if (tid == 0) {
+  if (tid == 0 && ok_flag) {
     constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
 #pragma unroll 4
     for (int ks = 0; ks < DIM / 16; ++ks) {
+      const uint64_t ad = tc::smem_desc_sw128(q_a + (ks >> 2) * (HQ * 128) + (ks & 3) * 32, 16, 1024);
       const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
-      tc::mma_f16_ts(tb + COL_S, tb + ks * 8, bd, id1, ks > 0);
+      tc::mma_f16_ss(tb + COL_S, ad, bd, id1, ks > 0);
     }
     tc::mma_commit(&mbar[0]);
     ok_flag = wait_mma(&mbar[0], 0) ? 1 : 0;
   }
   __syncthreads();
   tc::fence_after_sync();
-  // ---- softmax: head = lane row; two threads split the 160 keys ([80 kh, 80 kh + 80)) -
+  // Q is no longer read (the first product has completed): the cluster may now send
+  // merge blocks into its space.  Nothing written before this point is read by another
+  // CTA, so the arrive need not release.
+  tc::cluster_arrive_relaxed();
+  // ---- softmax: head = lane row; two threads (warps w and w ^ 4) split the 160 keys ------
   float e[80];
-  if (ok_flag && hw) {
+  if (ok_flag) {
     uint32_t r[96];
     tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh, r);
     tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 32, r + 32);
     tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 64, r + 64);
     tc::tmem_ld_wait();
+    const int4* ok4 = reinterpret_cast<const int4*>(keyok + 80 * kh);
     float mx = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 80; ++j) {
-      e[j] = keyok[80 * kh + j] ? __uint_as_float(r[j]) * p.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, e[j]);
+    for (int j4 = 0; j4 < 20; ++j4) {
+      const int4 v = ok4[j4];
+      const int okv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int j = 4 * j4 + t;
+        e[j] = okv[t] ? __uint_as_float(r[j]) * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, e[j]);
+      }
     }
     if (lv) pmax[kh][head] = mx;
   }
-  __syncthreads();
-  if (ok_flag && hw) {
+  // the two warps of a lane quarter exchange their halves' maxima; both have read S, so
+  // P may now overwrite it
+  tc::fence_before_sync();
+  asm volatile("bar.sync %0, 64;" :: "r"(1 + (warp & 3)) : "memory");
+  tc::fence_after_sync();
+  if (ok_flag) {
     const float m = fmaxf(pmax[0][head], pmax[1][head]);
     float l = 0.f;
     uint32_t pk[40];
 #pragma unroll
     for (int j = 0; j < 80; j += 2) {
-      const float x0 = (m == -INFINITY) ? 0.f : exp2f(e[j] - m);
-      const float x1 = (m == -INFINITY) ? 0.f : exp2f(e[j + 1] - m);
+      float x0 = 0.f, x1 = 0.f;
+      if (m != -INFINITY) {
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x0) : "f"(e[j] - m));
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x1) : "f"(e[j + 1] - m));
+      }
       const __half2 hp = __floats2half2_rn(x0, x1);
       pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
       l += __low2float(hp) + __high2float(hp);
@@ -599,7 +639,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     tc::tmem_st8(tb + lane_base + COL_S + 40 * kh + 32, pk + 32);
     tc::tmem_st_wait();
     if (lv) psum[kh][head] = l;
-    if (lv && kh == 0) linv[head] = m;           // row max, consumed just below
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -607,12 +646,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   if (tid < HQ) {
     const float l = psum[0][tid] + psum[1][tid];
     const bool any = ok_flag && l > 0.f;
-    mlx[tid] = any ? make_float2(linv[tid], l) : make_float2(-INFINITY, 0.f);
+    mlx[tid] = any ? make_float2(fmaxf(pmax[0][tid], pmax[1][tid]), l) : make_float2(-INFINITY, 0.f);
     linv[tid] = any ? 1.f / l : 0.f;
   }
-  // ---- MMA2 in two halves of 256 dims; each epilogue writes o = O / l (fp16) into this
-  //      CTA's shared memory: row h (1 KB), 16-byte chunk c at c ^ (h % 8).  Half 0 lands
-  //      in K-atoms 0..3 of the tile, which half 1 of MMA2 no longer reads. -------------
+  // ---- MMA2 per half of 256 dims into cols 256..511, each half followed by its epilogue:
+  //      o = O / l (fp16) into this CTA's shared memory, row h (1 KB) with 16-byte chunk c
+  //      at c ^ (h % 8).  Half 0 lands in K-atoms 0..3 of the KV tile, which the second
+  //      MMA2 no longer reads; half 1 is written after that MMA completes. -----------------
 #pragma unroll 1
   for (int hf = 0; hf < 2; ++hf) {
     if (tid == 0 && ok_flag) {
@@ -620,32 +660,33 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
       for (int ks = 0; ks < NK / 16; ++ks) {
         const uint64_t bd = tc::smem_desc_sw128(kv_a + (4 * hf) * ATOM + (2 * ks) * 1024, ATOM, 1024);
-        tc::mma_f16_ts(tb, tb + COL_S + ks * 8, bd, id2, ks > 0);
+        tc::mma_f16_ts(tb + COL_O, tb + COL_S + ks * 8, bd, id2, ks > 0);
       }
       tc::mma_commit(&mbar[1 + hf]);
       ok_flag = wait_mma(&mbar[1 + hf], 0) ? 1 : 0;
     }
     __syncthreads();
     tc::fence_after_sync();
-    if (ok_flag) {                                 // tcgen05.ld is warp-wide; only lanes 0..15 store
+    if (ok_flag) {                                 // tcgen05.ld is warp-wide; lanes 0..15 store
       const float li = linv[head];
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {            // 32 columns = 32 dims = 4 chunks
         uint32_t r[32];
-        tc::tmem_ld32(tb + lane_base + 128 * kh + 32 * c4, r);
+        tc::tmem_ld32(tb + lane_base + COL_O + 128 * kh + 32 * c4, r);
         tc::tmem_ld_wait();
+        if (lv) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t pk[4];
+          for (int i = 0; i < 4; ++i) {
+            uint32_t pk[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
-                                                 __uint_as_float(r[8 * i + 2 * t + 1]) * li);
-            pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          const int ch = 32 * hf + 16 * kh + 4 * c4 + i;
-          if (lv)
+            for (int t = 0; t < 4; ++t) {
+              const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
+                                                   __uint_as_float(r[8 * i + 2 * t + 1]) * li);
+              pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
+            }
+            const int ch = 32 * hf + 16 * kh + 4 * c4 + i;
             *reinterpret_cast<uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
         }
       }
     }
@@ -653,19 +694,36 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     __syncthreads();
     tc::fence_after_sync();
   }
-  // ---- merge across the cluster: CTA r combines heads [16 r, 16 r + 16) of the 4 chunks --
-  tc::cluster_sync();
+  // ---- merge: CTA r owns heads [16 r, 16 r + 16).  Each CTA sends the block of every
+  //      other CTA (16 heads x 1 KB of its fp16 o, then their 16 (max, sum) pairs) into that
+  //      CTA's former Q space by bulk copies, then combines the 4 chunks of its own heads
+  //      from local shared memory.  Slot j of CTA r holds chunk (r + 1 + j) % 4. ----------
+  const int rank = (int)tc::cluster_ctarank();
+  tc::fence_proxy_async_smem();                 // epilogue stores -> bulk-copy reads
+  __syncthreads();
+  tc::cluster_wait();                           // every CTA has finished MMA1
+  if (tid == 0) {
+#pragma unroll
+    for (int j = 0; j < NCH - 1; ++j) {
+      const int dst = (rank + 1 + j) % NCH;
+      const int slot = (rank - dst - 1 + 2 * NCH) % NCH;       // rank = (dst + 1 + slot) % 4
+      const uint32_t mb = tc::mapa(smem_u32(&mbar[4]), dst);
+      tc::bulk_copy_to_cluster(tc::mapa(q_a + slot * BLK, dst), sKV + dst * BLK, BLK, mb);
+      tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.rml[slot][0]), dst), &mlx[16 * dst], HQ / NCH * 8, mb);
+    }
+    ok_flag = (wait_mma(&mbar[4], 0) ? 1 : 0) & ok_flag;
+  }
+  __syncthreads();
+  tc::cluster_arrive_relaxed();                 // this CTA has received every block
   {
-    const uint32_t rank = tc::cluster_ctarank();
     float* wts = reinterpret_cast<float*>(&pmax[0][0]);       // [16][NCH] merge weights
     if (tid < 16) {
-      const int h = 16 * (int)rank + tid;
-      const uint32_t ml_a = smem_u32(&mlx[h]);
+      const int h = 16 * rank + tid;
       float2 mv[NCH];
       float M = -INFINITY, L = 0.f;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        mv[c] = tc::ld_dsmem_f2(tc::mapa(ml_a, c));
+        mv[c] = (c == rank) ? mlx[h] : ms.rml[(c - rank - 1 + NCH) % NCH][tid];
         M = fmaxf(M, mv[c].x);
       }
       float w4[NCH];
@@ -682,27 +740,19 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     __syncthreads();
     // item = (head, 16-byte chunk); a warp covers 32 consecutive chunks of one head row,
     // which the c ^ (h % 8) placement spreads over every bank
-    uint4 u[4][NCH];
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       const int idx = tid + it * THREADS;
       const int hh = idx >> 6, ch = idx & 63;
-      const int h = 16 * (int)rank + hh;
-      const uint32_t la = kv_a + h * 1024 + ((ch ^ (h & 7)) << 4);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c)
-        u[it][c] = (wts[hh * NCH + c] != 0.f) ? tc::ld_dsmem_v4(tc::mapa(la, c)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int idx = tid + it * THREADS;
-      const int hh = idx >> 6, ch = idx & 63;
-      const int h = 16 * (int)rank + hh;
+      const int h = 16 * rank + hh;
+      const int off = hh * 1024 + ((ch ^ (h & 7)) << 4);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const float wgt = wts[hh * NCH + c];
-        const uint32_t uw[4] = {u[it][c].x, u[it][c].y, u[it][c].z, u[it][c].w};
+        const uint8_t* src = (c == rank) ? sKV + rank * BLK : sQ + ((c - rank - 1 + NCH) % NCH) * BLK;
+        const uint4 u = *reinterpret_cast<const uint4*>(src + off);
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&uw[t]));
@@ -726,7 +776,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
     }
   }
-  tc::cluster_sync();                            // no CTA leaves while others read its memory
+  tc::cluster_wait();                            // every block sent from here has landed
+  if (tid == 0) tc::mbar_wait(&mbar[3], 0, MAX_POLL);   // no copy still in flight at exit
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TMEM_COLS);
@@ -811,6 +862,28 @@ static cudaError_t run_attn(const csa2_attn_args& a, AttnParams& ap, cudaStream_
   return cudaGetLastError();
 }
 
+// Tensor map of Q viewed as [B*64 rows][512] bf16: 64 x 64 boxes, 128-byte swizzle (the
+// canonical K-major operand layout).  Built on the host for every call (a plain function
+// of the pointer and sizes; the driver entry point is looked up once).
+static cudaError_t make_q_map(const csa2_attn_args& a, CUtensorMap* map) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t gdim[2] = {(cuuint64_t)tca::DIM, (cuuint64_t)a.B * tca::HQ};
+  const cuuint64_t gstride[1] = {(cuuint64_t)tca::DIM * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)tca::HQ};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q), gdim, gstride, box, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -818,8 +891,11 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  CUtensorMap qmap;
+  cudaError_t e = make_q_map(a, &qmap);
+  if (e != cudaSuccess) return e;
   ap.nchunk = tca::NCH;
-  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
+  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap, qmap);
   return cudaGetLastError();
 }
 

@@ -142,6 +142,19 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier.  A relaxed arrive does not wait for this thread's outstanding
+// memory operations (use it where only mbarrier initialisation, already released by
+// fence.mbarrier_init, must be ordered); the wait has acquire semantics.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {       // release semantics
+  asm volatile("barrier.cluster.arrive.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -175,8 +188,33 @@ __device__ __forceinline__ void mbar_init(uint64_t* mbar, uint32_t count) {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// One arrival that also raises the transaction count by `bytes` (TMA copies complete it).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"((uint32_t)__cvta_generic_to_shared(mbar)), "r"(bytes) : "memory");
+}
+
+// 2-D tiled TMA load of the box at (x, y) into the same shared-memory offset of every CTA
+// in `mask` of the cluster, each CTA's mbarrier at `mbar`'s offset receiving the bytes.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const void* tmap, int x, int y, uint64_t* mbar,
+                                                      uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%4, %5}], [%2], %3;"
+      :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(tmap), "r"((uint32_t)__cvta_generic_to_shared(mbar)),
+         "h"(mask), "r"(x), "r"(y)
+      : "memory");
+}
+
 // Wait for phase `parity` to complete, giving up after max_iter polls.  Returns false on
 // timeout (the caller records an error and stops issuing work).
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's
+// shared memory to shared memory of a CTA in the cluster; completion is signalled on the
+// destination CTA's mbarrier (dst and mbar are shared::cluster addresses, from mapa).
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "r"((uint32_t)__cvta_generic_to_shared(src)), "r"(bytes), "r"(mbar) : "memory");
+}
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t max_iter) {
   const uint32_t a = (uint32_t)__cvta_generic_to_shared(mbar);
   for (uint32_t i = 0; i < max_iter; ++i) {

@@ -59,7 +59,8 @@ typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 #define CSA2_DEVERR_SEQ          0x10u /* seq_of / seq index outside [0, num_seqs) */
 #define CSA2_DEVERR_SWA_RANGE    0x20u /* SWA window outside [0, swa_rows) */
 #define CSA2_DEVERR_POS          0x40u /* RoPE position outside [0, rope_max_pos) */
-#define CSA2_DEVERR_TIMEOUT      0x80u /* a bounded wait on tensor-core completion gave up */
+#define CSA2_DEVERR_TIMEOUT      0x80u /* a bounded wait on tensor-core or TMA completion gave up */
+#define CSA2_DEVERR_SMEM_ALIGN   0x100u /* dynamic shared memory was not 1024-byte aligned */
 
 #define CSA2_PAGE_SIZE 64
 
