@@ -15,8 +15,6 @@
 #include "internal.h"
 #include "tc.cuh"
 
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cstdlib>
 
 namespace csa2 {
@@ -353,26 +351,31 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // 4 CTAs and a decode batch of 32 fills the GPU in one wave.  The 4 CTAs of a query form
 // a thread-block cluster.
 //   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle)      160 KB
-//            Q 64 heads x 512 dims (K-major, 128-byte swizzle)                    64 KB
-//            Q arrives by TMA: each CTA of the cluster loads two 64-dim boxes and
-//            multicasts them to all four, so Q is read from memory once per query;
-//            it is converted bf16 -> fp16 in place.
+//            Q 64 heads x 512 dims fp16 (K-major, 128-byte swizzle)               64 KB
+//            Q is loaded at kernel start (it depends on nothing), converted
+//            bf16 -> fp16 in registers and stored swizzled.
 //   TMEM   : S = Q K^T (fp32, 160 columns)                              cols   0..159
 //            P = softmax numerators (fp16 pairs, A operand)             cols   0..79
-//            O half = P V (fp32, 256 dims)                              cols 256..511
+//            O quarter q = P V[:, 128q..] (fp32)      q0: 256..383, q1: 384..511,
+//                                                     q2: 128..255, q3: 256..383
 //   MMA1  S[64 x 160] = Q[smem] . KV^T        (A, B K-major)
-//   MMA2  O[64 x 256] = P[tmem] . KV[:, half] (B MN-major: the same tile read along
-//         the other axis), once per half of the 512 dims
+//   MMA2  O[64 x 128] = P[tmem] . KV[:, quarter] (B MN-major: the same tile read along
+//         the other axis); quarters 0..2 are issued back to back, quarter 3 once the
+//         epilogue has read quarter 0, so the epilogues overlap the products.
 // With M = 64 the 64 heads occupy lanes 0..15 of each of the four TMEM lane quarters, so
 // all eight warps (two per quarter, each taking half of the keys or dims) share the
-// softmax and the epilogue.  A head's softmax is a row of one thread.
-// Each CTA computes o = O / l (fp16) and (max, l) per head of its chunk; CTA r owns the
-// merge of heads [16 r, 16 r + 16): the others send it their blocks of those heads with
-// shared-to-shared bulk copies (into its Q space, free after its first product), and it
-// combines the 4 chunks from its own shared memory.
+// softmax and the epilogue; the 16x32bx2 access shape gives lanes 0..15 and 16..31 of a
+// warp two column ranges of the same 16 heads, so every thread carries data.
+// The epilogue writes o = O / l (fp16) into the Q space (free after MMA1), rows of 1 KB
+// per head.  CTA r owns the merge of heads [16 r, 16 r + 16): once every CTA of the
+// cluster has finished MMA2, the others send it their blocks of those heads (and their
+// (max, l) pairs) with shared-to-shared bulk copies into its KV space, and it combines the
+// 4 chunks from its own shared memory.
 // ---------------------------------------------------------------------------------
 namespace tca {
-constexpr int THREADS = 256;
+constexpr int NW = 256;                         // data threads: warps 0..7
+constexpr int THREADS = NW + 32;                // + warp 8, whose lane 0 issues the MMAs
+constexpr int ISSUER = NW;
 constexpr int HQ = 64;
 constexpr int DIM = 512;
 constexpr int NCH = 4;                          // chunks per query
@@ -380,31 +383,35 @@ constexpr int KT = 128;                         // selected-entry slots per chun
 constexpr int KW = 32;                          // window rows per chunk
 constexpr int NK = KT + KW;                     // keys per chunk
 constexpr int ATOM = NK / 8 * 1024;             // bytes per 64-dim K-atom of the KV tile
+constexpr int QATOM = HQ / 8 * 1024;            // bytes per 64-dim K-atom of the Q tile
 constexpr int SM_KV = NK * DIM * 2;             // 163840
-constexpr int SM_Q = HQ * DIM * 2;             // 65536
+constexpr int SM_Q = HQ * DIM * 2;              // 65536
 struct Misc {                                   // small per-CTA state, after the tiles
   int keyok[NK];
   float pmax[2][HQ];
   float psum[2][HQ];
-  float linv[HQ];
   alignas(16) float2 mlx[HQ];     // this chunk's (row max in log2 units, row sum) per head
   alignas(16) float2 rml[NCH - 1][HQ / NCH];   // received (max, sum) of the other chunks
-  uint64_t mbar[5];
+  uint64_t mbar[7];               // 0: MMA1, 1..4: MMA2 quarters, 5: received merge blocks,
+                                  // 6: quarter 0's columns read by the 8 data warps
   uint32_t tslot;
   int ok_flag;
 };
 constexpr int SMEM = SM_KV + SM_Q + (int)sizeof(Misc);   // no static shared memory
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0;               // S, then P over its first 80 columns
-constexpr uint32_t COL_O = 256;               // one half of O
+constexpr uint32_t COL_S = 0;                   // S, then P over its first 80 columns
 constexpr uint32_t MAX_POLL = 1u << 22;
 constexpr int BLK = HQ / NCH * DIM * 2;         // one CTA's merge block: 16 heads x 512 dims fp16
 constexpr uint32_t RECV_BYTES = (NCH - 1) * (BLK + HQ / NCH * 8);
 
-// byte offset of 16-byte chunk ch (8 fp16) of row r in the K-major KV tile
-__device__ __forceinline__ uint32_t kvoff(int r, int ch) {
-  return (uint32_t)((ch >> 3) * ATOM + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
+__device__ __forceinline__ uint32_t col_o(int q) { return q == 0 ? 256u : q == 1 ? 384u : q == 2 ? 128u : 256u; }
+
+// byte offset of 16-byte chunk ch (8 fp16) of row r in a K-major swizzled tile whose
+// 64-dim atoms are `atom` bytes apart
+__device__ __forceinline__ uint32_t tileoff(int r, int ch, int atom) {
+  return (uint32_t)((ch >> 3) * atom + (r >> 3) * 1024 + (r & 7) * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
+__device__ __forceinline__ uint32_t kvoff(int r, int ch) { return tileoff(r, ch, ATOM); }
 
 __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
   const bool ok = tc::mbar_wait(mbar, parity, MAX_POLL);
@@ -413,8 +420,7 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 }
 }  // namespace tca
 
-__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1)
-    k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap) {
+__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
   using namespace tca;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sKV = smem;
@@ -423,7 +429,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   int* keyok = ms.keyok;
   float (*pmax)[HQ] = ms.pmax;
   float (*psum)[HQ] = ms.psum;
-  float* linv = ms.linv;
   float2* mlx = ms.mlx;
   uint64_t* mbar = ms.mbar;
   int& ok_flag = ms.ok_flag;
@@ -436,9 +441,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   const uint32_t kv_a = smem_u32(sKV), q_a = smem_u32(sQ);
   // M = 64 tensor-memory layout: head h sits in lane 32 * (h / 16) + h % 16, so warp w
-  // (lane quarter w % 4) owns heads [16 (w % 4), 16 (w % 4) + 16) in its lanes 0..15 and
-  // warp >> 2 picks a half of the columns; lanes 16..31 mirror lanes 0..15 and write
-  // nothing that is read.
+  // (lane quarter w % 4) owns heads [16 (w % 4), 16 (w % 4) + 16) and warp >> 2 picks a
+  // half of the columns; threads t and t + 16 of a warp hold the same head.
   const bool lv = lane < 16;
   const int head = 16 * (warp & 3) + (lane & 15);
   const int kh = warp >> 2;
@@ -446,13 +450,20 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 
   if (warp == 0) tc::tmem_alloc(&ms.tslot, TMEM_COLS);
   if (tid == 32) {
-    tc::mbar_init(&mbar[0], 1);
-    tc::mbar_init(&mbar[1], 1);
-    tc::mbar_init(&mbar[2], 1);
-    tc::mbar_init(&mbar[3], 1);
-    tc::mbar_init(&mbar[4], 1);
-    tc::mbar_arrive_expect_tx(&mbar[3], SM_Q);   // the four multicast halves of Q
-    tc::mbar_arrive_expect_tx(&mbar[4], RECV_BYTES);   // the other chunks' merge blocks
+#pragma unroll
+    for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
+    tc::mbar_init(&mbar[6], NW / 32);
+    tc::mbar_arrive_expect_tx(&mbar[5], RECV_BYTES);   // the other chunks' merge blocks
+    ok_flag = 1;
+  }
+  // ---- Q first: 16 chunks of 16 bytes per thread, a warp reading 512 contiguous bytes --
+  const bool worker = tid < NW;
+  if (worker) {
+  uint4 qv[SM_Q / 16 / NW];
+  {
+    const uint4* qs = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
+#pragma unroll
+    for (int i = 0; i < SM_Q / 16 / NW; ++i) qv[i] = __ldg(qs + tid + i * NW);
   }
   // ---- each thread resolves the keys it gathers: FP4 slot fkey (2 threads per key) and
   //      window row skey (8 threads per key), then issues those loads at once -------------
@@ -497,19 +508,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   if (half == 0) keyok[fkey] = fok;
   if (part == 0) keyok[skey] = sok;
-  // ---- Q: every CTA's barrier is initialised and expecting its bytes before any CTA
-  //      multicasts; CTA r loads the 64-dim boxes 2r and 2r + 1 for the whole cluster --------
-  tc::fence_before_sync();
-  tc::cluster_arrive_relaxed();
-  tc::cluster_wait();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tb = ms.tslot;
-  if (tid == 0) {
-    const int rank = (int)tc::cluster_ctarank();
+  // ---- Q -> fp16 into the swizzled tile while the gathers are in flight -----------------
 #pragma unroll
-    for (int kb = 2 * rank; kb < 2 * rank + 2; ++kb)
-      tc::tma_load_2d_multicast(sQ + kb * 8192, &qmap, 64 * kb, HQ * b, &mbar[3], (uint16_t)((1u << NCH) - 1));
+  for (int i = 0; i < SM_Q / 16 / NW; ++i) {
+    const int idx = tid + i * NW, h = idx >> 6, ch = idx & 63;
+    *reinterpret_cast<uint4*>(sQ + tileoff(h, ch, QATOM)) =
+        make_uint4(bf16x2_to_f16x2(qv[i].x), bf16x2_to_f16x2(qv[i].y), bf16x2_to_f16x2(qv[i].z),
+                   bf16x2_to_f16x2(qv[i].w));
   }
   // ---- dequantise the gathered rows into the K-major KV tile ----------------------------
   if (fok) {
@@ -557,29 +562,18 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
     for (int t = 0; t < 8; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(skey, part * 8 + t)) = make_uint4(0, 0, 0, 0);
   }
-  // ---- Q arrived: bf16 -> fp16 in place (the swizzled layout is kept element for element)
-  if (tid == 0) {
-    ok_flag = wait_mma(&mbar[3], 0) ? 1 : 0;
-  }
-  __syncthreads();
-  if (ok_flag) {
-#pragma unroll
-    for (int i = 0; i < SM_Q / 16 / THREADS; ++i) {
-      uint4* qp = reinterpret_cast<uint4*>(sQ) + tid + i * THREADS;
-      const uint4 v = *qp;
-      *qp = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
-    }
-  }
+  }  // worker
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  const uint32_t tb = ms.tslot;
   // ---- MMA1: S = Q K^T -----------------------------------------------------------------
-  if (tid == 0 && ok_flag) {
+  if (tid == ISSUER) {
     constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
 #pragma unroll 4
     for (int ks = 0; ks < DIM / 16; ++ks) {
-      const uint64_t ad = tc::smem_desc_sw128(q_a + (ks >> 2) * (HQ * 128) + (ks & 3) * 32, 16, 1024);
+      const uint64_t ad = tc::smem_desc_sw128(q_a + (ks >> 2) * QATOM + (ks & 3) * 32, 16, 1024);
       const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
       tc::mma_f16_ss(tb + COL_S, ad, bd, id1, ks > 0);
     }
@@ -588,22 +582,20 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   __syncthreads();
   tc::fence_after_sync();
-  // Q is no longer read (the first product has completed): the cluster may now send
-  // merge blocks into its space.  Nothing written before this point is read by another
-  // CTA, so the arrive need not release.
-  tc::cluster_arrive_relaxed();
-  // ---- softmax: head = lane row; two threads (warps w and w ^ 4) split the 160 keys ------
-  float e[80];
+  // ---- softmax: a head's 160 keys are split over four threads: warps w and w ^ 4 take
+  //      halves of 80, and within a warp threads t and t + 16 take 40 each -------------------
+  const int sub = lane >> 4;                    // which 40-key (or 32-column) sub-range
+  if (worker) {
+  float e[40];
   if (ok_flag) {
-    uint32_t r[96];
-    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh, r);
-    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 32, r + 32);
-    tc::tmem_ld32(tb + lane_base + COL_S + 80 * kh + 64, r + 64);
+    uint32_t r[40];
+    tc::tmem_ld16x2_32<40>(tb + lane_base + COL_S + 80 * kh, r);
+    tc::tmem_ld16x2_8<40>(tb + lane_base + COL_S + 80 * kh + 32, r + 32);
     tc::tmem_ld_wait();
-    const int4* ok4 = reinterpret_cast<const int4*>(keyok + 80 * kh);
+    const int4* ok4 = reinterpret_cast<const int4*>(keyok + 80 * kh + 40 * sub);
     float mx = -INFINITY;
 #pragma unroll
-    for (int j4 = 0; j4 < 20; ++j4) {
+    for (int j4 = 0; j4 < 10; ++j4) {
       const int4 v = ok4[j4];
       const int okv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -613,6 +605,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
         mx = fmaxf(mx, e[j]);
       }
     }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     if (lv) pmax[kh][head] = mx;
   }
   // the two warps of a lane quarter exchange their halves' maxima; both have read S, so
@@ -623,9 +616,9 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   if (ok_flag) {
     const float m = fmaxf(pmax[0][head], pmax[1][head]);
     float l = 0.f;
-    uint32_t pk[40];
+    uint32_t pk[20];
 #pragma unroll
-    for (int j = 0; j < 80; j += 2) {
+    for (int j = 0; j < 40; j += 2) {
       float x0 = 0.f, x1 = 0.f;
       if (m != -INFINITY) {
         asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x0) : "f"(e[j] - m));
@@ -635,83 +628,103 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
       l += __low2float(hp) + __high2float(hp);
     }
-    tc::tmem_st32(tb + lane_base + COL_S + 40 * kh, pk);
-    tc::tmem_st8(tb + lane_base + COL_S + 40 * kh + 32, pk + 32);
+    // P column = key / 2: this thread's 40 keys are columns [40 kh + 20 sub, + 20)
+    tc::tmem_st16x2_16<20>(tb + lane_base + COL_S + 40 * kh, pk);
+    tc::tmem_st16x2_4<20>(tb + lane_base + COL_S + 40 * kh + 16, pk + 16);
     tc::tmem_st_wait();
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
     if (lv) psum[kh][head] = l;
   }
+  }  // worker
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (tid < HQ) {
-    const float l = psum[0][tid] + psum[1][tid];
-    const bool any = ok_flag && l > 0.f;
-    mlx[tid] = any ? make_float2(fmaxf(pmax[0][tid], pmax[1][tid]), l) : make_float2(-INFINITY, 0.f);
-    linv[tid] = any ? 1.f / l : 0.f;
-  }
-  // ---- MMA2 per half of 256 dims into cols 256..511, each half followed by its epilogue:
-  //      o = O / l (fp16) into this CTA's shared memory, row h (1 KB) with 16-byte chunk c
-  //      at c ^ (h % 8).  Half 0 lands in K-atoms 0..3 of the KV tile, which the second
-  //      MMA2 no longer reads; half 1 is written after that MMA completes. -----------------
-#pragma unroll 1
-  for (int hf = 0; hf < 2; ++hf) {
-    if (tid == 0 && ok_flag) {
-      constexpr uint32_t id2 = tc::idesc_f16(64, 256, 0, 0, 1);
+  // ---- MMA2 quarters 0..2 back to back; the epilogue of quarter q writes o = O / l (fp16)
+  //      into the Q space, row h (1 KB) with 16-byte chunk c at c ^ (h % 8) ---------------
+  auto issue_quarter = [&](int q) {
+    constexpr uint32_t id2 = tc::idesc_f16(64, 128, 0, 0, 1);
 #pragma unroll
-      for (int ks = 0; ks < NK / 16; ++ks) {
-        const uint64_t bd = tc::smem_desc_sw128(kv_a + (4 * hf) * ATOM + (2 * ks) * 1024, ATOM, 1024);
-        tc::mma_f16_ts(tb + COL_O, tb + COL_S + ks * 8, bd, id2, ks > 0);
-      }
-      tc::mma_commit(&mbar[1 + hf]);
-      ok_flag = wait_mma(&mbar[1 + hf], 0) ? 1 : 0;
+    for (int ks = 0; ks < NK / 16; ++ks) {
+      const uint64_t bd = tc::smem_desc_sw128(kv_a + (2 * q) * ATOM + (2 * ks) * 1024, ATOM, 1024);
+      tc::mma_f16_ts(tb + col_o(q), tb + COL_S + ks * 8, bd, id2, ks > 0);
     }
-    __syncthreads();
-    tc::fence_after_sync();
-    if (ok_flag) {                                 // tcgen05.ld is warp-wide; lanes 0..15 store
-      const float li = linv[head];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {            // 32 columns = 32 dims = 4 chunks
+    tc::mma_commit(&mbar[1 + q]);
+  };
+  if (!worker) {                                // warp 8
+    if (lane == 0 && ok_flag) {
+      issue_quarter(0);
+      issue_quarter(1);
+      issue_quarter(2);
+      // quarter 3 reuses quarter 0's columns once every data warp has read them
+      if (tc::mbar_wait(&mbar[6], 0, MAX_POLL)) {
+        tc::fence_after_sync();
+        issue_quarter(3);
+      } else {
+        raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+      }
+    }
+    __syncwarp();
+    tc::cluster_arrive_relaxed();               // this warp reads no shared memory
+  }
+  if (worker) {
+    if (tid < HQ) {
+      const float l = psum[0][tid] + psum[1][tid];
+      mlx[tid] = (ok_flag && l > 0.f) ? make_float2(fmaxf(pmax[0][tid], pmax[1][tid]), l) : make_float2(-INFINITY, 0.f);
+    }
+    const float lh = psum[0][head] + psum[1][head];
+    const float li = (ok_flag && lh > 0.f) ? 1.f / lh : 0.f;
+    bool ok = ok_flag != 0;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      if (ok) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(&mbar[1 + q], 0, MAX_POLL));
+        if (!ok && lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+      }
+      tc::fence_after_sync();
+      if (q == 3) tc::cluster_arrive_relaxed();   // the KV tile is no longer read: peers may send
+      if (ok) {                                   // 16 heads x 64 columns per warp
         uint32_t r[32];
-        tc::tmem_ld32(tb + lane_base + COL_O + 128 * kh + 32 * c4, r);
+        tc::tmem_ld16x2_32<32>(tb + lane_base + col_o(q) + 64 * kh, r);
         tc::tmem_ld_wait();
-        if (lv) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t pk[4];
+        for (int i = 0; i < 4; ++i) {
+          uint32_t pk[4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
-                                                   __uint_as_float(r[8 * i + 2 * t + 1]) * li);
-              pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
-            }
-            const int ch = 32 * hf + 16 * kh + 4 * c4 + i;
-            *reinterpret_cast<uint4*>(sKV + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int t = 0; t < 4; ++t) {
+            const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
+                                                 __uint_as_float(r[8 * i + 2 * t + 1]) * li);
+            pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
           }
+          const int ch = 16 * q + 8 * kh + 4 * sub + i;
+          *reinterpret_cast<uint4*>(sQ + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
       }
+      if (q == 0) {
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&mbar[6]);
+      }
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    if (!ok && lane == 0) ok_flag = 0;
   }
   // ---- merge: CTA r owns heads [16 r, 16 r + 16).  Each CTA sends the block of every
   //      other CTA (16 heads x 1 KB of its fp16 o, then their 16 (max, sum) pairs) into that
-  //      CTA's former Q space by bulk copies, then combines the 4 chunks of its own heads
-  //      from local shared memory.  Slot j of CTA r holds chunk (r + 1 + j) % 4. ----------
+  //      CTA's KV space by bulk copies, then combines the 4 chunks of its own heads from
+  //      local shared memory.  Slot j of CTA r holds chunk (r + 1 + j) % 4. ---------------
   const int rank = (int)tc::cluster_ctarank();
   tc::fence_proxy_async_smem();                 // epilogue stores -> bulk-copy reads
   __syncthreads();
-  tc::cluster_wait();                           // every CTA has finished MMA1
+  tc::cluster_wait();                           // every CTA has finished MMA2
   if (tid == 0) {
 #pragma unroll
     for (int j = 0; j < NCH - 1; ++j) {
       const int dst = (rank + 1 + j) % NCH;
       const int slot = (rank - dst - 1 + 2 * NCH) % NCH;       // rank = (dst + 1 + slot) % 4
-      const uint32_t mb = tc::mapa(smem_u32(&mbar[4]), dst);
-      tc::bulk_copy_to_cluster(tc::mapa(q_a + slot * BLK, dst), sKV + dst * BLK, BLK, mb);
+      const uint32_t mb = tc::mapa(smem_u32(&mbar[5]), dst);
+      tc::bulk_copy_to_cluster(tc::mapa(kv_a + slot * BLK, dst), sQ + dst * BLK, BLK, mb);
       tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.rml[slot][0]), dst), &mlx[16 * dst], HQ / NCH * 8, mb);
     }
-    ok_flag = (wait_mma(&mbar[4], 0) ? 1 : 0) & ok_flag;
+    ok_flag = (wait_mma(&mbar[5], 0) ? 1 : 0) & ok_flag;
   }
   __syncthreads();
   tc::cluster_arrive_relaxed();                 // this CTA has received every block
@@ -741,8 +754,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     // item = (head, 16-byte chunk); a warp covers 32 consecutive chunks of one head row,
     // which the c ^ (h % 8) placement spreads over every bank
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int idx = tid + it * THREADS;
+    for (int it = 0; it < 4 && worker; ++it) {
+      const int idx = tid + it * NW;
       const int hh = idx >> 6, ch = idx & 63;
       const int h = 16 * rank + hh;
       const int off = hh * 1024 + ((ch ^ (h & 7)) << 4);
@@ -750,7 +763,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const float wgt = wts[hh * NCH + c];
-        const uint8_t* src = (c == rank) ? sKV + rank * BLK : sQ + ((c - rank - 1 + NCH) % NCH) * BLK;
+        const uint8_t* src = (c == rank) ? sQ + rank * BLK : sKV + ((c - rank - 1 + NCH) % NCH) * BLK;
         const uint4 u = *reinterpret_cast<const uint4*>(src + off);
         const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -777,7 +790,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
   }
   tc::cluster_wait();                            // every block sent from here has landed
-  if (tid == 0) tc::mbar_wait(&mbar[3], 0, MAX_POLL);   // no copy still in flight at exit
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TMEM_COLS);
@@ -862,28 +874,6 @@ static cudaError_t run_attn(const csa2_attn_args& a, AttnParams& ap, cudaStream_
   return cudaGetLastError();
 }
 
-// Tensor map of Q viewed as [B*64 rows][512] bf16: 64 x 64 boxes, 128-byte swizzle (the
-// canonical K-major operand layout).  Built on the host for every call (a plain function
-// of the pointer and sizes; the driver entry point is looked up once).
-static cudaError_t make_q_map(const csa2_attn_args& a, CUtensorMap* map) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  const cuuint64_t gdim[2] = {(cuuint64_t)tca::DIM, (cuuint64_t)a.B * tca::HQ};
-  const cuuint64_t gstride[1] = {(cuuint64_t)tca::DIM * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)tca::HQ};
-  const cuuint32_t estride[2] = {1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q), gdim, gstride, box, estride,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -891,11 +881,8 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap qmap;
-  cudaError_t e = make_q_map(a, &qmap);
-  if (e != cudaSuccess) return e;
   ap.nchunk = tca::NCH;
-  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap, qmap);
+  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
   return cudaGetLastError();
 }
 
