@@ -5,6 +5,7 @@
 #include <cstring>
 
 #include "csa2.h"
+#include <cstdint>
 #include "internal.h"
 
 namespace {
@@ -43,9 +44,14 @@ csa2_status check_cache(const csa2_cache& c, bool need_codes, bool need_idx) {
   REQUIRE(c.num_pages <= (1 << 25), CSA2_ERR_UNSUPPORTED_SHAPE,
           "cache.num_pages must be <= 2^25 (row indices are 31-bit)");
   REQUIRE(c.d == 128 || c.d == 512, CSA2_ERR_UNSUPPORTED_SHAPE, "cache.d must be 128 or 512 (got %d)", c.d);
-  if (need_codes) REQUIRE(c.codes && c.scales, CSA2_ERR_INVALID_ARG, "cache.codes/scales is NULL");
+  if (need_codes) {
+    REQUIRE(c.codes && c.scales, CSA2_ERR_INVALID_ARG, "cache.codes/scales is NULL");
+    REQUIRE(((uintptr_t)c.codes & 15) == 0 && ((uintptr_t)c.scales & 15) == 0, CSA2_ERR_INVALID_ARG,
+            "cache.codes/scales must be 16-byte aligned");
+  }
   if (need_idx) {
     REQUIRE(c.idx_k, CSA2_ERR_INVALID_ARG, "cache.idx_k is NULL");
+    REQUIRE(((uintptr_t)c.idx_k & 15) == 0, CSA2_ERR_INVALID_ARG, "cache.idx_k must be 16-byte aligned");
     REQUIRE(c.d_ik == 64 || c.d_ik == 128, CSA2_ERR_UNSUPPORTED_SHAPE, "cache.d_ik must be 64 or 128 (got %d)",
             c.d_ik);
   }

@@ -247,6 +247,13 @@ __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const void* tma
 
 // Wait for phase `parity` to complete, giving up after max_iter polls.  Returns false on
 // timeout (the caller records an error and stops issuing work).
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global memory
+// into this CTA's shared memory, completing on this CTA's mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src), "r"(bytes),
+                  "r"((uint32_t)__cvta_generic_to_shared(mbar)) : "memory");
+}
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's
 // shared memory to shared memory of a CTA in the cluster; completion is signalled on the
 // destination CTA's mbarrier (dst and mbar are shared::cluster addresses, from mapa).

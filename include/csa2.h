@@ -67,9 +67,11 @@ typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 /* Paged cache planes (all device).  d in {128, 512}; d_ik in {64, 128};
  * num_pages <= 2^25 (2^31 entries). */
 typedef struct csa2_cache {
-  uint8_t* codes;              /* [num_pages][64][d/2]  E2M1 pairs, even channel in the low nibble */
-  uint8_t* scales;             /* [num_pages][64][d/16] E4M3 scale of each 16 channels */
-  uint16_t* idx_k;             /* [num_pages][64][d_ik] bf16 indexer K (may be NULL if unused) */
+  uint8_t* codes;              /* [num_pages][64][d/2]  E2M1 pairs, even channel in the low nibble;
+                                  16-byte aligned */
+  uint8_t* scales;             /* [num_pages][64][d/16] E4M3 scale of each 16 channels; 16-byte aligned */
+  uint16_t* idx_k;             /* [num_pages][64][d_ik] bf16 indexer K (may be NULL if unused);
+                                  16-byte aligned */
   const int32_t* page_table;   /* [num_seqs][max_pages] page id of each 64-entry page */
   int32_t num_pages;
   int32_t page_size;           /* must be 64 */
