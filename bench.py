@@ -42,7 +42,8 @@ def peaks():
 
 
 PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
-            ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu")}
+            ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu"),
+            ("k_select_cl_reindex", "decode128k"): ("k_select_cl_reindex_decode128k.md", "index.cu")}
 
 
 def profiled_traffic(kernel, workload_name):
