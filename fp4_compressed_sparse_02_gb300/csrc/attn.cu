@@ -81,6 +81,8 @@ struct ACfg {
 
 template <int DIM, int MT>
 __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   using C = ACfg<DIM, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sQ = smem;
@@ -421,6 +423,8 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 }  // namespace tca
 
 __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
+  pdl_wait();
+  pdl_trigger();
   using namespace tca;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sKV = smem;
@@ -799,6 +803,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 template <int DIM>
 __global__ void __launch_bounds__(DIM / 4) k_combine(const float* __restrict__ opart, const float2* __restrict__ ml,
                                                      int Hq, int nchunk, void* out, int out_f32, float* lse) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   float M = -INFINITY;
   for (int c = 0; c < nchunk; ++c) M = fmaxf(M, ml[((long long)b * nchunk + c) * Hq + h].x);
@@ -868,8 +874,8 @@ static cudaError_t run_attn(const csa2_attn_args& a, AttnParams& ap, cudaStream_
     attr_set = true;
   }
   dim3 grid(ap.nchunk, a.B);
-  k_attn_chunk<DIM, MT><<<grid, ATHREADS, C::SMEM, st>>>(ap);
-  k_combine<DIM><<<dim3(a.B, a.Hq), DIM / 4, 0, st>>>(ap.opart, ap.ml, a.Hq, ap.nchunk, a.out,
+  launch_k(k_attn_chunk<DIM, MT>, grid, ATHREADS, C::SMEM, st, ap);
+  launch_k(k_combine<DIM>, dim3(a.B, a.Hq), DIM / 4, 0, st, ap.opart, ap.ml, a.Hq, ap.nchunk, a.out,
                                                      a.out_dtype == CSA2_F32, a.lse);
   return cudaGetLastError();
 }
@@ -882,7 +888,7 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     attr_set = true;
   }
   ap.nchunk = tca::NCH;
-  k_attn_tc<<<dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st>>>(ap);
+  launch_k(k_attn_tc, dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st, ap);
   return cudaGetLastError();
 }
 

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "csa2.h"
 
 namespace csa2 {
@@ -17,6 +19,46 @@ constexpr int kPageShift = 6;
 // A kernel that meets an out-of-range value reported by the device (a page id, an
 // n_vis, a pool length) sets a bit here and skips the access.
 #define CSA2_DEFINE_ERROR_WORD(name) static __device__ unsigned int name = 0u
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation (launch_k): its CTAs may be scheduled while the
+// previous kernel of the stream is still running.  So each kernel calls pdl_wait()
+// before its first global-memory access -- it returns once the previous grid has
+// completed and its writes are visible, which keeps stream order for everything the
+// kernel reads or writes -- and pdl_trigger() to let the next kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host: launch `kernel` on stream `st` with programmatic stream serialisation
+// (launch_k), or without it (launch_k_late: the kernel starts only once the previous
+// kernel has completed, and its pdl_wait() is a no-op).  The cluster Top-k is launched
+// late: its 8-CTA clusters placed early on the few SMs a running attention leaves idle
+// pack worse than on an empty GPU.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k_late(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ void raise_error(unsigned int* word, unsigned int bit) {
   atomicOr(word, bit);

@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(256) k_project(const HT* __restrict__ H,
                                                  const uint16_t* __restrict__ Wkv,
                                                  const uint16_t* __restrict__ Wz, float* __restrict__ out,
                                                  int T, int d_model, int d, int N, int k_per_split) {
+  pdl_wait();
   __shared__ float As[PBK][PBM + 4];
   __shared__ float Bs[PBK][PBN + 4];
   const int tid = threadIdx.x;
@@ -115,6 +116,8 @@ template <typename HT>
 __global__ void __launch_bounds__(256) k_project_small(const HT* __restrict__ H, const uint16_t* __restrict__ Wkv,
                                                        const uint16_t* __restrict__ Wz, float* __restrict__ out,
                                                        int T, int d_model, int d, int N, int ks) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t psm[];
   uint16_t* Ws = reinterpret_cast<uint16_t*>(psm);                 // [ks][64] bf16
   float* Hs = reinterpret_cast<float*>(psm + (size_t)ks * 128);      // [T][ks]
@@ -159,6 +162,8 @@ __global__ void __launch_bounds__(256) k_project_small(const HT* __restrict__ H,
 __global__ void __launch_bounds__(128) k_project_mma(const uint16_t* __restrict__ H, const uint16_t* __restrict__ Wkv,
                                                      const uint16_t* __restrict__ Wz, float* __restrict__ out, int T,
                                                      int d_model, int d, int N, int ks) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(16) uint8_t psm[];
   const int HS = ks * 2 + 16, WS = 64 * 2 + 16;
   uint8_t* Hs = psm;                       // [64][HS]
@@ -271,6 +276,8 @@ __device__ __forceinline__ void load16_sum(const float* p, long long stride, int
 }
 
 __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
+  pdl_wait();
+  pdl_trigger();
   const int gpr = p.d / 16;                           // 16-channel groups per entry
   long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   long long g = gid / gpr;
@@ -360,6 +367,8 @@ template <int E, int DIK>
 __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __restrict__ seq,
                                                  const int* __restrict__ entry, int G,
                                                  const uint16_t* __restrict__ Wik) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int CPL = DIK / 32;                  // columns per lane: 4 or 2
   extern __shared__ float ik_sm[];
   const int d = cache.d;
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __
 template <int E, int DIK>
 static void launch_index_k(const csa2_compress_args& a, int G, cudaStream_t st) {
   const size_t sm = ((size_t)E * a.cache.d + 8 * E * DIK) * sizeof(float);
-  k_index_k<E, DIK><<<(G + E - 1) / E, 256, sm, st>>>(a.cache, a.seq, a.entry, G, a.W_ik);
+  launch_k(k_index_k<E, DIK>, (G + E - 1) / E, 256, sm, st, a.cache, a.seq, a.entry, G, a.W_ik);
 }
 
 // ---------------------------------------------------------------------------------
@@ -492,7 +501,7 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
       const size_t sm = (size_t)64 * (ks * 2 + 16) + (size_t)ks * 144;
       cudaError_t e = cudaFuncSetAttribute(k_project_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       if (e != cudaSuccess) return e;
-      k_project_mma<<<dim3(N / 64, s), 128, sm, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z, out, a.T,
+      launch_k(k_project_mma, dim3(N / 64, s), 128, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z, out, a.T,
                                                       a.d_model, d, N, ks);
     } else if (use_small(a)) {
       s = small_splits(a.T, a.d_model, N);
@@ -502,12 +511,12 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
       if (a.h_dtype == CSA2_F32) {
         e = cudaFuncSetAttribute(k_project_small<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
-        k_project_small<float><<<dim3(N / 64, s), 256, sm, st>>>(static_cast<const float*>(a.H), a.W_kv, a.W_z,
+        launch_k(k_project_small<float>, dim3(N / 64, s), 256, sm, st, static_cast<const float*>(a.H), a.W_kv, a.W_z,
                                                                  out, a.T, a.d_model, d, N, ks);
       } else {
         e = cudaFuncSetAttribute(k_project_small<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
-        k_project_small<uint16_t><<<dim3(N / 64, s), 256, sm, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv,
+        launch_k(k_project_small<uint16_t>, dim3(N / 64, s), 256, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv,
                                                                     a.W_z, out, a.T, a.d_model, d, N, ks);
       }
     } else {
@@ -515,10 +524,10 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
     int kps = ((a.d_model / s + PBK - 1) / PBK) * PBK;
     dim3 grid(N / PBN, (a.T + PBM - 1) / PBM, s);
     if (a.h_dtype == CSA2_F32)
-      k_project<float><<<grid, 256, 0, st>>>(static_cast<const float*>(a.H), a.W_kv, a.W_z, out,
+      launch_k(k_project<float>, grid, 256, 0, st, static_cast<const float*>(a.H), a.W_kv, a.W_z, out,
                                              a.T, a.d_model, d, N, kps);
     else
-      k_project<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z,
+      launch_k(k_project<uint16_t>, grid, 256, 0, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z,
                                                 out, a.T, a.d_model, d, N, kps);
     }
     qp.Cp = out;
@@ -546,7 +555,7 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   qp.cache = a.cache;
   qp.y_out = a.y_out;
   long long threads = (long long)G * (d / 16);
-  if (threads > 0) k_quant<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(qp);
+  if (threads > 0) launch_k(k_quant, (unsigned)((threads + 255) / 256), 256, 0, st, qp);
   if (a.W_ik && G > 0) {
     const bool many = G >= 2048;
     if (a.cache.d_ik == 128) {

@@ -114,6 +114,7 @@ struct ScanParams {
 
 template <int DK, int NHG>
 __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
+  pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int b = blockIdx.y;
@@ -296,6 +297,8 @@ constexpr int CL_PER_T = CL_SLICE / CL_THREADS;       // 8
 
 template <int DK, int NHG, bool SCORE>
 __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_select_cl(SelectParams p, PoolScoreParams sp) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sscore[SCORE ? CL_SLICE : 1];
   __shared__ int hist[2][256];
   __shared__ int total[256];
@@ -489,10 +492,10 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_sele
 template <int DK>
 static void launch_scan_dk(const ScanParams& sp, int nhg, dim3 grid, cudaStream_t st) {
   switch (nhg) {
-    case 1: k_full_scan<DK, 1><<<grid, 256, 0, st>>>(sp); break;
-    case 2: k_full_scan<DK, 2><<<grid, 256, 0, st>>>(sp); break;
-    case 3: k_full_scan<DK, 3><<<grid, 256, 0, st>>>(sp); break;
-    default: k_full_scan<DK, 4><<<grid, 256, 0, st>>>(sp); break;
+    case 1: launch_k(k_full_scan<DK, 1>, grid, 256, 0, st, sp); break;
+    case 2: launch_k(k_full_scan<DK, 2>, grid, 256, 0, st, sp); break;
+    case 3: launch_k(k_full_scan<DK, 3>, grid, 256, 0, st, sp); break;
+    default: launch_k(k_full_scan<DK, 4>, grid, 256, 0, st, sp); break;
   }
 }
 
@@ -532,7 +535,7 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sel.topk = a.topk;
   sel.topk_len = a.topk_len;
   PoolScoreParams none{};
-  k_select_cl<128, 1, false><<<dim3(NCL, a.B), CL_THREADS, 0, st>>>(sel, none);
+  launch_k_late(k_select_cl<128, 1, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
   return cudaGetLastError();
 }
 
@@ -544,10 +547,10 @@ template <int DK>
 static void launch_reindex_dk(const SelectParams& sel, const PoolScoreParams& pp, int nhg, int B, cudaStream_t st) {
   const dim3 grid(NCL, B);
   switch (nhg) {
-    case 1: k_select_cl<DK, 1, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
-    case 2: k_select_cl<DK, 2, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
-    case 3: k_select_cl<DK, 3, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
-    default: k_select_cl<DK, 4, true><<<grid, CL_THREADS, 0, st>>>(sel, pp); break;
+    case 1: launch_k_late(k_select_cl<DK, 1, true>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 2: launch_k_late(k_select_cl<DK, 2, true>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 3: launch_k_late(k_select_cl<DK, 3, true>, grid, CL_THREADS, 0, st, sel, pp); break;
+    default: launch_k_late(k_select_cl<DK, 4, true>, grid, CL_THREADS, 0, st, sel, pp); break;
   }
 }
 
