@@ -295,20 +295,37 @@ constexpr int CL_THREADS = 256;
 constexpr int CL_SLICE = 16384 / NCL;                 // 2048
 constexpr int CL_PER_T = CL_SLICE / CL_THREADS;       // 8
 
+// Histogram increment of `cnt` at `bin` for a warp: the lanes sharing the first active
+// lane's bin add once (in the leading digits most keys share one); the others add their
+// own.  Called by all 32 lanes of the warp.
+__device__ __forceinline__ void hist_add_warp(int* hist, int bin, int cnt) {
+  const bool active = cnt > 0;
+  const unsigned act = __ballot_sync(FULL_MASK, active);
+  if (!act) return;
+  const int lane = threadIdx.x & 31, leader = __ffs(act) - 1;
+  const int b0 = __shfl_sync(FULL_MASK, bin, leader);
+  const bool same = active && bin == b0;
+  const int tot = __reduce_add_sync(FULL_MASK, same ? cnt : 0);
+  if (lane == leader) atomicAdd(&hist[b0], tot);
+  if (active && !same) atomicAdd(&hist[bin], cnt);
+}
+
 template <int DK, int NHG, bool SCORE>
-__global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_select_cl(SelectParams p, PoolScoreParams sp) {
+__global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_select_cl(SelectParams p, PoolScoreParams sp) {
   pdl_wait();
   pdl_trigger();
   __shared__ float sscore[SCORE ? CL_SLICE : 1];
-  __shared__ int hist[2][256];
+  __shared__ int sent[SCORE ? CL_SLICE : 1];        // pool entries of the slice (Reindex)
+  __shared__ int hist[4][256];                      // one per radix pass, zeroed at entry
   __shared__ int total[256];
   __shared__ int scan_sh[32];
   __shared__ int pick[2];
-  __shared__ int xfer[2];
+  __shared__ int xfer;                              // this CTA's packed (above, equal) count
   __shared__ int base_sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y;
   const int rank = (int)tc::cluster_ctarank();
+  for (int i = tid; i < 4 * 256; i += CL_THREADS) (&hist[0][0])[i] = 0;
   int P;
   if (p.n_vis) {
     int n = __ldg(p.n_vis + b);
@@ -333,64 +350,73 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_sele
     for (int i = s0 + tid; i < min(s1, P); i += CL_THREADS) out[i] = p.pool[rowb + i];
     for (int i = P + rank * CL_THREADS + tid; i < k; i += NCL * CL_THREADS) out[i] = -1;
     if (tid == 0 && rank == 0) p.topk_len[b] = P;
-    return;
+    return;                                               // the same in every CTA of the cluster
   }
   const int e1 = min(s1, P);                              // valid positions [s0, e1)
   if constexpr (SCORE) {
     // ---- score this CTA's slice of the pool (Reindex).  Warp w owns tiles w, w+8, ...
-    //      of 32 positions (at most 8).  All of its rows are resolved first (pool id ->
-    //      page table), then tiles stream two at a time so 16 KB per warp are in flight.
+    //      of 32 positions; lane (g, c) owns rows g + 8u of a tile.  While a tile's rows
+    //      are loading, the next tile's rows are resolved (pool id -> page table) and the
+    //      pool ids of the tile after that are fetched.
     constexpr int NT = CL_SLICE / 32 / (CL_THREADS / 32);   // tiles per warp: 8
     const int g = lane >> 2, c = lane & 3;
     const int sq = __ldg(sp.seq_of + b);
     QFrag<DK, NHG> f;
     load_qfrag<DK, NHG>(sp.q + (long long)b * sp.H_i * DK, sp.w + (long long)b * sp.H_i, sp.H_i, f);
-    int ent[NT][4];
+    auto pos_of = [&](int it, int u) { return s0 + 32 * (warp + 8 * it) + g + 8 * u; };
+    auto fetch_ent = [&](int it, int* e) {
 #pragma unroll
-    for (int it = 0; it < NT; ++it)
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int pos = s0 + 32 * (warp + 8 * it) + g + 8 * t;
-        ent[it][t] = (pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
+      for (int u = 0; u < 4; ++u) {
+        const int pos = pos_of(it, u);
+        e[u] = (it < NT && pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
       }
-    int rw[NT][4];
+    };
+    auto resolve = [&](int it, const int* e, long long* rw) {
 #pragma unroll
-    for (int it = 0; it < NT; ++it)
+      for (int u = 0; u < 4; ++u) {
+        const int pos = pos_of(it, u);
+        if (it < NT && pos < e1 && c == 0) sent[pos - s0] = e[u];
+        rw[u] = (e[u] >= 0) ? entry_row(sp.cache, sq, e[u], &g_err_index) : -1;
+      }
+    };
+    int en[4];
+    long long rw[4];
+    fetch_ent(0, en);
+    resolve(0, en, rw);
+    fetch_ent(1, en);
+#pragma unroll 1
+    for (int it = 0; it < NT && s0 + 32 * (warp + 8 * it) < e1; ++it) {
+      uint4 A[4][DK / 32];
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
-        rw[it][t] = (ent[it][t] >= 0) ? (int)entry_row(sp.cache, sq, ent[it][t], &g_err_index) : -1;
+      for (int u = 0; u < 4; ++u) load_row<DK>(sp.cache.idx_k, rw[u], A[u]);
+      resolve(it + 1, en, rw);                            // next tile, while these rows load
+      fetch_ent(it + 2, en);
+      float sc[4];
+      tile_scores<DK, NHG>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
+      tile_scores<DK, NHG>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
+      if (c == 0) {
 #pragma unroll
-    for (int it = 0; it < NT; it += 2) {
-      if (s0 + 32 * (warp + 8 * it) >= e1) break;
-      uint4 A[2][4][DK / 32];
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int t = 0; t < 4; ++t) load_row<DK>(sp.cache.idx_k, rw[it + u][t], A[u][t]);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        float sc[4];
-        tile_scores<DK, NHG>(f, A[u][0], A[u][1], sp.relu != 0, sc[0], sc[1]);
-        tile_scores<DK, NHG>(f, A[u][2], A[u][3], sp.relu != 0, sc[2], sc[3]);
-        if (c == 0) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int pos = s0 + 32 * (warp + 8 * (it + u)) + g + 8 * t;
-            if (pos < e1) sscore[pos - s0] = sc[t];
-          }
+        for (int u = 0; u < 4; ++u) {
+          const int pos = pos_of(it, u);
+          if (pos < e1) sscore[pos - s0] = sc[u];
         }
       }
     }
-    __syncthreads();
   }
-  // ---- keys: 8 consecutive positions per thread ----------------------------------------
+  __syncthreads();                                        // scores and zeroed histograms
+  // ---- keys (and pool entries): 8 consecutive positions per thread ---------------------
   uint32_t key[CL_PER_T];
+  int ent[CL_PER_T];
   const int q0 = s0 + tid * CL_PER_T;
 #pragma unroll
   for (int i = 0; i < CL_PER_T; ++i) {
     const int q = q0 + i;
     float sv = 0.f;
-    if (q < e1) sv = SCORE ? sscore[q - s0] : p.score[rowb + q];
+    ent[i] = -1;
+    if (q < e1) {
+      sv = SCORE ? sscore[q - s0] : __ldg(p.score + rowb + q);
+      ent[i] = SCORE ? sent[q - s0] : __ldg(p.pool + rowb + q);
+    }
     key[i] = (q < e1) ? float_key(sv) : 0u;
   }
   uint32_t prefix = 0, mask = 0;
@@ -398,13 +424,25 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_sele
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    int* hb = hist[pass & 1];
-    hb[tid] = 0;
-    __syncthreads();
+    int* hb = hist[pass];
+    // this thread's keys in the digit of its first live key are counted once; the rest
+    // (rare in the leading digits) one by one
+    int b0 = 0, c0 = 0;
+    bool any = false;
 #pragma unroll
-    for (int i = 0; i < CL_PER_T; ++i)
-      if (q0 + i < e1 && (key[i] & mask) == prefix) atomicAdd(&hb[(key[i] >> shift) & 255], 1);
-    tc::cluster_sync();
+    for (int i = 0; i < CL_PER_T; ++i) {
+      const bool live = q0 + i < e1 && (key[i] & mask) == prefix;
+      const int bi = (int)((key[i] >> shift) & 255u);
+      if (live && !any) { b0 = bi; any = true; }
+      c0 += (live && bi == b0) ? 1 : 0;
+    }
+    hist_add_warp(hb, b0, c0);
+#pragma unroll
+    for (int i = 0; i < CL_PER_T; ++i) {
+      const int bi = (int)((key[i] >> shift) & 255u);
+      if (q0 + i < e1 && (key[i] & mask) == prefix && bi != b0) atomicAdd(&hb[bi], 1);
+    }
+    tc::cluster_sync();                                   // every CTA's histogram is complete
     {
       const uint32_t ha = smem_u32(&hb[tid]);
       int tsum = 0;
@@ -442,46 +480,36 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS) k_sele
     mask |= 0xFFu << shift;
     remaining = pick[1];
   }
-  // ---- ties at the threshold key go to the lowest positions, cluster-wide ---------------
-  int eq = 0;
-#pragma unroll
-  for (int i = 0; i < CL_PER_T; ++i) eq += (q0 + i < e1 && key[i] == prefix) ? 1 : 0;
-  int eq_tot;
-  int eqrank = block_exclusive_scan(eq, scan_sh, eq_tot);
-  if (tid == 0) xfer[0] = eq_tot;
-  tc::cluster_sync();
-  if (tid == 0) {
-    int bsum = 0;
-    for (int cc = 0; cc < rank; ++cc) bsum += tc::ld_dsmem_s32(tc::mapa(smem_u32(&xfer[0]), cc));
-    base_sh = bsum;
-  }
-  __syncthreads();
-  eqrank += base_sh;
-  unsigned selmask = 0;
-  int nsel = 0;
+  // ---- output slots from one scan of (keys above the threshold, keys equal to it):
+  //      ties at the threshold go to the lowest positions, cluster-wide ---------------------
+  int gt = 0, eq = 0;
 #pragma unroll
   for (int i = 0; i < CL_PER_T; ++i) {
-    bool sel = false;
     if (q0 + i < e1) {
-      if (key[i] > prefix) sel = true;
-      else if (key[i] == prefix) { sel = eqrank < remaining; ++eqrank; }
+      gt += key[i] > prefix ? 1 : 0;
+      eq += key[i] == prefix ? 1 : 0;
     }
-    if (sel) { selmask |= 1u << i; ++nsel; }
   }
-  int sel_tot;
-  int o = block_exclusive_scan(nsel, scan_sh, sel_tot);
-  if (tid == 0) xfer[1] = sel_tot;
+  int tot;
+  const int ex = block_exclusive_scan(gt | (eq << 16), scan_sh, tot);   // counts < 2^15
+  if (tid == 0) xfer = tot;
   tc::cluster_sync();
   if (tid == 0) {
     int bsum = 0;
-    for (int cc = 0; cc < rank; ++cc) bsum += tc::ld_dsmem_s32(tc::mapa(smem_u32(&xfer[1]), cc));
+    for (int cc = 0; cc < rank; ++cc) bsum += tc::ld_dsmem_s32(tc::mapa(smem_u32(&xfer), cc));
     base_sh = bsum;
   }
   __syncthreads();
-  o += base_sh;
+  const int before = base_sh + ex;
+  int er = before >> 16;                                  // equal keys before this thread
+  int o = (before & 0xffff) + min(er, remaining);
 #pragma unroll
-  for (int i = 0; i < CL_PER_T; ++i)
-    if ((selmask & (1u << i)) && o < k) out[o++] = p.pool[rowb + q0 + i];
+  for (int i = 0; i < CL_PER_T; ++i) {
+    if (q0 + i < e1 && (key[i] > prefix || (key[i] == prefix && er++ < remaining))) {
+      if (o < k) out[o] = ent[i];
+      ++o;
+    }
+  }
   if (tid == 0 && rank == 0) p.topk_len[b] = k;
   tc::cluster_sync();                                   // no CTA leaves while others read it
 }
