@@ -243,7 +243,8 @@ csa2_status csa2_get_device_error(uint32_t* word) {
   REQUIRE(word, CSA2_ERR_INVALID_ARG, "word is NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_status(e, "csa2_get_device_error");
-  *word = csa2::read_clear_error_compress() | csa2::read_clear_error_index() | csa2::read_clear_error_attn();
+  *word = csa2::read_clear_error_compress() | csa2::read_clear_error_proj() | csa2::read_clear_error_index() |
+          csa2::read_clear_error_attn();
   return cuda_status(cudaGetLastError(), "csa2_get_device_error");
 }
 

@@ -482,6 +482,7 @@ static int pick_splits(int T, int d_model, int N) {
 size_t compress_workspace_bytes(const csa2_compress_args& a) {
   if (!a.W_kv) return 0;
   int N = a.cache.d * (a.m > 1 ? 2 : 1);
+  if (project_tc_supported(a)) return (size_t)a.T * N * sizeof(float);
   int s = !use_small(a) ? pick_splits(a.T, a.d_model, N)
           : (a.h_dtype == CSA2_BF16 ? mma_splits(a.d_model, N) : small_splits(a.T, a.d_model, N));
   return (size_t)s * a.T * N * sizeof(float);
@@ -495,7 +496,11 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
     int N = d * (a.m > 1 ? 2 : 1);
     float* out = static_cast<float*>(ws);
     int s;
-    if (use_small(a) && a.h_dtype == CSA2_BF16) {
+    if (project_tc_supported(a)) {
+      s = 1;
+      cudaError_t e = launch_project_tc(a, out, st);
+      if (e != cudaSuccess) return e;
+    } else if (use_small(a) && a.h_dtype == CSA2_BF16) {
       s = mma_splits(a.d_model, N);
       const int ks = a.d_model / s;
       const size_t sm = (size_t)64 * (ks * 2 + 16) + (size_t)ks * 144;

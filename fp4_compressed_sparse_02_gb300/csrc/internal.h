@@ -14,6 +14,11 @@ size_t compress_workspace_bytes(const csa2_compress_args& a);
 cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t st);
 uint32_t read_clear_error_compress();
 
+// proj_tc.cu: tensor-core projection for many bf16 tokens (out[T][d or 2d], fp32)
+bool project_tc_supported(const csa2_compress_args& a);
+cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, cudaStream_t st);
+uint32_t read_clear_error_proj();
+
 // index.cu
 size_t index_full_workspace_bytes(const csa2_index_full_args& a);
 cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st);

@@ -2,7 +2,9 @@
 
   * FP4 codes / scales, given identical float32 rows: bit-exact.
   * FP4 codes / scales from a float32 GPU pipeline vs the float64 oracle: equal except
-    where the oracle's a/6 or y/s lies within 1e-5 (relative) of a rounding midpoint.
+    where the oracle's a/6 or y/s lies within 1e-5 (relative), or within the float32
+    computation's error bound when the test supplies one, of a rounding decision (an
+    E4M3 / E2M1 midpoint, or 0 for the sign of a code that rounds to zero).
   * Index sets: equal except for swaps at a selection boundary between entries whose
     oracle scores differ by <= 1e-5 relative (to the larger magnitude, with a floor of
     1e-5 x the largest |score| among the candidates for scores near zero).
@@ -76,10 +78,22 @@ def near_midpoint(x, grid, rel=REL_TIE):
     return near <= rel * np.maximum(x, 1e-30)
 
 
-def fp4_mismatch_is_tolerated(y_oracle, codes_g, scales_g, codes_o, scales_o):
+def near_midpoint_abs(x, grid, err):
+    """True where |x| lies within the absolute distance err (or REL_TIE relative) of a
+    midpoint of the ascending magnitude grid."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    mids = (grid[1:] + grid[:-1]) / 2
+    i = np.clip(np.searchsorted(mids, x), 1, len(mids) - 1)
+    near = np.minimum(np.abs(x - mids[i - 1]), np.abs(x - mids[np.minimum(i, len(mids) - 1)]))
+    return near <= np.maximum(REL_TIE * np.maximum(x, 1e-30), np.asarray(err, dtype=np.float64))
+
+
+def fp4_mismatch_is_tolerated(y_oracle, codes_g, scales_g, codes_o, scales_o, y_err=None):
     """Per 16-channel group: a mismatching group is tolerated only if the oracle's a/6 is
     near an E4M3 midpoint, or (same scale) every mismatching code's y/s is near an E2M1
-    midpoint.  Returns (n_mismatched_groups, n_tolerated)."""
+    midpoint.  "Near" is REL_TIE relative, or, when y_err (a bound on |y_gpu - y_oracle|
+    per element) is given, within that bound carried through the division.
+    Returns (n_mismatched_groups, n_tolerated)."""
     y = np.asarray(y_oracle, dtype=np.float32)
     G, d = y.shape
     cg = formats.fp4_unpack(codes_g).reshape(G, d // 16, 16)
@@ -88,17 +102,53 @@ def fp4_mismatch_is_tolerated(y_oracle, codes_g, scales_g, codes_o, scales_o):
     e4 = formats.e4m3_value(np.arange(0x7F))
     e2 = formats.e2m1_value(np.arange(8))
     yg = y.reshape(G, d // 16, 16)
+    eg = np.zeros_like(yg, dtype=np.float64) if y_err is None else np.asarray(y_err, np.float64).reshape(G, d // 16, 16)
     tol = 0
     for gi, qi in zip(*np.nonzero(bad)):
         a = np.abs(yg[gi, qi]).max()
         if scales_g[gi, qi] != scales_o[gi, qi]:
-            ok = near_midpoint(np.float32(a) / np.float32(6.0), e4).item()
+            ok = near_midpoint_abs(np.float32(a) / np.float32(6.0), e4, eg[gi, qi].max() / 6.0).item()
         else:
             s = np.float32(formats.e4m3_value(scales_o[gi, qi]))
             diff = cg[gi, qi] != co[gi, qi]
-            ok = bool(near_midpoint((yg[gi, qi] / s)[diff], e2).all())
+            yd, ed = yg[gi, qi][diff], eg[gi, qi][diff]
+            near = near_midpoint_abs(yd / s, e2, ed / s)
+            # E2M1 keeps the sign of a value that rounds to zero: +0 vs -0 is the decision
+            # at the boundary 0, tolerated when |y| is within the error bound of 0
+            zero = ((cg[gi, qi][diff] & 7) == 0) & ((co[gi, qi][diff] & 7) == 0) & (
+                np.abs(yd) <= np.maximum(ed, REL_TIE * s))
+            ok = bool((near | zero).all())
         tol += int(ok)
     return int(bad.sum()), tol
+
+
+def projection_error_bound(H, W_kv, W_z, m, d_rope, C, Z):
+    """Bound on |y_gpu - y_oracle| for the compressor from hidden states, per (group,
+    channel).  The projection sums K bf16 x bf16 products (exact in fp32) in fp32 in some
+    order: |error| <= gamma_K * sum_k |h_k w_k|, gamma_K = K u / (1 - K u), u = 2^-24
+    (the standard bound for recursive summation in any order).  The m-token softmax
+    pooling e = sum_j w_j C_j, w = softmax(Z), moves by at most max_j eC_j from the C
+    errors and, to first order, max_j eZ_j * (max_j C_j - min_j C_j) from the Z errors
+    (doubled here); the RoPE rotation of a pair adds the two errors of the pair."""
+    H = np.abs(np.asarray(H, dtype=np.float64))
+    K = H.shape[1]
+    u = 2.0 ** -24
+    gamma = K * u / (1 - K * u)
+    eC = gamma * (H @ np.abs(np.asarray(W_kv, dtype=np.float64)))
+    T, d = eC.shape
+    if m == 1:
+        e = eC
+    else:
+        eZ = gamma * (H @ np.abs(np.asarray(W_z, dtype=np.float64)))
+        Cg = np.asarray(C, dtype=np.float64).reshape(T // m, m, d)
+        e = eC.reshape(T // m, m, d).max(1) + 2.0 * eZ.reshape(T // m, m, d).max(1) * (Cg.max(1) - Cg.min(1))
+    if d_rope:
+        b = d - d_rope
+        pair = e[:, b::2] + e[:, b + 1::2]
+        e = e.copy()
+        e[:, b::2] = pair
+        e[:, b + 1::2] = pair
+    return e
 
 
 def rel_l2(a, b):

@@ -5,7 +5,7 @@ import torch
 
 from fp4_compressed_sparse_02_gb300 import csa2, synth
 from oracle import compress, formats
-from parity_utils import (bf16_dev, bf16_host_bits, fp4_mismatch_is_tolerated, paged_to_logical, to_dev)
+from parity_utils import (bf16_dev, projection_error_bound, bf16_host_bits, fp4_mismatch_is_tolerated, paged_to_logical, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -124,10 +124,13 @@ def test_quant_given_rows_pooled(m):
 
 
 @pytest.mark.parametrize("h_dtype,m,T,d_model", [("bf16", 1, 512, 256), ("f32", 1, 512, 256), ("bf16", 2, 512, 256),
+                                               ("bf16", 1, 200, 5120), ("bf16", 2, 384, 1024),
                                                ("bf16", 1, 32, 5120), ("f32", 1, 64, 1024), ("bf16", 2, 64, 512),
                                                ("bf16", 1, 1, 5120)])
 def test_compress_projection(h_dtype, m, T, d_model):
-    # T <= 64 takes the few-row projection (decode append); larger T the tiled one
+    # T <= 64 takes the few-row projection (decode append); larger bf16 T the tensor-core
+    # GEMM (ragged last tile at T = 200, an 80-deep K loop at d_model = 5120, W_KV and W_Z
+    # column tiles at m = 2); f32 H the tiled SIMT one
     r = np.random.default_rng(300 + m + T)
     d, d_ik = 512, 128
     if h_dtype == "bf16":
@@ -155,7 +158,10 @@ def test_compress_projection(h_dtype, m, T, d_model):
     yg = y.cpu().numpy()
     np.testing.assert_allclose(yg, ref["y"], rtol=1e-5, atol=1e-5 * np.abs(ref["y"]).max())
     codes, scales = _read_back(cache, pt, seq, entry)
-    bad, tol = fp4_mismatch_is_tolerated(ref["y"], codes, scales, ref["codes"], ref["scales"])
+    C = compress.project(H_host, formats.bf16_value(Wkv))
+    Z = compress.project(H_host, formats.bf16_value(Wz)) if m > 1 else None
+    y_err = projection_error_bound(H_host, formats.bf16_value(Wkv), formats.bf16_value(Wz), m, 64, C, Z)
+    bad, tol = fp4_mismatch_is_tolerated(ref["y"], codes, scales, ref["codes"], ref["scales"], y_err)
     assert bad == tol and bad <= max(2, 0.002 * G * d / 16)
     # indexer K: compare entries whose FP4 bytes agree, within one bf16 ulp
     ik = bf16_host_bits(cache.idx_k).reshape(-1, 64, d_ik)
