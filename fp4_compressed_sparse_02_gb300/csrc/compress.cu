@@ -446,9 +446,15 @@ __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __
 }
 
 template <int E, int DIK>
-static void launch_index_k(const csa2_compress_args& a, int G, cudaStream_t st) {
+static cudaError_t launch_index_k(const csa2_compress_args& a, int G, cudaStream_t st) {
   const size_t sm = ((size_t)E * a.cache.d + 8 * E * DIK) * sizeof(float);
-  launch_k(k_index_k<E, DIK>, (G + E - 1) / E, 256, sm, st, a.cache, a.seq, a.entry, G, a.W_ik);
+  static size_t attr_bytes = 0;                 // opt-in above 48 KB, raised when needed
+  if (sm > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(k_index_k<E, DIK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    attr_bytes = sm;
+  }
+  return launch_k(k_index_k<E, DIK>, (G + E - 1) / E, 256, sm, st, a.cache, a.seq, a.entry, G, a.W_ik);
 }
 
 // ---------------------------------------------------------------------------------
@@ -563,11 +569,12 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   if (threads > 0) launch_k(k_quant, (unsigned)((threads + 255) / 256), 256, 0, st, qp);
   if (a.W_ik && G > 0) {
     const bool many = G >= 2048;
-    if (a.cache.d_ik == 128) {
-      if (many) launch_index_k<8, 128>(a, G, st); else launch_index_k<1, 128>(a, G, st);
-    } else {
-      if (many) launch_index_k<8, 64>(a, G, st); else launch_index_k<1, 64>(a, G, st);
-    }
+    cudaError_t e;
+    if (a.cache.d_ik == 128)
+      e = many ? launch_index_k<8, 128>(a, G, st) : launch_index_k<1, 128>(a, G, st);
+    else
+      e = many ? launch_index_k<8, 64>(a, G, st) : launch_index_k<1, 64>(a, G, st);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

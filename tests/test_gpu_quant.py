@@ -170,9 +170,11 @@ def test_compress_projection(h_dtype, m, T, d_model):
     _check_index_k(ikg[same], ref["idx_k"][same], ref["codes"][same], ref["scales"][same], Wik)
 
 
-def test_index_k_of_bit_exact_entries():
-    r = np.random.default_rng(400)
-    G, d, d_ik = 777, 512, 128
+@pytest.mark.parametrize("G", [777, 2100])
+def test_index_k_of_bit_exact_entries(G):
+    # G >= 2048 takes the 8-entries-per-CTA indexer-K kernel (ragged last CTA at 2100)
+    r = np.random.default_rng(400 + G)
+    d, d_ik = 512, 128
     C = r.standard_normal((G, d)).astype(np.float32)
     Wik = synth.bf16_normal(r, (d, d_ik), 1 / np.sqrt(d))
     seq, entry, pt = _layout(r, G, 2)
