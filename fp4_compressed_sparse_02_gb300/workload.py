@@ -23,13 +23,22 @@ def _fp8_rows(rows, d, g, device):
     return (sign | expo | man).to(torch.uint8)
 
 
-def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedule=None, chunk_pages=32768):
-    """A decode step of B independent sequences with N visible entries each.
+def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedule=None, chunk_pages=32768,
+                 Ns=None):
+    """A decode step of B independent sequences with N visible entries each (or Ns[b]
+    entries for sequence b when Ns is given; N is then max(Ns)).
 
-    The cache holds N entries per sequence (entry N-1 is rewritten by the step's append
-    when append=True).  Pages are a random permutation.  Returns (DecodeStep, info)."""
+    The cache holds N (Ns[b]) entries per sequence (the last one is rewritten by the
+    step's append when append=True).  Pages are a random permutation; page-table slots
+    past a sequence's length point at page 0 and are never read.  Returns (DecodeStep,
+    info)."""
+    if Ns is not None:
+        Ns = [int(x) for x in Ns]
+        B = len(Ns)
+        N = max(Ns)
     B = B or cfg["B"]
     N = N or cfg["N"]
+    Ns = Ns or [N] * B
     d, d_ik, H_i, Hq, W, k = cfg["d"], cfg["d_ik"], cfg["H_i"], cfg["Hq"], cfg["W"], cfg["k"]
     NB, P, d_model, d_rope = cfg["NB"], cfg["P"], cfg["d_model"], cfg["d_rope"]
     g = torch.Generator(device=device)
@@ -37,8 +46,15 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
     gc = torch.Generator()
     gc.manual_seed(seed)
     mp = (N + 63) // 64
-    num_pages = B * mp
-    page_table = torch.randperm(num_pages, generator=gc).to(torch.int32).reshape(B, mp).to(device)
+    used = [(n + 63) // 64 for n in Ns]
+    num_pages = sum(used)
+    perm = torch.randperm(num_pages, generator=gc).to(torch.int32)
+    page_table = torch.zeros((B, mp), dtype=torch.int32)
+    o = 0
+    for b, u in enumerate(used):
+        page_table[b, :u] = perm[o:o + u]
+        o += u
+    page_table = page_table.to(device)
     cache = csa2.PagedCache(
         codes=torch.empty((num_pages, 64, d // 2), dtype=torch.uint8, device=device),
         scales=torch.empty((num_pages, 64, d // 16), dtype=torch.uint8, device=device),
@@ -52,7 +68,7 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
                                             dtype=torch.uint8)
         cache.idx_k[p0:p1] = _randn_bf16((p1 - p0, 64, d_ik), g, device)
     seq_of = torch.arange(B, dtype=torch.int32, device=device)
-    n_vis = torch.full((B,), N, dtype=torch.int32, device=device)
+    n_vis = torch.tensor(Ns, dtype=torch.int32, device=device)
     sched = schedule or decoder_schedule()
     layers = []
     for mode in sched:
@@ -71,14 +87,14 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
         app = dict(H=_randn_bf16((B, d_model), g, device),
                    W_kv=_randn_bf16((d_model, d), g, device, 1 / math.sqrt(d_model)),
                    W_ik=_randn_bf16((d, d_ik), g, device, 1 / math.sqrt(d)),
-                   pos=torch.full((B,), N - 1, dtype=torch.int32, device=device),
+                   pos=torch.tensor(Ns, dtype=torch.int32, device=device) - 1,
                    seq=torch.arange(B, dtype=torch.int32, device=device),
-                   entry=torch.full((B,), N - 1, dtype=torch.int32, device=device))
+                   entry=torch.tensor(Ns, dtype=torch.int32, device=device) - 1)
         cos, sin = synth.rope_tables(N, d_rope)
         rope = (torch.from_numpy(cos).to(device), torch.from_numpy(sin).to(device))
     step = DecodeStep(cache, seq_of, n_vis, N, layers, NB, P, k, W, append=app, rope=rope)
-    info = dict(B=B, N=N, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq, W=W, k=k, NB=NB,
-                P=P, d_model=d_model, d_rope=d_rope)
+    info = dict(B=B, N=N, Ns=Ns, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq, W=W, k=k,
+                NB=NB, P=P, d_model=d_model, d_rope=d_rope)
     return step, info
 
 
