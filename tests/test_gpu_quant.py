@@ -5,23 +5,12 @@ import torch
 
 from fp4_compressed_sparse_02_gb300 import csa2, synth
 from oracle import compress, formats
-from parity_utils import (bf16_dev, projection_error_bound, bf16_host_bits, fp4_mismatch_is_tolerated, paged_to_logical, to_dev)
+from parity_utils import (bf16_dev, check_index_k, projection_error_bound, bf16_host_bits, fp4_mismatch_is_tolerated, paged_to_logical, to_dev)
 
 pytestmark = pytest.mark.gpu
 
 
-def _check_index_k(got_bits, ref_bits, codes, scales, Wik):
-    """GPU indexer K (float32 sum of d products, then bf16) vs the oracle (float64 sum,
-    then bf16): within one bf16 ulp of the oracle value plus the float32 recursive-sum
-    error bound d * 2^-24 * sum_c |deq_c * W_c| (which dominates when the sum cancels)."""
-    a = formats.bf16_value(got_bits)
-    b = formats.bf16_value(ref_bits)
-    ulp = np.abs(formats.bf16_value(ref_bits.astype(np.uint32) + 1) - b)
-    deq = formats.fp4_dequantize(codes, scales)
-    mag = np.abs(deq) @ np.abs(formats.bf16_value(Wik))
-    d = deq.shape[-1]
-    bound = ulp + d * 2.0 ** -24 * mag
-    assert (np.abs(a - b) <= bound).all(), float(np.max(np.abs(a - b) - bound))
+_check_index_k = check_index_k
 
 
 def _special_rows(r, G, d):
