@@ -159,7 +159,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 // 16-byte streaming load that does not allocate in L1 (single-use HBM data).
 __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   uint4 r;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
