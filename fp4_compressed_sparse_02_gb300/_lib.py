@@ -53,7 +53,7 @@ STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_WOR
 EXPORTS = ["csa2_compress_quant", "csa2_compress_quant_workspace", "csa2_index_full",
            "csa2_index_full_workspace", "csa2_index_reindex", "csa2_index_reindex_workspace",
            "csa2_sparse_attn", "csa2_sparse_attn_workspace", "csa2_last_error_message",
-           "csa2_get_device_error", "csa2_version", "csa2_index_full_noalloc"]
+           "csa2_get_device_error", "csa2_version", "csa2_index_full_noalloc", "csa2_selftest_wait_timeout"]
 
 _lib = None
 
@@ -88,6 +88,8 @@ def lib():
     L.csa2_last_error_message.restype = ctypes.c_char_p
     L.csa2_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     L.csa2_get_device_error.restype = c_i32
+    L.csa2_selftest_wait_timeout.argtypes = [c_i32, c_vp]
+    L.csa2_selftest_wait_timeout.restype = c_i32
     L.csa2_version.argtypes = []
     L.csa2_version.restype = c_i32
     _lib = L

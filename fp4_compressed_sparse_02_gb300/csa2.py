@@ -241,3 +241,10 @@ def device_error():
 
 def version():
     return _lib.lib().csa2_version()
+
+
+def selftest_wait_timeout(polls=1000):
+    """Run the bounded-wait failure path once (one CTA waits on an mbarrier nothing
+    arrives on, gives up after `polls` polls and sets the timeout bit of the device error
+    word)."""
+    _lib.check(_lib.lib().csa2_selftest_wait_timeout(int(polls), _stream()))

@@ -250,4 +250,10 @@ csa2_status csa2_get_device_error(uint32_t* word) {
 
 int32_t csa2_version(void) { return 100; }
 
+csa2_status csa2_selftest_wait_timeout(int32_t polls, void* stream) {
+  REQUIRE(polls >= 1 && polls <= (1 << 20), CSA2_ERR_INVALID_ARG, "polls must be in 1..2^20 (got %d)", polls);
+  return cuda_status(csa2::launch_selftest_wait(polls, static_cast<cudaStream_t>(stream)),
+                     "csa2_selftest_wait_timeout");
+}
+
 }  // extern "C"

@@ -892,6 +892,20 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
   return cudaGetLastError();
 }
 
+// One CTA waiting on an mbarrier that nothing arrives on, for at most `polls` polls: the
+// failure path of every bounded wait (error bit, no trap, the kernel returns).
+__global__ void k_selftest_wait(int polls) {
+  pdl_wait();
+  __shared__ uint64_t mb;
+  if (threadIdx.x == 0) tc::mbar_init(&mb, 1);
+  __syncthreads();
+  if (threadIdx.x == 0 && !tc::mbar_wait(&mb, 0, (uint32_t)polls)) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_selftest_wait(int polls, cudaStream_t st) {
+  return launch_k(k_selftest_wait, 1, 32, 0, st, polls);
+}
+
 cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   if (a.B == 0) return cudaSuccess;
   AttnParams ap{};

@@ -33,5 +33,6 @@ cudaError_t index_noalloc_scratch(void** ptr, size_t* bytes);
 size_t attn_workspace_bytes(const csa2_attn_args& a);
 cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st);
 uint32_t read_clear_error_attn();
+cudaError_t launch_selftest_wait(int polls, cudaStream_t st);
 
 }  // namespace csa2

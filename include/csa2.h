@@ -286,6 +286,17 @@ csa2_status csa2_get_device_error(uint32_t* word);
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t csa2_version(void);
 
+/* ------------------------------------------------------------------------------
+ * csa2_selftest_wait_timeout -- exercises the failure path of the library's bounded
+ * waits.  Every wait of the tensor-core kernels (on an mbarrier or a cluster peer)
+ * gives up after a fixed number of polls, sets CSA2_DEVERR_TIMEOUT in the device error
+ * word, skips the work that depended on it and returns, so the context stays usable.
+ * This call launches one CTA that waits on an mbarrier that nothing arrives on, giving
+ * up after `polls` polls (1 <= polls <= 2^20), so that path can be tested without a
+ * fault.  It touches no memory outside the CTA.  The pages have no counterpart to it.
+ * -------------------------------------------------------------------------- */
+csa2_status csa2_selftest_wait_timeout(int32_t polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,3 +131,16 @@ def test_swa_window_outside_rows_is_flagged():
                                   to_dev(c["tlen"]), to_dev(c["swa"]), to_dev(c["swa_scale"]),
                                   to_dev(c["swa_start"]), to_dev(c["swa_len"]), c["W"])
     assert csa2.device_error() & 0x20
+
+
+def test_bounded_wait_times_out_reports_and_context_survives():
+    # a wait that nothing satisfies gives up, sets the timeout bit and returns
+    csa2.selftest_wait_timeout(1000)
+    assert csa2.device_error() & 0x80
+    assert csa2.device_error() == 0                 # the word was cleared by the read
+    # the context is still usable: a normal call right after runs and agrees
+    r = np.random.default_rng(55)
+    c = _case(r, 3, 64, 512, 512, 128, n=2000)
+    out, _ = _run(c)
+    ref, _ = _oracle(c)
+    _assert_close(out, ref)
