@@ -368,11 +368,11 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // all eight warps (two per quarter, each taking half of the keys or dims) share the
 // softmax and the epilogue; the 16x32bx2 access shape gives lanes 0..15 and 16..31 of a
 // warp two column ranges of the same 16 heads, so every thread carries data.
-// The epilogue writes o = O / l (fp16) into the Q space (free after MMA1), rows of 1 KB
-// per head.  CTA r owns the merge of heads [16 r, 16 r + 16): once every CTA of the
-// cluster has finished MMA2, the others send it their blocks of those heads (and their
-// (max, l) pairs) with shared-to-shared bulk copies into its KV space, and it combines the
-// 4 chunks from its own shared memory.
+// CTA r owns the merge of heads [16 r, 16 r + 16).  Once every CTA of the cluster has
+// finished MMA1 (a cluster barrier), the epilogue writes o = O / l (fp16) of each head and
+// its (max, l) pair straight into the owning CTA's Q space (slot = this chunk, 1 KB rows)
+// with distributed-shared-memory stores; a second cluster barrier (release / acquire)
+// makes them visible, and the owner combines the 4 chunks from its own shared memory.
 // ---------------------------------------------------------------------------------
 namespace tca {
 constexpr int NW = 256;                         // data threads: warps 0..7
@@ -392,10 +392,10 @@ struct Misc {                                   // small per-CTA state, after th
   int keyok[NK];
   float pmax[2][HQ];
   float psum[2][HQ];
-  alignas(16) float2 mlx[HQ];     // this chunk's (row max in log2 units, row sum) per head
-  alignas(16) float2 rml[NCH - 1][HQ / NCH];   // received (max, sum) of the other chunks
-  uint64_t mbar[7];               // 0: MMA1, 1..4: MMA2 quarters, 5: received merge blocks,
-                                  // 6: quarter 0's columns read by the 8 data warps
+  alignas(16) float2 rml[NCH][HQ / NCH];   // (row max in log2 units, row sum) of each chunk
+                                           // for this CTA's 16 heads
+  uint64_t mbar[7];               // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
+                                  // by the 8 data warps
   uint32_t tslot;
   int ok_flag;
 };
@@ -403,8 +403,7 @@ constexpr int SMEM = SM_KV + SM_Q + (int)sizeof(Misc);   // no static shared mem
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;                   // S, then P over its first 80 columns
 constexpr uint32_t MAX_POLL = 1u << 22;
-constexpr int BLK = HQ / NCH * DIM * 2;         // one CTA's merge block: 16 heads x 512 dims fp16
-constexpr uint32_t RECV_BYTES = (NCH - 1) * (BLK + HQ / NCH * 8);
+constexpr int BLK = HQ / NCH * DIM * 2;         // one chunk's block of 16 heads x 512 dims fp16
 
 __device__ __forceinline__ uint32_t col_o(int q) { return q == 0 ? 256u : q == 1 ? 384u : q == 2 ? 128u : 256u; }
 
@@ -433,7 +432,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   int* keyok = ms.keyok;
   float (*pmax)[HQ] = ms.pmax;
   float (*psum)[HQ] = ms.psum;
-  float2* mlx = ms.mlx;
   uint64_t* mbar = ms.mbar;
   int& ok_flag = ms.ok_flag;
 
@@ -457,7 +455,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
     for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
     tc::mbar_init(&mbar[6], NW / 32);
-    tc::mbar_arrive_expect_tx(&mbar[5], RECV_BYTES);   // the other chunks' merge blocks
     ok_flag = 1;
   }
   // ---- Q first: 16 chunks of 16 bytes per thread, a warp reading 512 contiguous bytes --
@@ -586,6 +583,9 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   __syncthreads();
   tc::fence_after_sync();
+  // Q is no longer read: the cluster may write merge blocks into this CTA's Q space.  Nothing
+  // written before this point is read by another CTA, so the arrive need not release.
+  tc::cluster_arrive_relaxed();
   // ---- softmax: a head's 160 keys are split over four threads: warps w and w ^ 4 take
   //      halves of 80, and within a warp threads t and t + 16 take 40 each -------------------
   const int sub = lane >> 4;                    // which 40-key (or 32-column) sub-range
@@ -654,6 +654,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
     tc::mma_commit(&mbar[1 + q]);
   };
+  const int rank = (int)tc::cluster_ctarank();
   if (!worker) {                                // warp 8
     if (lane == 0 && ok_flag) {
       issue_quarter(0);
@@ -668,16 +669,23 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
     }
     __syncwarp();
-    tc::cluster_arrive_relaxed();               // this warp reads no shared memory
+    tc::cluster_wait();                         // (every CTA has finished MMA1)
+    tc::cluster_arrive();                       // this warp writes nothing to the cluster
   }
   if (worker) {
-    if (tid < HQ) {
-      const float l = psum[0][tid] + psum[1][tid];
-      mlx[tid] = (ok_flag && l > 0.f) ? make_float2(fmaxf(pmax[0][tid], pmax[1][tid]), l) : make_float2(-INFINITY, 0.f);
-    }
     const float lh = psum[0][head] + psum[1][head];
-    const float li = (ok_flag && lh > 0.f) ? 1.f / lh : 0.f;
+    const bool anyh = ok_flag && lh > 0.f;
+    const float li = anyh ? 1.f / lh : 0.f;
     bool ok = ok_flag != 0;
+    // the heads of warp w belong to CTA w % 4 (heads [16 (w % 4), 16 (w % 4) + 16)); its
+    // 16-byte pieces of o go straight into that CTA's Q space, slot `rank`, row h % 16
+    const uint32_t dst_blk = tc::mapa(q_a + rank * BLK + (head & 15) * 1024, warp & 3);
+    tc::cluster_wait();                         // every CTA has finished MMA1: Q spaces free
+    if (lv && kh == 0) {
+      const float mh = fmaxf(pmax[0][head], pmax[1][head]);
+      tc::st_dsmem_f2(tc::mapa(smem_u32(&ms.rml[rank][head & 15]), warp & 3),
+                      anyh ? make_float2(mh, lh) : make_float2(-INFINITY, 0.f));
+    }
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       if (ok) {
@@ -685,7 +693,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
         if (!ok && lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
       }
       tc::fence_after_sync();
-      if (q == 3) tc::cluster_arrive_relaxed();   // the KV tile is no longer read: peers may send
       if (ok) {                                   // 16 heads x 64 columns per warp
         uint32_t r[32];
         tc::tmem_ld16x2_32<32>(tb + lane_base + col_o(q) + 64 * kh, r);
@@ -700,7 +707,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
             pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
           }
           const int ch = 16 * q + 8 * kh + 4 * sub + i;
-          *reinterpret_cast<uint4*>(sQ + head * 1024 + ((ch ^ (head & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          tc::st_dsmem_v4(dst_blk + ((ch ^ (head & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
       }
       if (q == 0) {
@@ -710,28 +717,11 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
     }
     if (!ok && lane == 0) ok_flag = 0;
+    tc::cluster_arrive();                       // releases this thread's stores to the cluster
   }
-  // ---- merge: CTA r owns heads [16 r, 16 r + 16).  Each CTA sends the block of every
-  //      other CTA (16 heads x 1 KB of its fp16 o, then their 16 (max, sum) pairs) into that
-  //      CTA's KV space by bulk copies, then combines the 4 chunks of its own heads from
-  //      local shared memory.  Slot j of CTA r holds chunk (r + 1 + j) % 4. ---------------
-  const int rank = (int)tc::cluster_ctarank();
-  tc::fence_proxy_async_smem();                 // epilogue stores -> bulk-copy reads
-  __syncthreads();
-  tc::cluster_wait();                           // every CTA has finished MMA2
-  if (tid == 0) {
-#pragma unroll
-    for (int j = 0; j < NCH - 1; ++j) {
-      const int dst = (rank + 1 + j) % NCH;
-      const int slot = (rank - dst - 1 + 2 * NCH) % NCH;       // rank = (dst + 1 + slot) % 4
-      const uint32_t mb = tc::mapa(smem_u32(&mbar[5]), dst);
-      tc::bulk_copy_to_cluster(tc::mapa(kv_a + slot * BLK, dst), sQ + dst * BLK, BLK, mb);
-      tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.rml[slot][0]), dst), &mlx[16 * dst], HQ / NCH * 8, mb);
-    }
-    ok_flag = (wait_mma(&mbar[5], 0) ? 1 : 0) & ok_flag;
-  }
-  __syncthreads();
-  tc::cluster_arrive_relaxed();                 // this CTA has received every block
+  tc::cluster_wait();                           // every chunk's block of this CTA's heads is here
+  // ---- merge: CTA r combines the 4 chunks of heads [16 r, 16 r + 16) from its Q space
+  //      (slot c = chunk c) -------------------------------------------------------------
   {
     float* wts = reinterpret_cast<float*>(&pmax[0][0]);       // [16][NCH] merge weights
     if (tid < 16) {
@@ -740,7 +730,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       float M = -INFINITY, L = 0.f;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        mv[c] = (c == rank) ? mlx[h] : ms.rml[(c - rank - 1 + NCH) % NCH][tid];
+        mv[c] = ms.rml[c][tid];
         M = fmaxf(M, mv[c].x);
       }
       float w4[NCH];
@@ -767,7 +757,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         const float wgt = wts[hh * NCH + c];
-        const uint8_t* src = (c == rank) ? sQ + rank * BLK : sKV + ((c - rank - 1 + NCH) % NCH) * BLK;
+        const uint8_t* src = sQ + c * BLK;
         const uint4 u = *reinterpret_cast<const uint4*>(src + off);
         const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -793,7 +783,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
     }
   }
-  tc::cluster_wait();                            // every block sent from here has landed
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TMEM_COLS);

@@ -210,6 +210,13 @@ __device__ __forceinline__ int ld_dsmem_s32(uint32_t caddr) {
   return v;
 }
 
+__device__ __forceinline__ void st_dsmem_v4(uint32_t caddr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f2(uint32_t caddr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};" :: "r"(caddr), "f"(v.x), "f"(v.y) : "memory");
+}
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t caddr) {
   float2 v;
   asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr));
