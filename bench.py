@@ -25,11 +25,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from fp4_compressed_sparse_02_gb300 import build as libbuild  # noqa: E402
-from fp4_compressed_sparse_02_gb300 import synth, workload  # noqa: E402
+from fp4_compressed_sparse_02_gb300 import csa2, synth, workload  # noqa: E402
 from fp4_compressed_sparse_02_gb300.schedule import FULL, REINDEX, REUSE  # noqa: E402
 
 METRIC = "CSA2 decode query-layers/s at 128K–1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
-WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M}
+WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M, "prefill_compress": synth.PREFILL}
 
 
 def peaks():
@@ -39,6 +39,15 @@ def peaks():
             j = json.load(f)
         return j.get("hbm_gbs", 6800.0), "measured"
     return 6800.0, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor peak (burst) of this GPU, TFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f).get("bf16_tflops", 1900.0), "measured"
+    return 1900.0, "fallback"
 
 
 PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
@@ -156,6 +165,67 @@ def run_reference(a):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_compress(a):
+    """The compressor of the encoder prefill chunk alone (65,536 bf16 tokens at m = 2 into
+    32,768 FP4 entries with their indexer K): the tensor-bound step, timed on one GPU
+    against the measured bf16 tensor peak."""
+    import math
+    libbuild.build()
+    cfg = synth.PREFILL
+    T, m, d, d_model, d_ik, d_rope = (cfg[x] for x in ("T", "m", "d", "d_model", "d_ik", "d_rope"))
+    G = T // m
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(0)
+    H = torch.randn((T, d_model), generator=g, device=dev).to(torch.bfloat16)
+    Wkv = (torch.randn((d_model, d), generator=g, device=dev) / math.sqrt(d_model)).to(torch.bfloat16)
+    Wz = (torch.randn((d_model, d), generator=g, device=dev) / math.sqrt(d_model)).to(torch.bfloat16)
+    Wik = (torch.randn((d, d_ik), generator=g, device=dev) / math.sqrt(d)).to(torch.bfloat16)
+    pt = torch.randperm(G // 64, generator=torch.Generator().manual_seed(0)).to(torch.int32).reshape(1, -1)
+    cache = csa2.PagedCache.allocate(1, G, d, d_ik, dev, pt)
+    seq = torch.zeros(G, dtype=torch.int32, device=dev)
+    entry = torch.arange(G, dtype=torch.int32, device=dev)
+    pos = torch.arange(G, dtype=torch.int32, device=dev) * m + m - 1
+    cos, sin = (torch.from_numpy(t).to(dev) for t in synth.rope_tables(T, d_rope))
+    ws = csa2.Workspace()
+    stream = torch.cuda.Stream()
+
+    def step():
+        csa2.compress_quant(cache, seq, entry, m=m, H=H, W_kv=Wkv, W_z=Wz, pos=pos, rope_cos=cos, rope_sin=sin,
+                            W_ik=Wik, ws=ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            step()
+    torch.cuda.synchronize()
+    assert csa2.device_error() == 0
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(a.steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / a.steps
+    flops = 2.0 * T * d_model * 2 * d + 2.0 * G * d * d_ik        # the two projections + indexer K
+    tflops = flops / (ms / 1000.0) / 1e12
+    peak, peak_kind = bf16_peak()
+    line = {"metric": "CSA2 compressor of the encoder prefill chunk (tokens/s)", "value": T / (ms / 1000.0),
+            "unit": "tokens/s", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"prefill_compress: T={T} bf16 tokens, m={m}, d_model={d_model}, d={d}, "
+                                   f"d_ik={d_ik} -> {G} FP4 entries", "l2": "inputs larger than L2 (671 MB of H)"},
+            "roofline": {"bound": "tensor", "kernel": "csa2_compress_quant (k_proj_tc + k_quant + k_index_k)",
+                         "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                         "traffic": None, "peak_source": peak_kind, "flop_per_step": flops},
+            "clocks": clk, "gpu_launches": 3 * a.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -169,6 +239,10 @@ def main():
     a.warmup = max(a.warmup, 3)
     if a.impl == "reference":
         run_reference(a)
+        return
+
+    if a.workload == "prefill_compress":
+        run_prefill_compress(a)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
