@@ -570,7 +570,9 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   if (a.W_ik && G > 0) {
     const bool many = G >= 2048;
     cudaError_t e;
-    if (a.cache.d_ik == 128)
+    if (index_k_tc_supported(a, G))
+      e = launch_index_k_tc(a, G, st);
+    else if (a.cache.d_ik == 128)
       e = many ? launch_index_k<8, 128>(a, G, st) : launch_index_k<1, 128>(a, G, st);
     else
       e = many ? launch_index_k<8, 64>(a, G, st) : launch_index_k<1, 64>(a, G, st);

@@ -18,6 +18,8 @@ uint32_t read_clear_error_compress();
 bool project_tc_supported(const csa2_compress_args& a);
 cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, cudaStream_t st);
 uint32_t read_clear_error_proj();
+bool index_k_tc_supported(const csa2_compress_args& a, int G);
+cudaError_t launch_index_k_tc(const csa2_compress_args& a, int G, cudaStream_t st);
 
 // index.cu
 size_t index_full_workspace_bytes(const csa2_index_full_args& a);
