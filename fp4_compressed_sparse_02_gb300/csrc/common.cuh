@@ -164,6 +164,34 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   return r;
 }
 
+// FP4 of one 16-channel group: scale byte = E4M3_RNE_satfinite(amax / 6), codes =
+// E2M1_RNE_sat(y_i / s) (float32 divisions), two codes per byte with the even channel in
+// the low nibble; a zero scale gives zero codes.
+__device__ __forceinline__ void fp4_group16(const float* y, uint32_t& w0, uint32_t& w1, uint32_t& sbyte) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(y[i]));
+  sbyte = cvt_e4m3(__fdiv_rn(a, 6.0f));
+  const float s = e4m3_to_f32(sbyte);
+  w0 = 0;
+  w1 = 0;
+  if (s > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w0 |= cvt_e2m1x2(__fdiv_rn(y[2 * i], s), __fdiv_rn(y[2 * i + 1], s)) << (8 * i);
+      w1 |= cvt_e2m1x2(__fdiv_rn(y[8 + 2 * i], s), __fdiv_rn(y[9 + 2 * i], s)) << (8 * i);
+    }
+  }
+}
+
+// RoPE of one channel pair, every product and sum rounded on its own.
+__device__ __forceinline__ void rope_pair(float& x0, float& x1, float cs, float sn) {
+  const float y0 = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+  const float y1 = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+  x0 = y0;
+  x1 = y1;
+}
+
 // Order-preserving map float -> uint32 (larger float -> larger key); -0 maps like +0.
 __device__ __forceinline__ uint32_t float_key(float f) {
   if (f == 0.0f) f = 0.0f;   // -0 and +0 get one key

@@ -323,12 +323,7 @@ __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
       const float* ct = p.rope_cos + (long long)ps * half + (c0 - rb) / 2;
       const float* st = p.rope_sin + (long long)ps * half + (c0 - rb) / 2;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float cs = __ldg(ct + i), sn = __ldg(st + i);
-        float x0 = y[2 * i], x1 = y[2 * i + 1];
-        y[2 * i] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-        y[2 * i + 1] = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
-      }
+      for (int i = 0; i < 8; ++i) rope_pair(y[2 * i], y[2 * i + 1], __ldg(ct + i), __ldg(st + i));
     }
   }
   if (p.y_out) {
@@ -336,20 +331,8 @@ __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) yo[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
   }
-  // scale = E4M3_RNE_satfinite(amax / 6); codes = E2M1_RNE_sat(y / scale)
-  float a = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(y[i]));
-  uint32_t sbyte = cvt_e4m3(__fdiv_rn(a, 6.0f));
-  float s = e4m3_to_f32(sbyte);
-  uint32_t w0 = 0, w1 = 0;
-  if (s > 0.f) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w0 |= cvt_e2m1x2(__fdiv_rn(y[2 * i], s), __fdiv_rn(y[2 * i + 1], s)) << (8 * i);
-      w1 |= cvt_e2m1x2(__fdiv_rn(y[8 + 2 * i], s), __fdiv_rn(y[9 + 2 * i], s)) << (8 * i);
-    }
-  }
+  uint32_t w0, w1, sbyte;
+  fp4_group16(y, w0, w1, sbyte);
   long long row = entry_row(p.cache, __ldg(p.seq + g), __ldg(p.entry + g), &g_err_compress);
   if (row < 0) return;
   uint2* cd = reinterpret_cast<uint2*>(p.cache.codes + row * (p.d / 2) + q * 8);
@@ -485,9 +468,19 @@ static int pick_splits(int T, int d_model, int N) {
   return s;
 }
 
+// The indexer-K projection of the G new entries (when W_ik is given).
+static cudaError_t launch_index_k_any(const csa2_compress_args& a, int G, cudaStream_t st) {
+  if (!a.W_ik || G <= 0) return cudaSuccess;
+  const bool many = G >= 2048;
+  if (index_k_tc_supported(a, G)) return launch_index_k_tc(a, G, st);
+  if (a.cache.d_ik == 128) return many ? launch_index_k<8, 128>(a, G, st) : launch_index_k<1, 128>(a, G, st);
+  return many ? launch_index_k<8, 64>(a, G, st) : launch_index_k<1, 64>(a, G, st);
+}
+
 size_t compress_workspace_bytes(const csa2_compress_args& a) {
   if (!a.W_kv) return 0;
   int N = a.cache.d * (a.m > 1 ? 2 : 1);
+  if (project_tc_fused(a)) return 0;
   if (project_tc_supported(a)) return (size_t)a.T * N * sizeof(float);
   int s = !use_small(a) ? pick_splits(a.T, a.d_model, N)
           : (a.h_dtype == CSA2_BF16 ? mma_splits(a.d_model, N) : small_splits(a.T, a.d_model, N));
@@ -502,9 +495,15 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
     int N = d * (a.m > 1 ? 2 : 1);
     float* out = static_cast<float*>(ws);
     int s;
+    if (project_tc_fused(a)) {
+      // projection, pooling, RoPE and FP4 in one kernel; then the indexer K
+      cudaError_t e = launch_project_tc(a, nullptr, true, st);
+      if (e != cudaSuccess) return e;
+      return launch_index_k_any(a, G, st);
+    }
     if (project_tc_supported(a)) {
       s = 1;
-      cudaError_t e = launch_project_tc(a, out, st);
+      cudaError_t e = launch_project_tc(a, out, false, st);
       if (e != cudaSuccess) return e;
     } else if (use_small(a) && a.h_dtype == CSA2_BF16) {
       s = mma_splits(a.d_model, N);
@@ -567,17 +566,8 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   qp.y_out = a.y_out;
   long long threads = (long long)G * (d / 16);
   if (threads > 0) launch_k(k_quant, (unsigned)((threads + 255) / 256), 256, 0, st, qp);
-  if (a.W_ik && G > 0) {
-    const bool many = G >= 2048;
-    cudaError_t e;
-    if (index_k_tc_supported(a, G))
-      e = launch_index_k_tc(a, G, st);
-    else if (a.cache.d_ik == 128)
-      e = many ? launch_index_k<8, 128>(a, G, st) : launch_index_k<1, 128>(a, G, st);
-    else
-      e = many ? launch_index_k<8, 64>(a, G, st) : launch_index_k<1, 64>(a, G, st);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = launch_index_k_any(a, G, st);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

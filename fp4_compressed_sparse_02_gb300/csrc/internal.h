@@ -16,7 +16,8 @@ uint32_t read_clear_error_compress();
 
 // proj_tc.cu: tensor-core projection for many bf16 tokens (out[T][d or 2d], fp32)
 bool project_tc_supported(const csa2_compress_args& a);
-cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, cudaStream_t st);
+bool project_tc_fused(const csa2_compress_args& a);     // pooling, RoPE and FP4 in the epilogue
+cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, bool fuse, cudaStream_t st);
 uint32_t read_clear_error_proj();
 bool index_k_tc_supported(const csa2_compress_args& a, int G);
 cudaError_t launch_index_k_tc(const csa2_compress_args& a, int G, cudaStream_t st);

@@ -30,7 +30,7 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;                 // 16 KB
 constexpr int B_BYTES = BN * BK * 2;                 // 32 KB: four 64-column blocks of 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM = STAGES * STAGE_BYTES + 128;     // + mbarriers and the TMEM slot
+constexpr int SMEM = STAGES * STAGE_BYTES + 128;     // + mbarriers and the TMEM slot (< 128 B)
 constexpr int THREADS = 192;
 constexpr uint32_t MAX_POLL = 1u << 24;
 }  // namespace ptc
@@ -43,11 +43,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The pooling / RoPE / FP4 epilogue fused into the GEMM (m = 1 or 2): at m = 2 a tile holds
+// channels [128 x, 128 x + 128) of C (TMEM columns 0..127) and of Z (128..255), and the two
+// tokens of a group are adjacent TMEM lanes of one warp, paired by a shuffle; at m = 1 a
+// tile holds channels [256 x, 256 x + 256) of C.  The arithmetic is k_quant's.
+struct ProjEpi {
+  csa2_cache cache;
+  const int* seq;
+  const int* entry;
+  const int* pos;
+  const float* rope_cos;
+  const float* rope_sin;
+  int d_rope, rope_max_pos, m, G;
+  float* y_out;
+};
+
+template <bool FUSE>
 __global__ void __launch_bounds__(ptc::THREADS, 1)
     k_proj_tc(const __grid_constant__ CUtensorMap mh, const __grid_constant__ CUtensorMap mkv,
-              const __grid_constant__ CUtensorMap mz, float* __restrict__ out, int T, int d_model, int d, int N) {
+              const __grid_constant__ CUtensorMap mz, float* __restrict__ out, int T, int d_model, int d, int N,
+              int ntn, int ntiles, ProjEpi ep) {
   using namespace ptc;
-  pdl_wait();                                        // many waves: dependents start at completion
+  pdl_wait();                                        // a persistent grid: dependents start at completion
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if ((smem_u32(smem) & 1023) != 0) {                // the same in every CTA
@@ -56,88 +73,201 @@ __global__ void __launch_bounds__(ptc::THREADS, 1)
   }
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(accf + 1);
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-  const CUtensorMap* mw = (n0 < d) ? &mkv : &mz;
-  const int nw0 = (n0 < d) ? n0 : n0 - d;
-  if (warp == 1) tc::tmem_alloc(tslot, BN);
+  uint64_t* accf = empty + STAGES;                   // [2] accumulator buffer b complete
+  uint64_t* acce = accf + 2;                         // [2] accumulator buffer b drained
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acce + 2);
+  const bool pair = FUSE && ep.m == 2;
+  if (warp == 1) tc::tmem_alloc(tslot, 2 * BN);
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(accf, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 4);                    // one arrival per epilogue warp
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
   const int nk = d_model / BK;
+  // tile t: output rows [128 (t / ntn), +128), column tile t % ntn (consecutive tiles share
+  // their rows of H, which L2 then serves to the other column tiles)
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % STAGES;
-        if (kb >= STAGES && !tc::mbar_wait(&empty[s], ((kb / STAGES) - 1) & 1, MAX_POLL)) {
-          raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
-          break;
-        }
-        uint8_t* st = smem + s * STAGE_BYTES;
-        tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-        tma_load_2d(st, &mh, kb * BK, m0, &full[s]);
+      long long it = 0;                              // K blocks issued by this CTA
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int m0 = (t / ntn) * BM, nt = t % ntn;
+        const int n0 = nt * BN;
+        const CUtensorMap* mw = (n0 < d) ? &mkv : &mz;
+        const int nw0 = (n0 < d) ? n0 : n0 - d;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (it >= STAGES && !tc::mbar_wait(&empty[s], (uint32_t)(((it / STAGES) - 1) & 1), MAX_POLL)) {
+            raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * STAGE_BYTES;
+          tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+          tma_load_2d(st, &mh, kb * BK, m0, &full[s]);
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(st + A_BYTES + j * 8192, mw, nw0 + 64 * j, kb * BK, &full[s]);
+          for (int j = 0; j < BN / 64; ++j) {
+            const CUtensorMap* mj = pair ? (j < 2 ? &mkv : &mz) : mw;
+            const int col = pair ? 128 * nt + 64 * (j & 1) : nw0 + 64 * j;
+            tma_load_2d(st + A_BYTES + j * 8192, mj, col, kb * BK, &full[s]);
+          }
+        }
+        if (!ok) break;
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_f16(BM, BN, 1, 0, 1);   // bf16; A K-major, B MN-major
+      long long it = 0;
+      int tl = 0;                                    // tiles of this CTA
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % STAGES;
-        if (!tc::mbar_wait(&full[s], (kb / STAGES) & 1, MAX_POLL)) {
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++tl) {
+        const int b = tl & 1;
+        if (tl >= 2 && !tc::mbar_wait(&acce[b], (uint32_t)(((tl >> 1) - 1) & 1), MAX_POLL)) {
           raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
-          ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t a = smem_u32(smem + s * STAGE_BYTES), bb = a + A_BYTES;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!tc::mbar_wait(&full[s], (uint32_t)((it / STAGES) & 1), MAX_POLL)) {
+            raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t a = smem_u32(smem + s * STAGE_BYTES), bb = a + A_BYTES;
 #pragma unroll
-        for (int k16 = 0; k16 < BK / 16; ++k16) {
-          const uint64_t ad = tc::smem_desc_sw128(a + 32 * k16, 16, 1024);
-          const uint64_t bd = tc::smem_desc_sw128(bb + 2048 * k16, 8192, 1024);
-          tc::mma_f16_ss(tb, ad, bd, idesc, (kb | k16) != 0 ? 1u : 0u);
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint64_t ad = tc::smem_desc_sw128(a + 32 * k16, 16, 1024);
+            const uint64_t bd = tc::smem_desc_sw128(bb + 2048 * k16, 8192, 1024);
+            tc::mma_f16_ss(tb + (uint32_t)(BN * b), ad, bd, idesc, (kb | k16) != 0 ? 1u : 0u);
+          }
+          tc::mma_commit(&empty[s]);                 // the stage is free once these have read it
         }
-        tc::mma_commit(&empty[s]);                 // the stage is free once these have read it
+        tc::mma_commit(&accf[b]);                    // buffer b holds tile t
       }
-      tc::mma_commit(accf);                        // the accumulator is complete
     }
   } else {
-    const int q = warp & 3;                        // warps 2..5 -> lane quarters 2, 3, 0, 1
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(accf, 0, MAX_POLL));
-    if (!ok && lane == 0) raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
-    tc::fence_after_sync();
-    if (ok) {
+    const int q = warp & 3;                          // warps 2..5 -> lane quarters 2, 3, 0, 1
+    int tl = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++tl) {
+      const int b = tl & 1;
+      const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&accf[b], (uint32_t)((tl >> 1) & 1), MAX_POLL));
+      if (!ok) {
+        if (lane == 0) raise_error(&g_err_proj, CSA2_DEVERR_TIMEOUT);
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t tq = tb + ((uint32_t)(32 * q) << 16) + (uint32_t)(BN * b);
+      const int m0 = (t / ntn) * BM, nt = t % ntn;
       const int row = m0 + 32 * q + lane;
+      if (!FUSE) {
+        const int n0 = nt * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tc::tmem_ld32(tb + ((uint32_t)(32 * q) << 16) + (uint32_t)c, r);
-        tc::tmem_ld_wait();
-        if (row < T) {
-          float4* o = reinterpret_cast<float4*>(out + (long long)row * N + n0 + c);
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          tc::tmem_ld32(tq + (uint32_t)c, r);
+          tc::tmem_ld_wait();
+          if (row < T) {
+            float4* o = reinterpret_cast<float4*>(out + (long long)row * N + n0 + c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), __uint_as_float(r[4 * i + 2]),
-                               __uint_as_float(r[4 * i + 3]));
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                 __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          }
+        }
+      } else {
+        const int CW = pair ? 128 : 256;             // channels of the tile
+        const int cbase = nt * CW;
+        const int g = row / ep.m;                    // entry (group)
+        const bool writer = row < T && (!pair || (lane & 1) == 0);
+        long long erow = -1;
+        int ps = -1;
+        if (writer && g < ep.G) {
+          erow = entry_row(ep.cache, __ldg(ep.seq + g), __ldg(ep.entry + g), &g_err_proj);
+          if (ep.d_rope > 0 && cbase + CW > d - ep.d_rope) {
+            ps = __ldg(ep.pos + g);
+            if (ps < 0 || ps >= ep.rope_max_pos) {
+              raise_error(&g_err_proj, CSA2_DEVERR_POS);
+              ps = -1;
+            }
+          }
+        }
+        const int rb = d - ep.d_rope, half = ep.d_rope / 2;
+#pragma unroll 1
+        for (int c = 0; c < CW; c += 32) {
+          uint32_t cv[32], zv[32];
+          tc::tmem_ld32(tq + (uint32_t)c, cv);
+          if (pair) tc::tmem_ld32(tq + 128u + (uint32_t)c, zv);
+          tc::tmem_ld_wait();
+          float y[32];
+          if (pair) {
+            const bool first = (lane & 1) == 0;      // the group's first token
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float c_me = __uint_as_float(cv[i]), z_me = __uint_as_float(zv[i]);
+              const float c_ot = __shfl_xor_sync(0xffffffffu, c_me, 1), z_ot = __shfl_xor_sync(0xffffffffu, z_me, 1);
+              const float c0 = first ? c_me : c_ot, c1 = first ? c_ot : c_me;
+              const float z0 = first ? z_me : z_ot, z1 = first ? z_ot : z_me;
+              const float zmax = fmaxf(fmaxf(-INFINITY, z0), z1);
+              const float e0 = expf(z0 - zmax), e1 = expf(z1 - zmax);
+              float den = 0.f, num = 0.f;
+              den += e0;
+              num = fmaf(e0, c0, num);
+              den += e1;
+              num = fmaf(e1, c1, num);
+              y[i] = num / den;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) y[i] = __uint_as_float(cv[i]);
+          }
+          if (!writer) continue;
+          const int ch0 = cbase + c;
+          if (ps >= 0) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2)
+              if (ch0 + i >= rb) {
+                const long long ti = (long long)ps * half + (ch0 + i - rb) / 2;
+                rope_pair(y[i], y[i + 1], __ldg(ep.rope_cos + ti), __ldg(ep.rope_sin + ti));
+              }
+          }
+          if (ep.y_out && g < ep.G) {
+            float4* yo = reinterpret_cast<float4*>(ep.y_out + (long long)g * d + ch0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yo[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+          }
+          if (erow >= 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t w0, w1, sb;
+              fp4_group16(y + 16 * h, w0, w1, sb);
+              const int grp = (ch0 + 16 * h) / 16;
+              *reinterpret_cast<uint2*>(ep.cache.codes + erow * (d / 2) + grp * 8) = make_uint2(w0, w1);
+              ep.cache.scales[erow * (d / 16) + grp] = (uint8_t)sb;
+            }
+          }
         }
       }
+      tc::fence_before_sync();                       // this warp's TMEM reads of buffer b are done
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acce[b]);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 1) tc::tmem_dealloc(tb, BN);
+  if (warp == 1) tc::tmem_dealloc(tb, 2 * BN);
 }
 
 // ---------------------------------------------------------------------------------
@@ -327,6 +457,11 @@ static bool bf16_map(CUtensorMap* map, const void* base, long long rows, long lo
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The fused epilogue handles m = 1 (256-channel tiles) and m = 2 (128 channels of C and Z).
+bool project_tc_fused(const csa2_compress_args& a) {
+  return project_tc_supported(a) && (a.m == 1 || a.m == 2) && a.cache.d % 256 == 0 && a.d_rope % 2 == 0;
+}
+
 bool project_tc_supported(const csa2_compress_args& a) {
   const int N = a.cache.d * (a.m > 1 ? 2 : 1);
   const bool aligned = ((uintptr_t)a.H & 15) == 0 && ((uintptr_t)a.W_kv & 15) == 0 &&
@@ -335,20 +470,48 @@ bool project_tc_supported(const csa2_compress_args& a) {
          N % ptc::BN == 0 && aligned && tensor_map_encoder() != nullptr;
 }
 
-cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, cudaStream_t st) {
+cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, bool fuse, cudaStream_t st) {
   const int d = a.cache.d, N = d * (a.m > 1 ? 2 : 1);
   CUtensorMap mh, mkv, mz;
   if (!bf16_map(&mh, a.H, a.T, a.d_model, ptc::BM) || !bf16_map(&mkv, a.W_kv, a.d_model, d, ptc::BK) ||
       !bf16_map(&mz, a.m > 1 ? a.W_z : a.W_kv, a.d_model, d, ptc::BK))
     return cudaErrorInvalidValue;
+  ProjEpi ep{};
+  ep.cache = a.cache;
+  ep.seq = a.seq;
+  ep.entry = a.entry;
+  ep.pos = a.pos;
+  ep.rope_cos = a.rope_cos;
+  ep.rope_sin = a.rope_sin;
+  ep.d_rope = a.d_rope;
+  ep.rope_max_pos = a.rope_max_pos;
+  ep.m = a.m;
+  ep.G = a.T / a.m;
+  ep.y_out = a.y_out;
+  const int ntn = fuse ? (a.m == 2 ? d / 128 : d / 256) : N / ptc::BN;
+  const int ntiles = ntn * ((a.T + ptc::BM - 1) / ptc::BM);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const dim3 grid((unsigned)(ntiles < sms ? ntiles : (sms > 0 ? sms : 1)));   // persistent: one CTA per SM
+  if (fuse) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(k_proj_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    return launch_k(k_proj_tc<true>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N, ntn,
+                    ntiles, ep);
+  }
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_proj_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_proj_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, ptc::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const dim3 grid(N / ptc::BN, (a.T + ptc::BM - 1) / ptc::BM);
-  return launch_k(k_proj_tc, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N);
+  return launch_k(k_proj_tc<false>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N, ntn,
+                  ntiles, ep);
 }
 
 uint32_t read_clear_error_proj() {

@@ -115,11 +115,14 @@ def test_quant_given_rows_pooled(m):
 @pytest.mark.parametrize("h_dtype,m,T,d_model", [("bf16", 1, 512, 256), ("f32", 1, 512, 256), ("bf16", 2, 512, 256),
                                                ("bf16", 1, 200, 5120), ("bf16", 2, 384, 1024),
                                                ("bf16", 1, 32, 5120), ("f32", 1, 64, 1024), ("bf16", 2, 64, 512),
-                                               ("bf16", 1, 1, 5120)])
+                                               ("bf16", 1, 1, 5120), ("bf16", 4, 512, 1024),
+                                               ("bf16", 2, 24576, 512), ("bf16", 4, 24576, 256)])
 def test_compress_projection(h_dtype, m, T, d_model):
     # T <= 64 takes the few-row projection (decode append); larger bf16 T the tensor-core
     # GEMM (ragged last tile at T = 200, an 80-deep K loop at d_model = 5120, W_KV and W_Z
-    # column tiles at m = 2); f32 H the tiled SIMT one
+    # column tiles at m = 2, pooling/RoPE/FP4 in its epilogue at m <= 2, several tiles per
+    # CTA of the persistent grid through both accumulator buffers at T = 24576); f32 H the
+    # tiled SIMT one
     r = np.random.default_rng(300 + m + T)
     d, d_ik = 512, 128
     if h_dtype == "bf16":
