@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 #include <cstdlib>
 
@@ -354,8 +355,9 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // a thread-block cluster.
 //   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle)      160 KB
 //            Q 64 heads x 512 dims fp16 (K-major, 128-byte swizzle)               64 KB
-//            Q is loaded at kernel start (it depends on nothing), converted
-//            bf16 -> fp16 in registers and stored swizzled.
+//            Q arrives by TMA (bf16, 64-dim x 16-head boxes, each CTA fetching 16 heads
+//            and multicasting them to the cluster) issued at kernel start; the data
+//            threads convert it to fp16 in place while their gathers are in flight.
 //   TMEM   : S = Q K^T (fp32, 160 columns)                              cols   0..159
 //            P = softmax numerators (fp16 pairs, A operand)             cols   0..79
 //            O quarter q = P V[:, 128q..] (fp32)      q0: 256..383, q1: 384..511,
@@ -394,16 +396,21 @@ struct Misc {                                   // small per-CTA state, after th
   float psum[2][HQ];
   alignas(16) float2 rml[NCH][HQ / NCH];   // (row max in log2 units, row sum) of each chunk
                                            // for this CTA's 16 heads
-  uint64_t mbar[7];               // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
-                                  // by the 8 data warps
+  alignas(16) float2 rml_out[NCH][HQ / NCH];   // this chunk's pairs for each owner's heads
+  uint64_t mbar[9];               // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
+                                  // by the 8 data warps, 7: Q landed, 8: the other chunks'
+                                  // blocks of this CTA's heads landed
   uint32_t tslot;
   int ok_flag;
 };
 constexpr int SMEM = SM_KV + SM_Q + (int)sizeof(Misc);   // no static shared memory
+static_assert(SMEM <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;                   // S, then P over its first 80 columns
 constexpr uint32_t MAX_POLL = 1u << 22;
 constexpr int BLK = HQ / NCH * DIM * 2;         // one chunk's block of 16 heads x 512 dims fp16
+constexpr int QBLK = BLK / 4;                   // its part of one O quarter (128 dims), 4 KB
+constexpr uint32_t RECV_BYTES = (NCH - 1) * (4 * QBLK + HQ / NCH * 8);   // from the 3 other chunks
 
 __device__ __forceinline__ uint32_t col_o(int q) { return q == 0 ? 256u : q == 1 ? 384u : q == 2 ? 128u : 256u; }
 
@@ -421,7 +428,8 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 }
 }  // namespace tca
 
-__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1) k_attn_tc(AttnParams p) {
+__global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1)
+    k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap) {
   pdl_wait();
   pdl_trigger();
   using namespace tca;
@@ -450,22 +458,38 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   const int kh = warp >> 2;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  if (warp == 0) tc::tmem_alloc(&ms.tslot, TMEM_COLS);
-  if (tid == 32) {
-#pragma unroll
-    for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
-    tc::mbar_init(&mbar[6], NW / 32);
-    ok_flag = 1;
-  }
-  // ---- Q first: 16 chunks of 16 bytes per thread, a warp reading 512 contiguous bytes --
+  // Q: CTA r of the cluster fetches heads [16 r, 16 r + 16) and multicasts them to all four,
+  // so every CTA's mbarrier 7 must be initialised before anyone's copy is issued: warp 8
+  // initialises, arrives on a cluster barrier and waits on it before issuing; the data warps
+  // arrive at once and wait for that phase only after issuing their gathers.  Warp 8 also
+  // allocates TMEM (and frees it at the end).
   const bool worker = tid < NW;
   if (worker) {
-  uint4 qv[SM_Q / 16 / NW];
-  {
-    const uint4* qs = reinterpret_cast<const uint4*>(p.q + (long long)b * HQ * DIM);
+    tc::cluster_arrive_relaxed();
+  } else {
+    tc::tmem_alloc(&ms.tslot, TMEM_COLS);
+    if (tid == ISSUER) {
 #pragma unroll
-    for (int i = 0; i < SM_Q / 16 / NW; ++i) qv[i] = __ldg(qs + tid + i * NW);
+      for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
+      tc::mbar_init(&mbar[6], NW / 32);
+      tc::mbar_init(&mbar[7], 1);
+      tc::mbar_init(&mbar[8], 1);
+      tc::mbar_arrive_expect_tx(&mbar[8], RECV_BYTES);
+      tc::fence_proxy_async_smem();             // the initialised barriers, seen by the TMA unit
+      ok_flag = 1;
+    }
+    __syncwarp();
+    tc::cluster_arrive_relaxed();               // after fence.mbarrier_init (in mbar_init)
+    tc::cluster_wait();
+    if (tid == ISSUER) {
+      const int r = (int)tc::cluster_ctarank();
+      tc::mbar_arrive_expect_tx(&mbar[7], SM_Q);
+#pragma unroll
+      for (int a = 0; a < DIM / 64; ++a)
+        tc::tma_load_2d_multicast(sQ + a * QATOM + r * 2048, &qmap, 64 * a, b * HQ + 16 * r, &mbar[7], 0xF);
+    }
   }
+  if (worker) {
   // ---- each thread resolves the keys it gathers: FP4 slot fkey (2 threads per key) and
   //      window row skey (8 threads per key), then issues those loads at once -------------
   const int fkey = tid >> 1, half = tid & 1;
@@ -509,13 +533,21 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   }
   if (half == 0) keyok[fkey] = fok;
   if (part == 0) keyok[skey] = sok;
-  // ---- Q -> fp16 into the swizzled tile while the gathers are in flight -----------------
+  // ---- Q -> fp16 in place while the gathers are in flight.  The start-up cluster phase
+  //      (complete long before this point) orders warp 8's barrier initialisation before
+  //      this wait.  Chunk idx = tid + i NW is 16-byte chunk idx % 64 of head idx / 64. ------
+  tc::cluster_wait();
+  if (tc::mbar_wait_warp(&mbar[7], 0, MAX_POLL)) {
 #pragma unroll
-  for (int i = 0; i < SM_Q / 16 / NW; ++i) {
-    const int idx = tid + i * NW, h = idx >> 6, ch = idx & 63;
-    *reinterpret_cast<uint4*>(sQ + tileoff(h, ch, QATOM)) =
-        make_uint4(bf16x2_to_f16x2(qv[i].x), bf16x2_to_f16x2(qv[i].y), bf16x2_to_f16x2(qv[i].z),
-                   bf16x2_to_f16x2(qv[i].w));
+    for (int i = 0; i < SM_Q / 16 / NW; ++i) {
+      const int idx = tid + i * NW, h = idx >> 6, ch = idx & 63;
+      uint4* qp = reinterpret_cast<uint4*>(sQ + tileoff(h, ch, QATOM));
+      const uint4 v = *qp;
+      *qp = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    }
+  } else {
+    raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+    ok_flag = 0;
   }
   // ---- dequantise the gathered rows into the K-major KV tile ----------------------------
   if (fok) {
@@ -570,7 +602,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   tc::fence_after_sync();
   const uint32_t tb = ms.tslot;
   // ---- MMA1: S = Q K^T -----------------------------------------------------------------
-  if (tid == ISSUER) {
+  if (tid == ISSUER && ok_flag) {
     constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
 #pragma unroll 4
     for (int ks = 0; ks < DIM / 16; ++ks) {
@@ -643,8 +675,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // ---- MMA2 quarters 0..2 back to back; the epilogue of quarter q writes o = O / l (fp16)
-  //      into the Q space, row h (1 KB) with 16-byte chunk c at c ^ (h % 8) ---------------
+  // ---- MMA2 quarters 0..2 back to back.  The epilogue of quarter q turns O / l into fp16 and
+  //      places each owner's 16 heads x 128 dims as a 4 KB block (head row hh: 256 bytes,
+  //      16-byte chunk cq at cq ^ hh): this CTA's own heads straight into its Q space (slot
+  //      `rank`, block q), another owner's into the KV atoms that quarter q has finished
+  //      reading, from where one thread sends it with a bulk copy into the owner's slot
+  //      `rank` (completing on the owner's mbarrier 8).  Bulk copies keep the data off the
+  //      load/store path the products share. ------------------------------------------------
   auto issue_quarter = [&](int q) {
     constexpr uint32_t id2 = tc::idesc_f16(64, 128, 0, 0, 1);
 #pragma unroll
@@ -670,56 +707,74 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
     __syncwarp();
     tc::cluster_wait();                         // (every CTA has finished MMA1)
-    tc::cluster_arrive();                       // this warp writes nothing to the cluster
   }
   if (worker) {
     const float lh = psum[0][head] + psum[1][head];
     const bool anyh = ok_flag && lh > 0.f;
     const float li = anyh ? 1.f / lh : 0.f;
     bool ok = ok_flag != 0;
-    // the heads of warp w belong to CTA w % 4 (heads [16 (w % 4), 16 (w % 4) + 16)); its
-    // 16-byte pieces of o go straight into that CTA's Q space, slot `rank`, row h % 16
-    const uint32_t dst_blk = tc::mapa(q_a + rank * BLK + (head & 15) * 1024, warp & 3);
+    const int owner = warp & 3, hh = head & 15;
+    const bool remote = owner != rank;
     tc::cluster_wait();                         // every CTA has finished MMA1: Q spaces free
     if (lv && kh == 0) {
-      const float mh = fmaxf(pmax[0][head], pmax[1][head]);
-      tc::st_dsmem_f2(tc::mapa(smem_u32(&ms.rml[rank][head & 15]), warp & 3),
-                      anyh ? make_float2(mh, lh) : make_float2(-INFINITY, 0.f));
+      const float2 v = anyh ? make_float2(fmaxf(pmax[0][head], pmax[1][head]), lh) : make_float2(-INFINITY, 0.f);
+      if (remote) ms.rml_out[owner][hh] = v;
+      else ms.rml[rank][hh] = v;
     }
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       if (ok) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&mbar[1 + q], 0, MAX_POLL));
+        ok = tc::mbar_wait_warp(&mbar[1 + q], 0, MAX_POLL);
         if (!ok && lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
       }
       tc::fence_after_sync();
+      uint8_t* blk = remote ? sKV + (2 * q) * ATOM + owner * QBLK : sQ + rank * BLK + q * QBLK;
+      uint32_t r[32];
       if (ok) {                                   // 16 heads x 64 columns per warp
-        uint32_t r[32];
         tc::tmem_ld16x2_32<32>(tb + lane_base + col_o(q) + 64 * kh, r);
         tc::tmem_ld_wait();
+      } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t pk[4];
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
-                                                 __uint_as_float(r[8 * i + 2 * t + 1]) * li);
-            pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          const int ch = 16 * q + 8 * kh + 4 * sub + i;
-          tc::st_dsmem_v4(dst_blk + ((ch ^ (head & 7)) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+      for (int i = 0; i < 4; ++i) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * i + 2 * t]) * li,
+                                               __uint_as_float(r[8 * i + 2 * t + 1]) * li);
+          pk[t] = *reinterpret_cast<const uint32_t*>(&hv);
         }
+        const int cq = 8 * kh + 4 * sub + i;
+        *reinterpret_cast<uint4*>(blk + hh * 256 + ((cq ^ hh) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       if (q == 0) {
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&mbar[6]);
       }
+      if (remote) {                               // warps owner and owner + 4 fill the block
+        tc::fence_proxy_async_smem();
+        asm volatile("bar.sync %0, 64;" :: "r"(1 + owner) : "memory");
+        if (kh == 0 && lane == 0) {
+          const uint32_t dmb = tc::mapa(smem_u32(&mbar[8]), owner);
+          tc::bulk_copy_to_cluster(tc::mapa(q_a + rank * BLK + q * QBLK, owner), blk, QBLK, dmb);
+          if (q == 0)
+            tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.rml[rank][0]), owner), &ms.rml_out[owner][0],
+                                     HQ / NCH * 8, dmb);
+        }
+      }
     }
     if (!ok && lane == 0) ok_flag = 0;
-    tc::cluster_arrive();                       // releases this thread's stores to the cluster
   }
-  tc::cluster_wait();                           // every chunk's block of this CTA's heads is here
+  // the other chunks' blocks of this CTA's heads have landed once mbarrier 8 completes; its
+  // own were written by its own warps before the barrier below.  Every CTA arrives on the
+  // cluster's last phase only after that, so when the phase completes every bulk copy out of
+  // every CTA's shared memory has finished and the CTAs may exit.
+  if (!tc::mbar_wait_warp(&mbar[8], 0, MAX_POLL) && lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+  tc::cluster_arrive_relaxed();
+  __syncthreads();
   // ---- merge: CTA r combines the 4 chunks of heads [16 r, 16 r + 16) from its Q space
   //      (slot c = chunk c) -------------------------------------------------------------
   {
@@ -745,14 +800,14 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       if (p.lse) p.lse[(long long)b * HQ + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
-    // item = (head, 16-byte chunk); a warp covers 32 consecutive chunks of one head row,
-    // which the c ^ (h % 8) placement spreads over every bank
+    // item = (head, 16-byte chunk); a warp covers 32 consecutive chunks of one head, two
+    // 256-byte rows of quarter blocks
 #pragma unroll
     for (int it = 0; it < 4 && worker; ++it) {
       const int idx = tid + it * NW;
       const int hh = idx >> 6, ch = idx & 63;
       const int h = 16 * rank + hh;
-      const int off = hh * 1024 + ((ch ^ (h & 7)) << 4);
+      const int off = (ch >> 4) * QBLK + hh * 256 + (((ch & 15) ^ hh) << 4);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
@@ -783,9 +838,10 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
     }
   }
+  tc::cluster_wait();                           // every CTA has all of its blocks
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, TMEM_COLS);
+  if (warp == NW / 32) tc::tmem_dealloc(tb, TMEM_COLS);
 }
 
 // Merge the chunk partials of (query b, head h).  Thread -> 4 dims.
@@ -877,7 +933,9 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     attr_set = true;
   }
   ap.nchunk = tca::NCH;
-  launch_k(k_attn_tc, dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st, ap);
+  CUtensorMap qmap;                             // q as [B * 64 heads][512] bf16, 16 heads x 64 dims boxes
+  if (!bf16_map(&qmap, a.q, (long long)a.B * tca::HQ, tca::DIM, tca::HQ / tca::NCH)) return cudaErrorInvalidValue;
+  launch_k(k_attn_tc, dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st, ap, qmap);
   return cudaGetLastError();
 }
 
@@ -923,7 +981,7 @@ cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   ap.lse = a.lse;
   const int mt = (a.Hq + 15) / 16;
   if (a.cache.d == 512 && a.Hq == 64 && a.k <= tca::NCH * tca::KT && a.swa_max <= tca::NCH * tca::KW &&
-      !attn_force_legacy())
+      tensor_map_encoder() != nullptr && !attn_force_legacy())
     return run_attn_tc(a, ap, st);
   if (a.cache.d == 512) {
     if (mt == 4) return run_attn<512, 4>(a, ap, st);

@@ -17,9 +17,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
-
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include "tmap.h"
 
 namespace csa2 {
 
@@ -35,13 +33,6 @@ constexpr int THREADS = 192;
 constexpr uint32_t MAX_POLL = 1u << 24;
 }  // namespace ptc
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
-      :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(map), "r"((uint32_t)__cvta_generic_to_shared(mbar)),
-         "r"(x), "r"(y)
-      : "memory");
-}
 
 // The pooling / RoPE / FP4 epilogue fused into the GEMM (m = 1 or 2): at m = 2 a tile holds
 // channels [128 x, 128 x + 128) of C (TMEM columns 0..127) and of Z (128..255), and the two
@@ -114,12 +105,12 @@ __global__ void __launch_bounds__(ptc::THREADS, 1)
           }
           uint8_t* st = smem + s * STAGE_BYTES;
           tc::mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-          tma_load_2d(st, &mh, kb * BK, m0, &full[s]);
+          tc::tma_load_2d(st, &mh, kb * BK, m0, &full[s]);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j) {
             const CUtensorMap* mj = pair ? (j < 2 ? &mkv : &mz) : mw;
             const int col = pair ? 128 * nt + 64 * (j & 1) : nw0 + 64 * j;
-            tma_load_2d(st + A_BYTES + j * 8192, mj, col, kb * BK, &full[s]);
+            tc::tma_load_2d(st + A_BYTES + j * 8192, mj, col, kb * BK, &full[s]);
           }
         }
         if (!ok) break;
@@ -431,32 +422,6 @@ cudaError_t launch_index_k_tc(const csa2_compress_args& a, int G, cudaStream_t s
 // ---------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  return encode;
-}
-
-// bf16 matrix [rows][cols] (row stride `cols` elements), boxes of box_rows x 64 columns,
-// 128-byte swizzle (the canonical operand layout of the MMA).
-static bool bf16_map(CUtensorMap* map, const void* base, long long rows, long long cols, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
-  const cuuint32_t estride[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The fused epilogue handles m = 1 (256-channel tiles) and m = 2 (128 channels of C and Z).
 bool project_tc_fused(const csa2_compress_args& a) {
   return project_tc_supported(a) && (a.m == 1 || a.m == 2) && a.cache.d % 256 == 0 && a.d_rope % 2 == 0;

@@ -240,6 +240,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* mbar, uint32_t b
                :: "r"((uint32_t)__cvta_generic_to_shared(mbar)), "r"(bytes) : "memory");
 }
 
+// 2-D tiled TMA load of the box at (x, y) of the tensor map into this CTA's shared memory,
+// completing on `mbar` (which counts the bytes).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(map), "r"((uint32_t)__cvta_generic_to_shared(mbar)),
+         "r"(x), "r"(y)
+      : "memory");
+}
+
 // 2-D tiled TMA load of the box at (x, y) into the same shared-memory offset of every CTA
 // in `mask` of the cluster, each CTA's mbarrier at `mbar`'s offset receiving the bytes.
 __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const void* tmap, int x, int y, uint64_t* mbar,
@@ -278,6 +288,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint3
     if (done) return true;
   }
   return false;
+}
+
+// The same wait for a whole warp, polled by lane 0 only (fewer threads spinning on the
+// barrier's shared-memory word); every lane must call it.  The warp barrier after the
+// broadcast orders lane 0's acquire before the other lanes' reads.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* mbar, uint32_t parity, uint32_t max_iter) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(mbar, parity, max_iter);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok;
 }
 
 }  // namespace tc
