@@ -74,6 +74,33 @@ def test_attn_parity(B, Hq, d, k, W):
     np.testing.assert_allclose(lse, rlse, rtol=1e-4, atol=1e-4)
 
 
+def _offset16(t):
+    """A copy of t whose data starts 16 bytes past a 256-byte boundary (16-byte aligned,
+    not 32-byte aligned)."""
+    n = t.numel() * t.element_size()
+    buf = torch.zeros(n + 256, dtype=torch.uint8, device=t.device)
+    v = buf[16:16 + n].view(t.dtype).view(t.shape)
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+def test_attn_16_byte_aligned_arrays():
+    # codes and window rows that are only 16-byte aligned take the 16-byte gather loads
+    r = np.random.default_rng(77)
+    c = _case(r, 5, 64, 512, 512, 128, n=3000)
+    ref, rlse = _oracle(c)
+    cache = c["cache"]
+    c["cache"] = csa2.PagedCache(_offset16(cache.codes), cache.scales, cache.idx_k, cache.page_table)
+    swa = _offset16(to_dev(c["swa"]))
+    out, lse = csa2.sparse_attn(c["cache"], bf16_dev(c["q"]), to_dev(c["seq_of"]), to_dev(c["topk"]),
+                                to_dev(c["tlen"]), swa, to_dev(c["swa_scale"]), to_dev(c["swa_start"]),
+                                to_dev(c["swa_len"]), c["W"], out_dtype=torch.float32)
+    assert csa2.device_error() == 0
+    _assert_close(out.cpu().numpy(), ref)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, rtol=1e-4, atol=1e-4)
+
+
 def test_attn_bf16_output_and_determinism():
     r = np.random.default_rng(50)
     c = _case(r, 4, 64, 512, 512, 128, n=5000)
