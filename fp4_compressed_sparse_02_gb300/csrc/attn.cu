@@ -51,7 +51,6 @@ struct AttnParams {
   void* out;
   int out_f32;
   float* lse;
-  int wide_loads;                 // cache.codes and swa are 32-byte aligned
 };
 
 // byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile of `rowbytes`
@@ -398,9 +397,9 @@ struct Misc {                                   // small per-CTA state, after th
   alignas(16) float2 rml[NCH][HQ / NCH];   // (row max in log2 units, row sum) of each chunk
                                            // for this CTA's 16 heads
   alignas(16) float2 rml_out[NCH][HQ / NCH];   // this chunk's pairs for each owner's heads
-  uint64_t mbar[9];               // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
+  uint64_t mbar[10];              // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
                                   // by the 8 data warps, 7: Q landed, 8: the other chunks'
-                                  // blocks of this CTA's heads landed
+                                  // blocks of this CTA's heads landed, 9: the raw rows landed
   uint32_t tslot;
   int ok_flag;
 };
@@ -410,6 +409,12 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0;                   // S, then P over its first 80 columns
 constexpr uint32_t MAX_POLL = 1u << 22;
 constexpr int BLK = HQ / NCH * DIM * 2;         // one chunk's block of 16 heads x 512 dims fp16
+// raw rows land by TMA in the tail of the KV tile (read into registers before any
+// dequantised row is written): FP4 codes [128][256 B], scales [128][32 B], window rows as
+// two 256-byte halves [2][32][256 B]
+constexpr int STG_CODES = 32768, STG_SCALES = 4096, STG_SWA = 16384;
+constexpr int STG = SM_KV - (STG_CODES + STG_SCALES + STG_SWA);
+static_assert(STG % 1024 == 0, "staging alignment");
 constexpr int QBLK = BLK / 4;                   // its part of one O quarter (128 dims), 4 KB
 constexpr uint32_t RECV_BYTES = (NCH - 1) * (4 * QBLK + HQ / NCH * 8);   // from the 3 other chunks
 
@@ -430,7 +435,8 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 }  // namespace tca
 
 __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1)
-    k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap) {
+    k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
+              const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap wmap) {
   pdl_wait();
   pdl_trigger();
   using namespace tca;
@@ -476,6 +482,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       tc::mbar_init(&mbar[7], 1);
       tc::mbar_init(&mbar[8], 1);
       tc::mbar_arrive_expect_tx(&mbar[8], RECV_BYTES);
+      tc::mbar_init(&mbar[9], 1);
+      tc::mbar_arrive_expect_tx(&mbar[9], STG_CODES + STG_SCALES + (p.swa_max > 0 ? STG_SWA : 0));
       tc::fence_proxy_async_smem();             // the initialised barriers, seen by the TMA unit
       ok_flag = 1;
     }
@@ -491,12 +499,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
   }
   if (worker) {
-  // ---- each thread resolves the keys it gathers: FP4 slot fkey (2 threads per key) and
-  //      window row skey (8 threads per key), then issues those loads at once -------------
+  // ---- each thread resolves the keys it dequantises: FP4 slot fkey (2 threads per key)
+  //      and window row skey (8 threads per key) -------------------------------------------
   const int fkey = tid >> 1, half = tid & 1;
   const int skey = KT + (tid >> 3), part = tid & 7;
   long long frow = -1, srow = -1;
   float ssc = 0.f;
+  int wrow0 = 0;                                // first window row of this chunk
   {
     const int j = chunk * KT + fkey;
     if (j < p.k) {
@@ -505,11 +514,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       const int sq = __ldg(p.seq_of + b);
       if (j < tl && e >= 0) frow = entry_row(p.cache, sq, e, &g_err_attn);
     }
-    const int w = chunk * KW + (tid >> 3);
-    if (w < p.swa_max) {
+    if (p.swa_max > 0) {
+      const int w = chunk * KW + (tid >> 3);
       const int wl = __ldg(p.swa_len + b);
-      const long long r = (long long)__ldg(p.swa_start + b) + w;
-      if (w < wl) {
+      const long long r0 = (long long)__ldg(p.swa_start + b) + chunk * KW;
+      wrow0 = (int)max(-(long long)KW, min(r0, (long long)p.swa_rows));   // TMA fills rows outside
+      const long long r = r0 + (tid >> 3);
+      if (w < p.swa_max && w < wl) {
         if (r >= 0 && r < p.swa_rows) {
           srow = r;
           ssc = __ldg(p.swa_scale + r);
@@ -520,35 +531,31 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     }
   }
   const bool fok = frow >= 0, sok = srow >= 0;
-  uint4 cw[8], sv = make_uint4(0, 0, 0, 0), wv[4];
-  // 32-byte loads where the arrays allow them (fewer requests in flight for the same bytes)
-  if (fok) {
-    const uint4* cp = reinterpret_cast<const uint4*>(p.cache.codes + frow * (DIM / 2) + half * 128);
-    sv = __ldg(reinterpret_cast<const uint4*>(p.cache.scales + frow * (DIM / 16) + half * 16));
-    if (p.wide_loads) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ldg_stream_v8(cp + 2 * i, cw[2 * i], cw[2 * i + 1]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) cw[i] = ldg_stream_v4(cp + i);
+  // ---- the raw rows come by TMA into the staging area, off the load/store path: per warp,
+  //      lanes 0, 8, 16, 24 gather the code and scale rows of 4 keys (held by lanes l, l+2,
+  //      l+4, l+6; a key without a row reads row 0, unused), thread 0 the chunk's 32
+  //      consecutive window rows (rows outside the array read as zero).  The start-up
+  //      cluster phase (complete by now) orders warp 8's initialisation of mbarrier 9 (and
+  //      7) before these copies and the waits below. ------------------------------------------
+  tc::cluster_wait();
+  {
+    const int rowc = fok ? (int)frow : 0, base = lane & ~7;
+    const int r0 = __shfl_sync(0xffffffffu, rowc, base), r1 = __shfl_sync(0xffffffffu, rowc, base + 2);
+    const int r2 = __shfl_sync(0xffffffffu, rowc, base + 4), r3 = __shfl_sync(0xffffffffu, rowc, base + 6);
+    if ((lane & 7) == 0) {
+      const int g = warp * 4 + (lane >> 3);
+      tc::tma_gather4(sKV + STG + g * 1024, &cmap, 0, r0, r1, r2, r3, &mbar[9]);
+      tc::tma_gather4(sKV + STG + STG_CODES + g * 128, &smap, 0, r0, r1, r2, r3, &mbar[9]);
     }
-  }
-  if (sok) {
-    const uint4* rp = reinterpret_cast<const uint4*>(p.swa + srow * DIM + part * 64);
-    if (p.wide_loads) {
-      ldg_stream_v8(rp, wv[0], wv[1]);
-      ldg_stream_v8(rp + 2, wv[2], wv[3]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) wv[i] = __ldg(rp + i);
+    if (tid == 0 && p.swa_max > 0) {
+      tc::tma_load_2d(sKV + STG + STG_CODES + STG_SCALES, &wmap, 0, wrow0, &mbar[9]);
+      tc::tma_load_2d(sKV + STG + STG_CODES + STG_SCALES + STG_SWA / 2, &wmap, 256, wrow0, &mbar[9]);
     }
   }
   if (half == 0) keyok[fkey] = fok;
   if (part == 0) keyok[skey] = sok;
-  // ---- Q -> fp16 in place while the gathers are in flight.  The start-up cluster phase
-  //      (complete long before this point) orders warp 8's barrier initialisation before
-  //      this wait.  Chunk idx = tid + i NW is 16-byte chunk idx % 64 of head idx / 64. ------
-  tc::cluster_wait();
+  // ---- Q -> fp16 in place while the rows are in flight.  Chunk idx = tid + i NW is
+  //      16-byte chunk idx % 64 of head idx / 64. -------------------------------------------
   if (tc::mbar_wait_warp(&mbar[7], 0, MAX_POLL)) {
 #pragma unroll
     for (int i = 0; i < SM_Q / 16 / NW; ++i) {
@@ -561,12 +568,34 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
     ok_flag = 0;
   }
-  // ---- dequantise the gathered rows into the K-major KV tile ----------------------------
+  // ---- raw rows into registers; step i of a thread reads 16-byte piece (i + rot) of its
+  //      part, which spreads a quarter warp over the banks.  Every thread has its bytes
+  //      before any dequantised row overwrites the staging area. --------------------------
+  uint4 cw[8], sv, wv[4];
+  const int rot_f = lane & 7, rot_s = part >> 1;
+  if (!tc::mbar_wait_warp(&mbar[9], 0, MAX_POLL)) {
+    if (lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+    ok_flag = 0;
+  }
+  {
+    const uint8_t* cs = sKV + STG + fkey * 256 + half * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cw[i] = *reinterpret_cast<const uint4*>(cs + 16 * ((i + rot_f) & 7));
+    sv = *reinterpret_cast<const uint4*>(sKV + STG + STG_CODES + fkey * 32 + half * 16);
+    const uint8_t* ws = sKV + STG + STG_CODES + STG_SCALES + (part >> 2) * (STG_SWA / 2) + (tid >> 3) * 256 +
+                        (part & 3) * 64;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const uint4*>(ws + 16 * ((i + rot_s) & 3));
+  }
+  asm volatile("bar.sync 5, %0;" :: "n"(NW) : "memory");
+  // ---- dequantise into the K-major KV tile --------------------------------------------------
   if (fok) {
     const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {               // 16 code bytes = 32 dims = scale groups 2i, 2i+1
-      const uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sw[i >> 1] >> (16 * (i & 1))));
+    for (int i = 0; i < 8; ++i) {               // 16 code bytes = 32 dims = scale groups 2c, 2c+1
+      const int c = (i + rot_f) & 7;
+      const uint32_t sc2 = c < 2 ? sw[0] : c < 4 ? sw[1] : c < 6 ? sw[2] : sw[3];
+      const uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sc2 >> (16 * (c & 1))));
       const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
       const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
       uint32_t o[16];
@@ -575,7 +604,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
         for (int bi = 0; bi < 4; ++bi)
           o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
-      const int ch0 = half * 32 + i * 4;
+      const int ch0 = half * 32 + c * 4;
 #pragma unroll
       for (int t = 0; t < 4; ++t)
         *reinterpret_cast<uint4*>(sKV + kvoff(fkey, ch0 + t)) = make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
@@ -588,6 +617,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     const float sc = ssc;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {               // 16 bytes = 16 dims = 2 chunks
+      const int c = (i + rot_s) & 3;
       const uint32_t words[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
       uint32_t o[8];
 #pragma unroll
@@ -599,7 +629,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
           __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
           o[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
         }
-      const int ch0 = part * 8 + i * 2;
+      const int ch0 = part * 8 + c * 2;
       *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
@@ -945,9 +975,20 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     attr_set = true;
   }
   ap.nchunk = tca::NCH;
-  CUtensorMap qmap;                             // q as [B * 64 heads][512] bf16, 16 heads x 64 dims boxes
-  if (!bf16_map(&qmap, a.q, (long long)a.B * tca::HQ, tca::DIM, tca::HQ / tca::NCH)) return cudaErrorInvalidValue;
-  launch_k(k_attn_tc, dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st, ap, qmap);
+  CUtensorMap qmap, cmap, smap, wmap;            // q as [B * 64 heads][512] bf16, 16 heads x 64 dims boxes;
+                                                // code / scale rows (one-row boxes, gathered 4 at a time);
+                                                // window rows (32 rows x 256 bytes)
+  const long long rows = (long long)a.cache.num_pages * 64;
+  if (!bf16_map(&qmap, a.q, (long long)a.B * tca::HQ, tca::DIM, tca::HQ / tca::NCH) ||
+      !u8_map(&cmap, a.cache.codes, rows, tca::DIM / 2, tca::DIM / 2, 1) ||
+      !u8_map(&smap, a.cache.scales, rows, tca::DIM / 16, tca::DIM / 16, 1))
+    return cudaErrorInvalidValue;
+  if (a.swa_max > 0) {
+    if (!u8_map(&wmap, a.swa, a.swa_rows, tca::DIM, 256, tca::KW)) return cudaErrorInvalidValue;
+  } else {
+    wmap = cmap;                                // not read
+  }
+  launch_k(k_attn_tc, dim3(tca::NCH, a.B), tca::THREADS, tca::SMEM, st, ap, qmap, cmap, smap, wmap);
   return cudaGetLastError();
 }
 
@@ -991,10 +1032,9 @@ cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   ap.out = a.out;
   ap.out_f32 = a.out_dtype == CSA2_F32;
   ap.lse = a.lse;
-  ap.wide_loads = ((uintptr_t)a.cache.codes & 31) == 0 && ((uintptr_t)a.swa & 31) == 0;
   const int mt = (a.Hq + 15) / 16;
   if (a.cache.d == 512 && a.Hq == 64 && a.k <= tca::NCH * tca::KT && a.swa_max <= tca::NCH * tca::KW &&
-      tensor_map_encoder() != nullptr && !attn_force_legacy())
+      (long long)a.cache.num_pages * 64 < (1ll << 31) && tensor_map_encoder() != nullptr && !attn_force_legacy())
     return run_attn_tc(a, ap, st);
   if (a.cache.d == 512) {
     if (mt == 4) return run_attn<512, 4>(a, ap, st);

@@ -250,6 +250,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// TMA gather of four rows r0..r3 (one-row boxes starting at column x) of a 2-D tensor map
+// into consecutive box-sized pieces of shared memory, completing on `mbar`.
+__device__ __forceinline__ void tma_gather4(void* dst, const void* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+      :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+         "r"((uint32_t)__cvta_generic_to_shared(mbar))
+      : "memory");
+}
+
 // 2-D tiled TMA load of the box at (x, y) into the same shared-memory offset of every CTA
 // in `mask` of the cluster, each CTA's mbarrier at `mbar`'s offset receiving the bytes.
 __device__ __forceinline__ void tma_load_2d_multicast(void* dst, const void* tmap, int x, int y, uint64_t* mbar,
