@@ -614,7 +614,11 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     for (int t = 0; t < 32; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(fkey, half * 32 + t)) = make_uint4(0, 0, 0, 0);
   }
   if (sok) {
-    const float sc = ssc;
+    // E4M3 (exact in fp16) times the row scale split as sc_hi + sc_lo (fp16 each): one
+    // multiply and one fused multiply-add in fp16, within 2^-11 of the exact product
+    const __half shi = __float2half_rn(ssc);
+    const __half slo = __float2half_rn(ssc - __half2float(shi));
+    const __half2 shi2 = __halves2half2(shi, shi), slo2 = __halves2half2(slo, slo);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {               // 16 bytes = 16 dims = 2 chunks
       const int c = (i + rot_s) & 3;
@@ -626,8 +630,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
         for (int hi = 0; hi < 2; ++hi) {
           const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
           const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-          __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
-          o[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
+          const __half2 r = __hfma2(hv, slo2, __hmul2(hv, shi2));
+          o[wi * 2 + hi] = *reinterpret_cast<const uint32_t*>(&r);
         }
       const int ch0 = part * 8 + c * 2;
       *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
