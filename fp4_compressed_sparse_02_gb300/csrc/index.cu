@@ -13,6 +13,7 @@
 // operands, so the k-slots of the fragment are mapped to the dims each thread loads
 // contiguously (32j + 8c + [0, 8) for lane c of a row quad).  The indexer Q of the query
 // is loaded with the same mapping once per warp.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -110,6 +111,7 @@ struct ScanParams {
   int relu;
   int* pool;              // [B][NB*P]
   float* pool_score;      // [B][NB*P]
+  int B;
 };
 
 template <int DK, int NHG>
@@ -117,9 +119,12 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int b = blockIdx.y;
-  const int j = blockIdx.x * 8 + warp;
-  if (j >= p.NB) return;
+  // persistent: warp w of CTA x takes pool blocks u = 8 x + w, + 8 gridDim.x, ... of all
+  // queries (u = b NB + j)
+  const long long total = (long long)p.B * p.NB;
+  for (long long u = (long long)blockIdx.x * 8 + warp; u < total; u += (long long)gridDim.x * 8) {
+  const int b = (int)(u / p.NB);
+  const int j = (int)(u % p.NB);
   int n = __ldg(p.n_vis + b);
   if (n < 0 || n > p.max_n) {
     if (lane == 0 && j == 0) raise_error(&g_err_index, CSA2_DEVERR_N_VIS);
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
     long long o = (long long)b * p.NB * P + off + rank;
     p.pool[o] = ti;
     p.pool_score[o] = tv;
+  }
   }
 }
 
@@ -547,8 +553,13 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sp.relu = a.relu;
   sp.pool = a.pool;
   sp.pool_score = static_cast<float*>(ws);
+  sp.B = a.B;
   const int nhg = (a.H_i + 7) / 8;
-  dim3 grid((a.num_blocks + 7) / 8, a.B);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long units = ((long long)a.B * a.num_blocks + 7) / 8;
+  dim3 grid((unsigned)std::min<long long>(units, 2LL * (sms > 0 ? sms : 1)));   // two resident CTAs per SM
   if (a.cache.d_ik == 128) launch_scan_dk<128>(sp, nhg, grid, st);
   else launch_scan_dk<64>(sp, nhg, grid, st);
   SelectParams sel{};
