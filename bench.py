@@ -1,6 +1,6 @@
 """CSA2 decode benchmark: query-layers/s of the 20-layer decoder step on one GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m|decode128k_hi32|decode128k_verify6|prefill_compress]
                [--impl gb300|reference]
 
 A step = one decode token for B independent sequences of N visible entries: the new
@@ -29,7 +29,10 @@ from fp4_compressed_sparse_02_gb300 import csa2, synth, workload  # noqa: E402
 from fp4_compressed_sparse_02_gb300.schedule import FULL, REINDEX, REUSE  # noqa: E402
 
 METRIC = "CSA2 decode query-layers/s at 128K–1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
-WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M, "prefill_compress": synth.PREFILL}
+WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M, "decode128k_hi32": synth.DEC128K_HI32,
+             "decode128k_verify6": synth.DEC128K_V6, "prefill_compress": synth.PREFILL}
+SYNTH_NAME = {"decode128k": "DEC128K", "decode1m": "DEC1M", "decode128k_hi32": "DEC128K_HI32",
+              "decode128k_verify6": "DEC128K_V6"}
 
 
 def peaks():
@@ -141,7 +144,7 @@ def run_reference(a):
     if rank != 0:
         return
     cfg = WORKLOADS[a.workload]
-    name = "DEC128K" if a.workload == "decode128k" else "DEC1M"
+    name = SYNTH_NAME[a.workload]
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
     sys.path.insert(0, ROOT)
     os.environ.update(env)
@@ -414,8 +417,10 @@ def main():
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"{a.workload}: 20-layer CSA2 decoder step, N={info['N']} visible entries, "
-                                   f"B={B} sequences per GPU, Top-{info['k']}, SWA {info['W']}, "
-                                   f"pool {info['NB']}x{info['P']}",
+                                   + (f"B={B} sequences per GPU" if info.get("G", 1) == 1 else
+                                      f"B={info['seqs']} sequences x {info['G']} verification positions = {B} "
+                                      f"queries per GPU (Full scan of a sequence shared by its {info['G']} queries)")
+                                   + f", Top-{info['k']}, SWA {info['W']}, pool {info['NB']}x{info['P']}",
                        "N": info["N"], "B": B, "layers": info["layers"], "d_kv": info["d"], "Hq": info["Hq"],
                        "indexer": f"{info['H_i']}x{info['d_ik']}", "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB algorithmic bytes per step"},
@@ -434,8 +439,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
         }
         if not a.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(info["N"], a.cpu_queries,
-                                                "DEC128K" if a.workload == "decode128k" else "DEC1M")
+            line["cpu_baseline"] = cpu_baseline(info["N"], a.cpu_queries, SYNTH_NAME[a.workload])
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -29,7 +29,7 @@ class IndexFullArgs(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_size_t), ("B", c_i32), ("H_i", c_i32), ("q_idx", c_vp),
                 ("w", c_vp), ("cache", Cache), ("seq_of", c_vp), ("n_vis", c_vp), ("max_n", c_i32),
                 ("num_blocks", c_i32), ("per_block", c_i32), ("k", c_i32), ("relu", c_i32),
-                ("pool", c_vp), ("pool_len", c_vp), ("topk", c_vp), ("topk_len", c_vp)]
+                ("pool", c_vp), ("pool_len", c_vp), ("topk", c_vp), ("topk_len", c_vp), ("group", c_i32)]
 
 
 class IndexReindexArgs(ctypes.Structure):

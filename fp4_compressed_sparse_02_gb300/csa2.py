@@ -159,9 +159,11 @@ def compress_quant(cache: PagedCache, seq, entry, *, m=1, C=None, Z=None, H=None
 
 
 def index_full(cache: PagedCache, q_idx, w, seq_of, n_vis, max_n, num_blocks=2048, per_block=8, k=512,
-               relu=True, out=None, ws=None):
+               relu=True, out=None, ws=None, group=1):
     """Full-mode indexer.  q_idx bf16 [B, H_i, d_ik], w float32 [B, H_i], seq_of / n_vis
-    int32 [B].  Returns (pool [B, NB*P], pool_len [B], topk [B, k], topk_len [B])."""
+    int32 [B].  group > 1: queries g*group .. g*group+group-1 share one sequence and scan it
+    together (each cache row read once; results as if scanned alone).  Returns (pool
+    [B, NB*P], pool_len [B], topk [B, k], topk_len [B])."""
     B, H_i, _ = q_idx.shape
     dev = q_idx.device
     if out is None:
@@ -180,6 +182,7 @@ def index_full(cache: PagedCache, q_idx, w, seq_of, n_vis, max_n, num_blocks=204
     a.seq_of, a.n_vis, a.max_n = _ptr(seq_of), _ptr(n_vis), int(max_n)
     a.num_blocks, a.per_block, a.k, a.relu = num_blocks, per_block, k, int(bool(relu))
     a.pool, a.pool_len, a.topk, a.topk_len = _ptr(pool), _ptr(pool_len), _ptr(topk), _ptr(topk_len)
+    a.group = int(group)
     _call("csa2_index_full", a, ws, dev)
     return out
 

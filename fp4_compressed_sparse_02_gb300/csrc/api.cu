@@ -111,6 +111,11 @@ csa2_status check_full(const csa2_index_full_args* a) {
   REQUIRE(a->max_n >= 0 && (long long)a->max_n <= (long long)a->cache.max_pages * CSA2_PAGE_SIZE,
           CSA2_ERR_INVALID_ARG, "max_n must be in [0, max_pages*64]");
   if (a->B > 0) REQUIRE(a->n_vis && a->pool && a->pool_len, CSA2_ERR_INVALID_ARG, "a required pointer is NULL");
+  REQUIRE(a->group >= 0 && a->group <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group must be in 0..8 (got %d)", a->group);
+  if (a->group > 1) {
+    REQUIRE(a->B % a->group == 0, CSA2_ERR_INVALID_ARG, "B (%d) must be a multiple of group (%d)", a->B, a->group);
+    REQUIRE(a->H_i <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group > 1 needs H_i <= 8 (got %d)", a->H_i);
+  }
   return CSA2_OK;
 }
 

@@ -114,6 +114,80 @@ struct ScanParams {
   int B;
 };
 
+// Offer the warp's 32 candidates (cv, ci: one per lane) to a block's best-P list (tv, ti in
+// lanes 0..P-1, best first; thv, thi: its P-th entry in every lane).
+__device__ __forceinline__ void topp_offer(float cv, int ci, int P, float& tv, int& ti, float& thv, int& thi) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(FULL_MASK, better(cv, ci, thv, thi));
+  if (m == 0) return;
+  if (__popc(m) <= 3 || P > 16) {
+    // few candidates (or a long list): insert them one by one
+    unsigned mm = m;
+    while (mm) {
+      const int src = __ffs(mm) - 1;
+      mm &= mm - 1;
+      const float xv = __shfl_sync(FULL_MASK, cv, src);
+      const int xi = __shfl_sync(FULL_MASK, ci, src);
+      const unsigned bm = __ballot_sync(FULL_MASK, lane < P && better(xv, xi, tv, ti));
+      if (bm) {
+        const int at = __ffs(bm) - 1;
+        const float upv = __shfl_up_sync(FULL_MASK, tv, 1);
+        const int upi = __shfl_up_sync(FULL_MASK, ti, 1);
+        if (lane > at && lane < P) { tv = upv; ti = upi; }
+        if (lane == at) { tv = xv; ti = xi; }
+      }
+    }
+  } else {
+    // many candidates: bitonic sort of the 32 (best first), then a bitonic merge of
+    // the best Pp of them with the list (Pp = P rounded up to a power of two <= 16)
+#pragma unroll
+    for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        const float ov = __shfl_xor_sync(FULL_MASK, cv, jj);
+        const int oi = __shfl_xor_sync(FULL_MASK, ci, jj);
+        const bool want_better = (((lane & jj) == 0) == ((lane & kk) == 0));
+        const bool ob = better(ov, oi, cv, ci);
+        if (want_better == ob) { cv = ov; ci = oi; }
+      }
+    }
+    int Pp = 1;
+    while (Pp < P) Pp <<= 1;
+    const float nv = __shfl_sync(FULL_MASK, cv, (2 * Pp - 1 - lane) & 31);
+    const int ni = __shfl_sync(FULL_MASK, ci, (2 * Pp - 1 - lane) & 31);
+    float mv = (lane < Pp) ? tv : nv;
+    int mi = (lane < Pp) ? ti : ni;
+    for (int jj = Pp; jj > 0; jj >>= 1) {
+      const float ov = __shfl_xor_sync(FULL_MASK, mv, jj);
+      const int oi = __shfl_xor_sync(FULL_MASK, mi, jj);
+      const bool want_better = (lane & jj) == 0;
+      const bool ob = better(ov, oi, mv, mi);
+      if (want_better == ob) { mv = ov; mi = oi; }
+    }
+    if (lane < P) { tv = mv; ti = mi; }
+  }
+  thv = __shfl_sync(FULL_MASK, tv, P - 1);
+  thi = __shfl_sync(FULL_MASK, ti, P - 1);
+}
+
+// Write a block's kept entries (the list of lanes 0..kept-1) to the pool, ascending by entry.
+__device__ __forceinline__ void topp_write(const ScanParams& p, int b, int j, int n, long long lo, long long hi,
+                                           float tv, int ti) {
+  const int lane = threadIdx.x & 31, P = p.P;
+  const int kept = (int)((hi - lo) < (long long)P ? (hi - lo) : (long long)P);
+  int rank = 0;
+  for (int l = 0; l < P; ++l) {
+    int oi = __shfl_sync(FULL_MASK, ti, l);
+    rank += (l < kept && oi < ti) ? 1 : 0;
+  }
+  const long long off = ((long long)n >= (long long)P * p.NB) ? (long long)P * j : lo;
+  if (lane < kept) {
+    long long o = (long long)b * p.NB * P + off + rank;
+    p.pool[o] = ti;
+    p.pool_score[o] = tv;
+  }
+}
+
 template <int DK, int NHG>
 __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   pdl_wait();
@@ -161,69 +235,84 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
     for (int t = 1; t < 4; ++t)
       if (c == t) { cv = sc[t]; ci = (int)r[t]; }
     if ((long long)ci >= hi) { cv = -INFINITY; ci = 0x7fffffff; }
-    const unsigned m = __ballot_sync(FULL_MASK, better(cv, ci, thv, thi));
-    if (m == 0) continue;
-    if (__popc(m) <= 3 || P > 16) {
-      // few candidates (or a long list): insert them one by one
-      unsigned mm = m;
-      while (mm) {
-        const int src = __ffs(mm) - 1;
-        mm &= mm - 1;
-        const float xv = __shfl_sync(FULL_MASK, cv, src);
-        const int xi = __shfl_sync(FULL_MASK, ci, src);
-        const unsigned bm = __ballot_sync(FULL_MASK, lane < P && better(xv, xi, tv, ti));
-        if (bm) {
-          const int at = __ffs(bm) - 1;
-          const float upv = __shfl_up_sync(FULL_MASK, tv, 1);
-          const int upi = __shfl_up_sync(FULL_MASK, ti, 1);
-          if (lane > at && lane < P) { tv = upv; ti = upi; }
-          if (lane == at) { tv = xv; ti = xi; }
-        }
-      }
-    } else {
-      // many candidates: bitonic sort of the 32 (best first), then a bitonic merge of
-      // the best Pp of them with the list (Pp = P rounded up to a power of two <= 16)
+    topp_offer(cv, ci, P, tv, ti, thv, thi);
+  }
+  topp_write(p, b, j, n, lo, hi, tv, ti);
+  }
+}
+
+// Full scan of G queries of one sequence at once (G consecutive queries sharing seq_of, e.g.
+// the positions of a speculative-decoding verification step): each indexer-K row is read
+// once and scored against every query (H_i <= 8).  Query q keeps its own blocks of its own
+// n_vis: the warp of block j reads rows [min_q lo_q, max_q hi_q) and offers each query only
+// its rows, so every query's pool and scores equal those of scanning it alone.
+template <int DK, int G>
+__global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const long long total = (long long)(p.B / G) * p.NB;
+  for (long long u = (long long)blockIdx.x * 8 + warp; u < total; u += (long long)gridDim.x * 8) {
+    const int grp = (int)(u / p.NB), j = (int)(u % p.NB);
+    const int b0 = grp * G;
+    const int s = __ldg(p.seq_of + b0);
+    int n[G], lo[G], hi[G];
+    int rlo = 0x7fffffff, rhi = 0;
 #pragma unroll
-      for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-          const float ov = __shfl_xor_sync(FULL_MASK, cv, jj);
-          const int oi = __shfl_xor_sync(FULL_MASK, ci, jj);
-          const bool want_better = (((lane & jj) == 0) == ((lane & kk) == 0));
-          const bool ob = better(ov, oi, cv, ci);
-          if (want_better == ob) { cv = ov; ci = oi; }
-        }
+    for (int q = 0; q < G; ++q) {
+      int nq = __ldg(p.n_vis + b0 + q);
+      if (nq < 0 || nq > p.max_n) {
+        if (lane == 0 && j == 0) raise_error(&g_err_index, CSA2_DEVERR_N_VIS);
+        nq = max(0, min(nq, p.max_n));
       }
-      int Pp = 1;
-      while (Pp < P) Pp <<= 1;
-      const float nv = __shfl_sync(FULL_MASK, cv, (2 * Pp - 1 - lane) & 31);
-      const int ni = __shfl_sync(FULL_MASK, ci, (2 * Pp - 1 - lane) & 31);
-      float mv = (lane < Pp) ? tv : nv;
-      int mi = (lane < Pp) ? ti : ni;
-      for (int jj = Pp; jj > 0; jj >>= 1) {
-        const float ov = __shfl_xor_sync(FULL_MASK, mv, jj);
-        const int oi = __shfl_xor_sync(FULL_MASK, mi, jj);
-        const bool want_better = (lane & jj) == 0;
-        const bool ob = better(ov, oi, mv, mi);
-        if (want_better == ob) { mv = ov; mi = oi; }
+      if (q > 0 && __ldg(p.seq_of + b0 + q) != s && lane == 0 && j == 0) raise_error(&g_err_index, CSA2_DEVERR_SEQ);
+      n[q] = nq;
+      lo[q] = (int)(((long long)j * nq) / p.NB);
+      hi[q] = (int)(((long long)(j + 1) * nq) / p.NB);
+      if (lo[q] < hi[q]) {
+        rlo = min(rlo, lo[q]);
+        rhi = max(rhi, hi[q]);
       }
-      if (lane < P) { tv = mv; ti = mi; }
     }
-    thv = __shfl_sync(FULL_MASK, tv, P - 1);
-    thi = __shfl_sync(FULL_MASK, ti, P - 1);
-  }
-  const int kept = (int)((hi - lo) < (long long)P ? (hi - lo) : (long long)P);
-  int rank = 0;
-  for (int l = 0; l < P; ++l) {
-    int oi = __shfl_sync(FULL_MASK, ti, l);
-    rank += (l < kept && oi < ti) ? 1 : 0;
-  }
-  const long long off = ((long long)n >= (long long)P * p.NB) ? (long long)P * j : lo;
-  if (lane < kept) {
-    long long o = (long long)b * p.NB * P + off + rank;
-    p.pool[o] = ti;
-    p.pool_score[o] = tv;
-  }
+    float tv[G], thv[G];
+    int ti[G], thi[G];
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
+      tv[q] = -INFINITY;
+      ti[q] = 0x7fffffff;
+      thv[q] = -INFINITY;
+      thi[q] = 0x7fffffff;
+    }
+    for (int base = rlo; base < rhi; base += 32) {
+      const int r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
+      uint4 A[4][DK / 32];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const long long row = (r[t] < rhi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
+        load_row<DK>(p.cache.idx_k, row, A[t]);
+      }
+      // lane (g, c) owns candidate row base + g + 8c (a permutation of the 32 rows)
+      int ci = r[0];
+#pragma unroll
+      for (int t = 1; t < 4; ++t)
+        if (c == t) ci = r[t];
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        QFrag<DK, 1> f;
+        load_qfrag<DK, 1>(p.q + (long long)(b0 + q) * p.H_i * DK, p.w + (long long)(b0 + q) * p.H_i, p.H_i, f);
+        float sc[4];
+        tile_scores<DK, 1>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, 1>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+        float cv = sc[0];
+#pragma unroll
+        for (int t = 1; t < 4; ++t)
+          if (c == t) cv = sc[t];
+        const bool mine = ci >= lo[q] && ci < hi[q];
+        topp_offer(mine ? cv : -INFINITY, mine ? ci : 0x7fffffff, p.P, tv[q], ti[q], thv[q], thi[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < G; ++q) topp_write(p, b0 + q, j, n[q], lo[q], hi[q], tv[q], ti[q]);
   }
 }
 
@@ -523,13 +612,38 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
 // ---------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------
+// persistent grid: as many CTAs as can be resident at once (the register use differs with
+// the variant), capped by the work
+template <typename K>
+static void launch_persistent(K kernel, const ScanParams& sp, long long units, cudaStream_t st) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  const dim3 grid((unsigned)std::min<long long>(units, (long long)per_sm * (sms > 0 ? sms : 1)));
+  launch_k(kernel, grid, 256, 0, st, sp);
+}
+
 template <int DK>
-static void launch_scan_dk(const ScanParams& sp, int nhg, dim3 grid, cudaStream_t st) {
+static void launch_scan_group(const ScanParams& sp, int group, long long units, cudaStream_t st) {
+  switch (group) {
+    case 2: launch_persistent(k_full_scan_g<DK, 2>, sp, units, st); break;
+    case 3: launch_persistent(k_full_scan_g<DK, 3>, sp, units, st); break;
+    case 4: launch_persistent(k_full_scan_g<DK, 4>, sp, units, st); break;
+    case 5: launch_persistent(k_full_scan_g<DK, 5>, sp, units, st); break;
+    case 6: launch_persistent(k_full_scan_g<DK, 6>, sp, units, st); break;
+    case 7: launch_persistent(k_full_scan_g<DK, 7>, sp, units, st); break;
+    default: launch_persistent(k_full_scan_g<DK, 8>, sp, units, st); break;
+  }
+}
+
+template <int DK>
+static void launch_scan_dk(const ScanParams& sp, int nhg, long long units, cudaStream_t st) {
   switch (nhg) {
-    case 1: launch_k(k_full_scan<DK, 1>, grid, 256, 0, st, sp); break;
-    case 2: launch_k(k_full_scan<DK, 2>, grid, 256, 0, st, sp); break;
-    case 3: launch_k(k_full_scan<DK, 3>, grid, 256, 0, st, sp); break;
-    default: launch_k(k_full_scan<DK, 4>, grid, 256, 0, st, sp); break;
+    case 1: launch_persistent(k_full_scan<DK, 1>, sp, units, st); break;
+    case 2: launch_persistent(k_full_scan<DK, 2>, sp, units, st); break;
+    case 3: launch_persistent(k_full_scan<DK, 3>, sp, units, st); break;
+    default: launch_persistent(k_full_scan<DK, 4>, sp, units, st); break;
   }
 }
 
@@ -555,13 +669,16 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sp.pool_score = static_cast<float*>(ws);
   sp.B = a.B;
   const int nhg = (a.H_i + 7) / 8;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long units = ((long long)a.B * a.num_blocks + 7) / 8;
-  dim3 grid((unsigned)std::min<long long>(units, 2LL * (sms > 0 ? sms : 1)));   // two resident CTAs per SM
-  if (a.cache.d_ik == 128) launch_scan_dk<128>(sp, nhg, grid, st);
-  else launch_scan_dk<64>(sp, nhg, grid, st);
+  const int group = a.group > 1 ? a.group : 1;
+  const long long units = ((long long)(a.B / group) * a.num_blocks + 7) / 8;   // CTAs of 8 blocks' work
+  if (group > 1) {
+    if (a.cache.d_ik == 128) launch_scan_group<128>(sp, group, units, st);
+    else launch_scan_group<64>(sp, group, units, st);
+  } else if (a.cache.d_ik == 128) {
+    launch_scan_dk<128>(sp, nhg, units, st);
+  } else {
+    launch_scan_dk<64>(sp, nhg, units, st);
+  }
   SelectParams sel{};
   sel.score = static_cast<const float*>(ws);
   sel.pool = a.pool;

@@ -30,8 +30,9 @@ class DecodeStep:
     """
 
     def __init__(self, cache, seq_of, n_vis, max_n, layers, num_blocks, per_block, k, swa_max,
-                 append=None, rope=None, out_dtype=torch.bfloat16):
+                 append=None, rope=None, out_dtype=torch.bfloat16, group=1):
         self.cache = cache
+        self.group = group                        # queries per sequence scanned together by Full
         self.seq_of = seq_of
         self.n_vis = n_vis
         self.max_n = max_n
@@ -69,7 +70,7 @@ class DecodeStep:
         if mode == FULL:
             csa2.index_full(self.cache, L["q_idx"], L["w"], self.seq_of, self.n_vis, self.max_n, self.NB,
                             self.P, self.k, out=(self.pool, self.pool_len, self.topk[i], self.topk_len[i]),
-                            ws=self.ws)
+                            ws=self.ws, group=self.group)
         elif mode == REINDEX:
             csa2.index_reindex(self.cache, L["q_idx"], L["w"], self.seq_of, self.pool, self.pool_len, self.k,
                                out=(self.topk[i], self.topk_len[i]), ws=self.ws)

@@ -95,6 +95,12 @@ TINY = dict(name="tiny_full_layer", N=4096, m=1, d=128, d_model=256, Hq=8, H_i=4
             NB=64, P=8, k=64, W=32, B=16, d_rope=32)
 DEC128K = dict(name="decoder_N131072_B32", N=131072, m=1, d=512, d_model=5120, Hq=64, H_i=8,
                d_ik=128, NB=2048, P=8, k=512, W=128, B=32, d_rope=64)
+# the pages' 32-head indexer (4x the scoring FLOPs of DEC128K for the same bytes)
+DEC128K_HI32 = dict(name="decoder_N131072_B32_Hi32", N=131072, m=1, d=512, d_model=5120, Hq=64, H_i=32,
+                    d_ik=128, NB=2048, P=8, k=512, W=128, B=32, d_rope=64)
+# a speculative-decoding verification step: 32 sequences x 6 consecutive positions
+DEC128K_V6 = dict(name="decoder_N131072_B32x6", N=131072, m=1, d=512, d_model=5120, Hq=64, H_i=8,
+                  d_ik=128, NB=2048, P=8, k=512, W=128, B=32, G=6, d_rope=64)
 DEC1M = dict(name="decoder_N1048576_B64", N=1048576, m=1, d=512, d_model=5120, Hq=64, H_i=8,
              d_ik=128, NB=2048, P=8, k=512, W=128, B=64, d_rope=64)
 PREFILL = dict(name="encoder_prefill_T65536", T=65536, m=2, d=512, d_model=5120, Hq=64, H_i=8,

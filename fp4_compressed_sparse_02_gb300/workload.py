@@ -24,9 +24,13 @@ def _fp8_rows(rows, d, g, device):
 
 
 def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedule=None, chunk_pages=32768,
-                 Ns=None):
+                 Ns=None, G=None):
     """A decode step of B independent sequences with N visible entries each (or Ns[b]
     entries for sequence b when Ns is given; N is then max(Ns)).
+
+    G > 1 (cfg["G"] by default): G consecutive queries per sequence, the positions of a
+    speculative-decoding verification step: query (b, t) sees Ns[b] - G + 1 + t entries,
+    appends its own entry, and the Full scan runs the G queries of a sequence together.
 
     The cache holds N (Ns[b]) entries per sequence (the last one is rewritten by the
     step's append when append=True).  Pages are a random permutation; page-table slots
@@ -39,6 +43,8 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
     B = B or cfg["B"]
     N = N or cfg["N"]
     Ns = Ns or [N] * B
+    G = G or cfg.get("G", 1)
+    Q = B * G                                    # queries
     d, d_ik, H_i, Hq, W, k = cfg["d"], cfg["d_ik"], cfg["H_i"], cfg["Hq"], cfg["W"], cfg["k"]
     NB, P, d_model, d_rope = cfg["NB"], cfg["P"], cfg["d_model"], cfg["d_rope"]
     g = torch.Generator(device=device)
@@ -67,34 +73,35 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
         cache.scales[p0:p1] = torch.randint(0x20, 0x40, (p1 - p0, 64, d // 16), generator=g, device=device,
                                             dtype=torch.uint8)
         cache.idx_k[p0:p1] = _randn_bf16((p1 - p0, 64, d_ik), g, device)
-    seq_of = torch.arange(B, dtype=torch.int32, device=device)
-    n_vis = torch.tensor(Ns, dtype=torch.int32, device=device)
+    seq_of = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(G)
+    nq = [n - G + 1 + t for n in Ns for t in range(G)]
+    n_vis = torch.tensor(nq, dtype=torch.int32, device=device)
     sched = schedule or decoder_schedule()
     layers = []
     for mode in sched:
-        L = dict(mode=mode, q=_randn_bf16((B, Hq, d), g, device),
-                 swa=_fp8_rows(B * W, d, g, device),
-                 swa_scale=(torch.rand(B * W, generator=g, device=device) * 0.015 + 0.005).float(),
-                 swa_start=torch.arange(B, dtype=torch.int32, device=device) * W,
-                 swa_len=torch.full((B,), W, dtype=torch.int32, device=device))
+        L = dict(mode=mode, q=_randn_bf16((Q, Hq, d), g, device),
+                 swa=_fp8_rows(Q * W, d, g, device),
+                 swa_scale=(torch.rand(Q * W, generator=g, device=device) * 0.015 + 0.005).float(),
+                 swa_start=torch.arange(Q, dtype=torch.int32, device=device) * W,
+                 swa_len=torch.full((Q,), W, dtype=torch.int32, device=device))
         if mode in (FULL, REINDEX):
-            L["q_idx"] = _randn_bf16((B, H_i, d_ik), g, device)
-            L["w"] = torch.randn((B, H_i), generator=g, device=device) / math.sqrt(H_i)
+            L["q_idx"] = _randn_bf16((Q, H_i, d_ik), g, device)
+            L["w"] = torch.randn((Q, H_i), generator=g, device=device) / math.sqrt(H_i)
         layers.append(L)
     app = None
     rope = None
     if append:
-        app = dict(H=_randn_bf16((B, d_model), g, device),
+        app = dict(H=_randn_bf16((Q, d_model), g, device),
                    W_kv=_randn_bf16((d_model, d), g, device, 1 / math.sqrt(d_model)),
                    W_ik=_randn_bf16((d, d_ik), g, device, 1 / math.sqrt(d)),
-                   pos=torch.tensor(Ns, dtype=torch.int32, device=device) - 1,
-                   seq=torch.arange(B, dtype=torch.int32, device=device),
-                   entry=torch.tensor(Ns, dtype=torch.int32, device=device) - 1)
+                   pos=n_vis - 1,
+                   seq=seq_of.clone(),
+                   entry=n_vis - 1)
         cos, sin = synth.rope_tables(N, d_rope)
         rope = (torch.from_numpy(cos).to(device), torch.from_numpy(sin).to(device))
-    step = DecodeStep(cache, seq_of, n_vis, N, layers, NB, P, k, W, append=app, rope=rope)
-    info = dict(B=B, N=N, Ns=Ns, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq, W=W, k=k,
-                NB=NB, P=P, d_model=d_model, d_rope=d_rope)
+    step = DecodeStep(cache, seq_of, n_vis, N, layers, NB, P, k, W, append=app, rope=rope, group=G)
+    info = dict(B=Q, G=G, seqs=B, N=N, Ns=Ns, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq,
+                W=W, k=k, NB=NB, P=P, d_model=d_model, d_rope=d_rope)
     return step, info
 
 
@@ -103,7 +110,8 @@ def algorithmic_bytes(info):
 
     append     : H row (d_model*2) + W_kv + W_ik once (shared by the batch) + the new
                  entry (d/2 + d/16 + 2*d_ik) per query
-    Full       : n*2*d_ik of indexer K + q_idx + w + pool (4*NB*P) + topk (4k) per query
+    Full       : n*2*d_ik of indexer K (once per group of G queries of a sequence) + q_idx
+                 + w + pool (4*NB*P) + topk (4k) per query
     Reindex    : pool*(2*d_ik) gathered indexer K + pool ids (4*NB*P) + q_idx + w + topk
     attention  : k*(d/2 + d/16) FP4 rows + W*(d + 4) SWA rows + q (2*Hq*d)
                  + out (2*Hq*d) + topk ids (4k) per query-layer
@@ -111,7 +119,7 @@ def algorithmic_bytes(info):
     B, N, d, d_ik, H_i, Hq, W, k = (info[x] for x in ("B", "N", "d", "d_ik", "H_i", "Hq", "W", "k"))
     pool = info["NB"] * info["P"]
     per_q = {}
-    per_q["full"] = N * 2 * d_ik + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
+    per_q["full"] = N * 2 * d_ik // info.get("G", 1) + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
     per_q["reindex"] = min(N, pool) * 2 * d_ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
     per_q["attn"] = k * (d // 2 + d // 16) + W * (d + 4) + 2 * Hq * d * 2 + 4 * k
     tot = 0

@@ -148,6 +148,12 @@ csa2_status csa2_compress_quant_workspace(const csa2_compress_args* args, size_t
  * topk_len [B].  Scores are float32 on the device.
  * Supported: H_i in 1..32, d_ik in {64, 128}, per_block in 1..32, NB*per_block <= 16384,
  * k in 1..2048, max_n <= max_pages*64.
+ *
+ * group (0 or 1: every query scans alone; 2..8): queries g*group .. g*group+group-1 belong
+ * to one sequence (equal seq_of; a mismatch sets CSA2_DEVERR_SEQ) and are scanned together,
+ * each indexer-K row read once for all of them -- e.g. the 1 + 5 positions of a
+ * speculative-decoding verification step.  n_vis may differ within a group.  Results are
+ * those of scanning every query alone.  Needs B % group == 0 and H_i <= 8.
  * -------------------------------------------------------------------------- */
 typedef struct csa2_index_full_args {
   size_t struct_size;
@@ -167,6 +173,7 @@ typedef struct csa2_index_full_args {
   int32_t* pool_len;           /* device [B] */
   int32_t* topk;               /* device [B][k] */
   int32_t* topk_len;           /* device [B] */
+  int32_t group;               /* queries scanned together (see above); 0 = 1 */
 } csa2_index_full_args;
 
 csa2_status csa2_index_full(const csa2_index_full_args* args, void* workspace,

@@ -89,6 +89,23 @@ def test_workspace_too_small_is_reported(L):
     assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 1
 
 
+def test_full_group_checks_on_host(L):
+    a = _lib.IndexFullArgs()
+    a.struct_size = ctypes.sizeof(a)
+    a.B, a.H_i, a.k = 6, 8, 512
+    a.cache = _cache(idx_k=FAKE, page_table=FAKE, max_pages=4)
+    a.q_idx = a.w = a.seq_of = a.n_vis = a.pool = a.pool_len = a.topk = a.topk_len = FAKE
+    a.max_n, a.num_blocks, a.per_block = 256, 2048, 8
+    a.group = 4                          # B = 6 is not a multiple of 4
+    assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 1
+    assert b"multiple of group" in L.csa2_last_error_message()
+    a.group = 9
+    assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 2
+    a.group, a.H_i = 3, 16               # grouped scans take H_i <= 8
+    assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 2
+    assert b"H_i" in L.csa2_last_error_message()
+
+
 def test_compress_rejects_partial_group_and_bad_m(L):
     a = _lib.CompressArgs()
     a.struct_size = ctypes.sizeof(a)

@@ -94,6 +94,33 @@ def test_full_head_counts(H_i):
     assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 4
 
 
+def _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, group):
+    pool, plen, topk, tlen = csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(n_vis),
+                                             int(n_vis.max()), NB, P, k, group=group)
+    assert csa2.device_error() == 0
+    return pool.cpu().numpy(), plen.cpu().numpy(), topk.cpu().numpy(), tlen.cpu().numpy()
+
+
+@pytest.mark.parametrize("d_ik,H_i,NB,group", [(128, 8, 2048, 6), (64, 4, 64, 2), (128, 3, 256, 8), (128, 8, 512, 5)])
+def test_full_grouped_queries(d_ik, H_i, NB, group):
+    # groups of consecutive queries of one sequence (a verification step: positions n-g+1
+    # .. n, one entry apart) scanned together: equal to the oracle per query and to the
+    # same queries scanned one by one, bit for bit
+    r = np.random.default_rng(40 + group + NB)
+    P, k = 8, min(512, NB * 8 // 4)
+    nseq = 3
+    ends = [20000, 16384 + group // 2, 70001] if NB == 2048 else [5000, 1500, 9001]
+    n_vis = np.array([e - group + 1 + t for e in ends for t in range(group)], dtype=np.int32)
+    seq_of = np.repeat(np.arange(nseq), group).astype(np.int32)
+    B = len(n_vis)
+    cache, K, q, w = _setup(r, nseq, int(n_vis.max()), d_ik, H_i, B)
+    got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, group)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 8
+    alone = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    for x, y in zip(got, alone):
+        np.testing.assert_array_equal(x, y)
+
+
 def test_exact_ties_break_to_lower_index():
     # a cache of only three distinct rows: scores tie exactly in large groups, so the
     # selection must follow the lower-index rule bit for bit.
