@@ -507,17 +507,18 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   float ssc = 0.f;
   int wrow0 = 0;                                // first window row of this chunk
   {
-    const int j = chunk * KT + fkey;
-    if (j < p.k) {
-      const int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
-      const int e = __ldg(p.topk + (long long)b * p.k + j);
-      const int sq = __ldg(p.seq_of + b);
-      if (j < tl && e >= 0) frow = entry_row(p.cache, sq, e, &g_err_attn);
-    }
+    // two rounds of loads: first every index that depends on nothing, then the page-table
+    // entry and the window row's scale together
+    const int j = chunk * KT + fkey, w = chunk * KW + (tid >> 3);
+    const int tl = p.topk_len ? __ldg(p.topk_len + b) : p.k;
+    const int e = (j < p.k) ? __ldg(p.topk + (long long)b * p.k + j) : -1;
+    const int sq = __ldg(p.seq_of + b);
+    const int wl = p.swa_max > 0 ? __ldg(p.swa_len + b) : 0;
+    const long long r0 = p.swa_max > 0 ? (long long)__ldg(p.swa_start + b) + chunk * KW : 0;
+    int page = -1;
+    bool fslot = false;
+    if (j < p.k && j < tl && e >= 0) page = entry_page_load(p.cache, sq, e, &g_err_attn, fslot);
     if (p.swa_max > 0) {
-      const int w = chunk * KW + (tid >> 3);
-      const int wl = __ldg(p.swa_len + b);
-      const long long r0 = (long long)__ldg(p.swa_start + b) + chunk * KW;
       wrow0 = (int)max(-(long long)KW, min(r0, (long long)p.swa_rows));   // TMA fills rows outside
       const long long r = r0 + (tid >> 3);
       if (w < p.swa_max && w < wl) {
@@ -529,6 +530,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
         }
       }
     }
+    if (fslot) frow = entry_row_of_page(p.cache, page, e, &g_err_attn);
   }
   const bool fok = frow >= 0, sok = srow >= 0;
   // ---- the raw rows come by TMA into the staging area, off the load/store path: per warp,

@@ -76,6 +76,23 @@ __device__ __forceinline__ long long entry_row(const csa2_cache& c, int s, long 
   return ((long long)page << kPageShift) | (e & (kPage - 1));
 }
 
+// entry_row in two halves, so that other loads can be issued between the page-table load and
+// the use of its value: the first checks the slot and issues the load (slot_ok false after a
+// reported error), the second checks the page id and forms the row.
+__device__ __forceinline__ int entry_page_load(const csa2_cache& c, int s, long long e, unsigned int* err,
+                                               bool& slot_ok) {
+  const long long p = e >> kPageShift;
+  slot_ok = false;
+  if (s < 0 || s >= c.num_seqs) { raise_error(err, CSA2_DEVERR_SEQ); return -1; }
+  if (e < 0 || p >= c.max_pages) { raise_error(err, CSA2_DEVERR_PAGE_SLOT); return -1; }
+  slot_ok = true;
+  return __ldg(c.page_table + (long long)s * c.max_pages + p);
+}
+__device__ __forceinline__ long long entry_row_of_page(const csa2_cache& c, int page, long long e, unsigned int* err) {
+  if (page < 0 || page >= c.num_pages) { raise_error(err, CSA2_DEVERR_PAGE_ID); return -1; }
+  return ((long long)page << kPageShift) | (e & (kPage - 1));
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }

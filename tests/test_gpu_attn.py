@@ -128,6 +128,20 @@ def test_attn_empty_and_one_sided():
     np.testing.assert_allclose(lse[1:], rlse[1:], rtol=1e-4, atol=1e-4)
 
 
+def test_attn_window_only_layer():
+    # an SWA-only layer (the encoder's first two layers): k = 0, no selection at all
+    r = np.random.default_rng(52)
+    c = _case(r, 6, 64, 512, 0, 128, n=500)
+    empty = torch.empty((6, 0), dtype=torch.int32, device="cuda")
+    out, lse = csa2.sparse_attn(c["cache"], bf16_dev(c["q"]), to_dev(c["seq_of"]), empty, None, to_dev(c["swa"]),
+                                to_dev(c["swa_scale"]), to_dev(c["swa_start"]), to_dev(c["swa_len"]), c["W"],
+                                out_dtype=torch.float32)
+    assert csa2.device_error() == 0
+    ref, rlse = _oracle(c)
+    _assert_close(out.cpu().numpy(), ref)
+    np.testing.assert_allclose(lse.cpu().numpy(), rlse, rtol=1e-4, atol=1e-4)
+
+
 def test_attn_without_topk_len_reads_all_slots():
     r = np.random.default_rng(52)
     c = _case(r, 3, 64, 512, 512, 128, n=4000, fill=0.5)
