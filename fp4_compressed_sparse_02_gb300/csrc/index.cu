@@ -209,8 +209,14 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   const long long hi = ((long long)(j + 1) * n) / p.NB;
   const int P = p.P;
 
-  QFrag<DK, NHG> f;
-  load_qfrag<DK, NHG>(p.q + (long long)b * p.H_i * DK, p.w + (long long)b * p.H_i, p.H_i, f);
+  // up to two head groups keep their Q fragments in registers; more are streamed from L1
+  // one group at a time (registers for two resident CTAs per SM)
+  constexpr bool STREAM_Q = NHG > 2;
+  constexpr int NHG_REG = STREAM_Q ? 1 : NHG;
+  const uint16_t* qb = p.q + (long long)b * p.H_i * DK;
+  const float* wb = p.w + (long long)b * p.H_i;
+  QFrag<DK, NHG_REG> f;
+  if (!STREAM_Q) load_qfrag<DK, NHG_REG>(qb, wb, p.H_i, f);
 
   float tv = -INFINITY;
   int ti = 0x7fffffff;
@@ -226,8 +232,23 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
       load_row<DK>(p.cache.idx_k, row, A[t]);
     }
     float sc[4];
-    tile_scores<DK, NHG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
-    tile_scores<DK, NHG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+    if (STREAM_Q) {
+      sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+#pragma unroll 1
+      for (int hg = 0; hg < NHG; ++hg) {
+        load_qfrag<DK, NHG_REG>(qb + hg * 8 * DK, wb + hg * 8, p.H_i - hg * 8, f);
+        float x0, x1, x2, x3;
+        tile_scores<DK, NHG_REG>(f, A[0], A[1], p.relu != 0, x0, x1);
+        tile_scores<DK, NHG_REG>(f, A[2], A[3], p.relu != 0, x2, x3);
+        sc[0] += x0;
+        sc[1] += x1;
+        sc[2] += x2;
+        sc[3] += x3;
+      }
+    } else {
+      tile_scores<DK, NHG_REG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+      tile_scores<DK, NHG_REG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+    }
     // lane (g, c) owns candidate row r[c] = base + g + 8c (a permutation of the 32 rows)
     float cv = sc[0];
     int ci = (int)r[0];
