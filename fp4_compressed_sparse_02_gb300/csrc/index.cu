@@ -477,8 +477,13 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     constexpr int NT = CL_SLICE / 32 / (CL_THREADS / 32);   // tiles per warp: 8
     const int g = lane >> 2, c = lane & 3;
     const int sq = __ldg(sp.seq_of + b);
-    QFrag<DK, NHG> f;
-    load_qfrag<DK, NHG>(sp.q + (long long)b * sp.H_i * DK, sp.w + (long long)b * sp.H_i, sp.H_i, f);
+    // as in the Full scan: more than two head groups stream their Q fragments from L1
+    constexpr bool STREAM_Q = NHG > 2;
+    constexpr int NHG_REG = STREAM_Q ? 1 : NHG;
+    const uint16_t* qb = sp.q + (long long)b * sp.H_i * DK;
+    const float* wb = sp.w + (long long)b * sp.H_i;
+    QFrag<DK, NHG_REG> f;
+    if (!STREAM_Q) load_qfrag<DK, NHG_REG>(qb, wb, sp.H_i, f);
     auto pos_of = [&](int it, int u) { return s0 + 32 * (warp + 8 * it) + g + 8 * u; };
     auto fetch_ent = [&](int it, int* e) {
 #pragma unroll
@@ -508,8 +513,23 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
       resolve(it + 1, en, rw);                            // next tile, while these rows load
       fetch_ent(it + 2, en);
       float sc[4];
-      tile_scores<DK, NHG>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
-      tile_scores<DK, NHG>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
+      if (STREAM_Q) {
+        sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+#pragma unroll 1
+        for (int hg = 0; hg < NHG; ++hg) {
+          load_qfrag<DK, NHG_REG>(qb + hg * 8 * DK, wb + hg * 8, sp.H_i - hg * 8, f);
+          float x0, x1, x2, x3;
+          tile_scores<DK, NHG_REG>(f, A[0], A[1], sp.relu != 0, x0, x1);
+          tile_scores<DK, NHG_REG>(f, A[2], A[3], sp.relu != 0, x2, x3);
+          sc[0] += x0;
+          sc[1] += x1;
+          sc[2] += x2;
+          sc[3] += x3;
+        }
+      } else {
+        tile_scores<DK, NHG_REG>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, NHG_REG>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
+      }
       if (c == 0) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
