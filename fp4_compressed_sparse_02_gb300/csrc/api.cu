@@ -111,10 +111,11 @@ csa2_status check_full(const csa2_index_full_args* a) {
   REQUIRE(a->max_n >= 0 && (long long)a->max_n <= (long long)a->cache.max_pages * CSA2_PAGE_SIZE,
           CSA2_ERR_INVALID_ARG, "max_n must be in [0, max_pages*64]");
   if (a->B > 0) REQUIRE(a->n_vis && a->pool && a->pool_len, CSA2_ERR_INVALID_ARG, "a required pointer is NULL");
-  REQUIRE(a->group >= 0 && a->group <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group must be in 0..8 (got %d)", a->group);
+  REQUIRE(a->group >= 0, CSA2_ERR_INVALID_ARG, "group must be >= 0 (got %d)", a->group);
   if (a->group > 1) {
     REQUIRE(a->B % a->group == 0, CSA2_ERR_INVALID_ARG, "B (%d) must be a multiple of group (%d)", a->B, a->group);
-    REQUIRE(a->H_i <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group > 1 needs H_i <= 8 (got %d)", a->H_i);
+    if (a->group <= 8)
+      REQUIRE(a->H_i <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group 2..8 needs H_i <= 8 (got %d)", a->H_i);
   }
   return CSA2_OK;
 }
@@ -206,7 +207,10 @@ csa2_status csa2_index_full_noalloc(const csa2_index_full_args* a, void* stream)
   size_t have = 0;
   cudaError_t e = csa2::index_noalloc_scratch(&scratch, &have);
   if (e != cudaSuccess) return cuda_status(e, "csa2_index_full_noalloc: scratch address lookup");
-  return cuda_status(csa2::launch_index_full(*a, scratch, static_cast<cudaStream_t>(stream)),
+  // the fixed scratch holds the pool scores only: a large group scans its queries one by one
+  csa2_index_full_args b = *a;
+  if (csa2::full_scores_tc_supported(b)) b.group = 1;
+  return cuda_status(csa2::launch_index_full(b, scratch, static_cast<cudaStream_t>(stream)),
                      "csa2_index_full_noalloc");
 }
 
@@ -249,7 +253,7 @@ csa2_status csa2_get_device_error(uint32_t* word) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_status(e, "csa2_get_device_error");
   *word = csa2::read_clear_error_compress() | csa2::read_clear_error_proj() | csa2::read_clear_error_index() |
-          csa2::read_clear_error_attn();
+          csa2::read_clear_error_score() | csa2::read_clear_error_attn();
   return cuda_status(cudaGetLastError(), "csa2_get_device_error");
 }
 

@@ -651,6 +651,135 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
 }
 
 // ---------------------------------------------------------------------------------
+// Top-k of one query's pool by one CTA, for many queries at once (a prefill chunk): the
+// same 4-pass radix select and tie rule as k_select_cl (so the same output), with block
+// barriers instead of the cluster's.  Full mode (scores written by the scan) only.
+// ---------------------------------------------------------------------------------
+constexpr int C1_THREADS = 512;
+constexpr int C1_PER_T = 16384 / C1_THREADS;          // 32 consecutive positions per thread
+constexpr int C1_ROW = C1_THREADS + 1;                // padded row of the key array
+constexpr size_t C1_SMEM = (size_t)C1_PER_T * C1_ROW * sizeof(uint32_t);
+
+// The keys live in shared memory (skey[i * C1_ROW + t] = key of position 32 t + i; the pad
+// word keeps both the coalesced fill and the per-thread reads free of bank conflicts), so
+// that two CTAs share an SM and one's loads overlap the other's passes.
+__global__ void __launch_bounds__(C1_THREADS, 2) k_select_cta(SelectParams p) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ uint32_t skey[];
+  __shared__ int hist[4][256];                      // one per radix pass, zeroed at entry
+  __shared__ int scan_sh[32];
+  __shared__ int pick[2];
+  const int tid = threadIdx.x;
+  const int b = blockIdx.x;
+  for (int i = tid; i < 4 * 256; i += C1_THREADS) (&hist[0][0])[i] = 0;
+  const int n = max(0, min(__ldg(p.n_vis + b), p.max_n));
+  const int P = min(n, p.stride);
+  const long long rowb = (long long)b * p.stride;
+  const int k = p.k;
+  int* out = p.topk + (long long)b * k;
+  if (p.pool_len_out && tid == 0) p.pool_len_out[b] = P;
+  if (p.pool_out)
+    for (int i = P + tid; i < p.stride; i += C1_THREADS) p.pool_out[rowb + i] = -1;
+  if (P <= k) {                                    // every candidate is selected
+    for (int i = tid; i < P; i += C1_THREADS) out[i] = p.pool[rowb + i];
+    for (int i = P + tid; i < k; i += C1_THREADS) out[i] = -1;
+    if (tid == 0) p.topk_len[b] = P;
+    return;
+  }
+  // coalesced fill, eight loads in flight per thread: position q = c * 512 + tid
+#pragma unroll 1
+  for (int c0 = 0; c0 < C1_PER_T; c0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = (c0 + u) * C1_THREADS + tid;
+      v[u] = q < P ? __ldg(p.score + rowb + q) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = (c0 + u) * C1_THREADS + tid;
+      skey[(q & 31) * C1_ROW + (q >> 5)] = q < P ? float_key(v[u]) : 0u;
+    }
+  }
+  __syncthreads();                                 // keys and zeroed histograms
+  const int q0 = tid * C1_PER_T;
+  const int nv = min(C1_PER_T, max(0, P - q0));   // this thread's valid positions
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    int* hb = hist[pass];
+    // the keys in the digit of this thread's first live key are counted once; the rest
+    // (rare in the leading digits) one by one
+    int b0 = -1, c0 = 0;
+#pragma unroll 8
+    for (int i = 0; i < nv; ++i) {
+      const uint32_t key = skey[i * C1_ROW + tid];
+      if ((key & mask) == prefix) {
+        const int bi = (int)((key >> shift) & 255u);
+        if (b0 < 0) b0 = bi;
+        if (bi == b0) ++c0;
+        else atomicAdd(&hb[bi], 1);
+      }
+    }
+    hist_add_warp(hb, max(b0, 0), c0);
+    __syncthreads();
+    if (tid < 32) {
+      int cnt[8], local = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { cnt[i] = hb[255 - 8 * tid - i]; local += cnt[i]; }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL_MASK, incl, o);
+        if (tid >= o) incl += y;
+      }
+      const int excl = incl - local;
+      if (excl < remaining && remaining <= incl) {
+        int cum = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + cnt[i] >= remaining) {
+            pick[0] = 255 - 8 * tid - i;
+            pick[1] = remaining - cum;
+            break;
+          }
+          cum += cnt[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= ((uint32_t)pick[0]) << shift;
+    mask |= 0xFFu << shift;
+    remaining = pick[1];
+  }
+  // output slots from one scan of (keys above the threshold, keys equal to it): ties at the
+  // threshold go to the lowest positions
+  int gt = 0, eq = 0;
+#pragma unroll 8
+  for (int i = 0; i < nv; ++i) {
+    const uint32_t key = skey[i * C1_ROW + tid];
+    gt += key > prefix ? 1 : 0;
+    eq += key == prefix ? 1 : 0;
+  }
+  int tot;
+  const int ex = block_exclusive_scan(gt | (eq << 16), scan_sh, tot);   // counts < 2^15
+  int er = ex >> 16;                                // equal keys before this thread
+  int o = (ex & 0xffff) + min(er, remaining);
+#pragma unroll 8
+  for (int i = 0; i < nv; ++i) {
+    const uint32_t key = skey[i * C1_ROW + tid];
+    if (key > prefix || (key == prefix && er++ < remaining)) {
+      if (o < k) out[o] = __ldg(p.pool + rowb + q0 + i);
+      ++o;
+    }
+  }
+  if (tid == 0) p.topk_len[b] = k;
+}
+
+// ---------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------
 // persistent grid: as many CTAs as can be resident at once (the register use differs with
@@ -689,7 +818,9 @@ static void launch_scan_dk(const ScanParams& sp, int nhg, long long units, cudaS
 }
 
 size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
-  return (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
+  // pool scores, then (tensor-core scoring of a large group) the score matrix
+  const size_t pool = (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
+  return pool + (full_scores_tc_supported(a) ? full_scores_tc_bytes(a) : 0);
 }
 
 cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st) {
@@ -712,7 +843,12 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   const int nhg = (a.H_i + 7) / 8;
   const int group = a.group > 1 ? a.group : 1;
   const long long units = ((long long)(a.B / group) * a.num_blocks + 7) / 8;   // CTAs of 8 blocks' work
-  if (group > 1) {
+  if (full_scores_tc_supported(a)) {              // many queries of one sequence: a dense product
+    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (size_t)a.B * a.num_blocks * a.per_block *
+                                                                        sizeof(float));
+    cudaError_t e = launch_full_scores_tc(a, S, static_cast<float*>(ws), st);
+    if (e != cudaSuccess) return e;
+  } else if (group > 1 && group <= 8) {
     if (a.cache.d_ik == 128) launch_scan_group<128>(sp, group, units, st);
     else launch_scan_group<64>(sp, group, units, st);
   } else if (a.cache.d_ik == 128) {
@@ -731,8 +867,18 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sel.k = a.k;
   sel.topk = a.topk;
   sel.topk_len = a.topk_len;
-  PoolScoreParams none{};
-  launch_k_late(k_select_cl<128, 1, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
+  if (a.B >= 256) {                                // many queries: a CTA each, no cluster barriers
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(k_select_cta, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C1_SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    launch_k(k_select_cta, a.B, C1_THREADS, C1_SMEM, st, sel);
+  } else {
+    PoolScoreParams none{};
+    launch_k_late(k_select_cl<128, 1, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
+  }
   return cudaGetLastError();
 }
 

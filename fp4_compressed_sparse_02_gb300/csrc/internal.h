@@ -22,6 +22,13 @@ uint32_t read_clear_error_proj();
 bool index_k_tc_supported(const csa2_compress_args& a, int G);
 cudaError_t launch_index_k_tc(const csa2_compress_args& a, int G, cudaStream_t st);
 
+// score_tc.cu: Full-indexer scores of many queries of one sequence on the tensor cores
+// (csa2_index_full with group >= 32), then each block's best entries into the pool
+bool full_scores_tc_supported(const csa2_index_full_args& a);
+size_t full_scores_tc_bytes(const csa2_index_full_args& a);
+cudaError_t launch_full_scores_tc(const csa2_index_full_args& a, float* S, float* pool_score, cudaStream_t st);
+uint32_t read_clear_error_score();
+
 // index.cu
 size_t index_full_workspace_bytes(const csa2_index_full_args& a);
 cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st);

@@ -99,9 +99,9 @@ def test_full_group_checks_on_host(L):
     a.group = 4                          # B = 6 is not a multiple of 4
     assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 1
     assert b"multiple of group" in L.csa2_last_error_message()
-    a.group = 9
-    assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 2
-    a.group, a.H_i = 3, 16               # grouped scans take H_i <= 8
+    a.group = -1
+    assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 1
+    a.group, a.H_i = 3, 16               # grouped scans of 2..8 queries take H_i <= 8
     assert L.csa2_index_full(ctypes.byref(a), FAKE, 1 << 30, None) == 2
     assert b"H_i" in L.csa2_last_error_message()
 

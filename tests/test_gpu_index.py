@@ -121,6 +121,50 @@ def test_full_grouped_queries(d_ik, H_i, NB, group):
         np.testing.assert_array_equal(x, y)
 
 
+@pytest.mark.parametrize("ends,NB", [((3000, 2200), 256), ((1500, 700), 256), ((9000, 5000), 2048)])
+def test_full_tensor_core_group(ends, NB):
+    # a large group of causal queries per sequence (a prefill chunk): the scores are one
+    # tensor-core product; pools and top-k against the oracle per query
+    r = np.random.default_rng(60 + ends[0] + NB)
+    P, k, d_ik, H_i, G = 8, 128, 128, 8, 64
+    n_vis = np.array([e - G + 1 + t for e in ends for t in range(G)], dtype=np.int32)
+    seq_of = np.repeat(np.arange(len(ends)), G).astype(np.int32)
+    cache, K, q, w = _setup(r, len(ends), int(n_vis.max()), d_ik, H_i, len(n_vis))
+    got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, G)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 16
+
+
+def test_full_many_queries_one_cta_each():
+    # 300 queries (the per-query selection runs one CTA per query from 256 queries on):
+    # equal to the oracle, and bit for bit to the same queries in batches below 256
+    r = np.random.default_rng(70)
+    NB, P, k, d_ik, H_i = 256, 8, 128, 128, 8
+    n_vis = r.integers(0, 6000, 300).astype(np.int32)
+    n_vis[:6] = [0, 1, 127, 128, 129, NB * P]
+    seq_of = (np.arange(300) % 3).astype(np.int32)
+    cache, K, q, w = _setup(r, 3, int(n_vis.max()), d_ik, H_i, 300)
+    got = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 16
+    for lo, hi in ((0, 150), (150, 300)):
+        part = csa2.index_full(cache, bf16_dev(q[lo:hi]), to_dev(w[lo:hi]), to_dev(seq_of[lo:hi]),
+                               to_dev(n_vis[lo:hi]), int(n_vis.max()), NB, P, k)
+        assert csa2.device_error() == 0
+        for x, y in zip(got, part):
+            np.testing.assert_array_equal(x[lo:hi], y.cpu().numpy())
+
+
+def test_full_tensor_core_group_many_queries():
+    # 2 x 256 causal queries: tensor-core scores and one CTA per query for the selection
+    r = np.random.default_rng(71)
+    P, k, d_ik, H_i, G, NB = 8, 256, 128, 8, 256, 512
+    ends = (6000, 4500)
+    n_vis = np.array([e - G + 1 + t for e in ends for t in range(G)], dtype=np.int32)
+    seq_of = np.repeat(np.arange(len(ends)), G).astype(np.int32)
+    cache, K, q, w = _setup(r, len(ends), int(n_vis.max()), d_ik, H_i, len(n_vis))
+    got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, G)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 32
+
+
 def test_exact_ties_break_to_lower_index():
     # a cache of only three distinct rows: scores tie exactly in large groups, so the
     # selection must follow the lower-index rule bit for bit.

@@ -96,8 +96,9 @@ def test_prefill_index_attention_full_size():
             L["q_idx"] = _randn_bf16((Q, H_i, d_ik), g)
             L["w"] = torch.randn((Q, H_i), generator=g, device="cuda") / math.sqrt(H_i)
         layers.append(L)
+    # the chunk's queries form one group: the Full scores are one tensor-core product
     step = DecodeStep(cache, torch.zeros(Q, dtype=torch.int32, device="cuda"), torch.from_numpy(n_vis).cuda(), NE,
-                      layers, NB, P, k, W)
+                      layers, NB, P, k, W, group=Q)
     step.run()
     torch.cuda.synchronize()
     assert csa2.device_error() == 0
