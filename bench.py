@@ -1,6 +1,6 @@
 """CSA2 decode benchmark: query-layers/s of the 20-layer decoder step on one GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m|decode128k_hi32|decode128k_verify6|prefill_compress]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m|decode128k_hi32|decode128k_verify6|prefill_compress|prefill|sweep]
                [--impl gb300|reference]
 
 A step = one decode token for B independent sequences of N visible entries: the new
@@ -30,7 +30,8 @@ from fp4_compressed_sparse_02_gb300.schedule import FULL, REINDEX, REUSE  # noqa
 
 METRIC = "CSA2 decode query-layers/s at 128K–1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
 WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M, "decode128k_hi32": synth.DEC128K_HI32,
-             "decode128k_verify6": synth.DEC128K_V6, "prefill_compress": synth.PREFILL}
+             "decode128k_verify6": synth.DEC128K_V6, "prefill_compress": synth.PREFILL, "prefill": synth.PREFILL,
+             "sweep": synth.DEC1M}
 SYNTH_NAME = {"decode128k": "DEC128K", "decode1m": "DEC1M", "decode128k_hi32": "DEC128K_HI32",
               "decode128k_verify6": "DEC128K_V6"}
 
@@ -143,6 +144,10 @@ def run_reference(a):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if a.workload not in SYNTH_NAME:
+        print(json.dumps({"impl": "reference", "unavailable": f"the oracle reference arm times decode query-steps; "
+                                                               f"{a.workload} has no oracle timing"}), flush=True)
+        return
     cfg = WORKLOADS[a.workload]
     name = SYNTH_NAME[a.workload]
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
@@ -233,16 +238,191 @@ def run_prefill_compress(a):
     print(json.dumps(line), flush=True)
 
 
+def bf16_peak_sustained():
+    """Dense bf16 tensor peak of this GPU held for seconds under the power cap, TFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        if "bf16_tflops_sustained" in j:
+            return j["bf16_tflops_sustained"], "measured"
+    return 1700.0, "fallback"
+
+
+def run_prefill(a):
+    """The whole encoder prefill chunk: 3 groups x [compress 65,536 tokens at m = 2, Full
+    index of the 8,192 causal query tokens, attention of 6 layers (Full + Reuse x 5)] =
+    18 query-layers per query token.  Tensor-bound; reported against the sustained bf16
+    peak, with the attention (the dominant kernel) timed live by events."""
+    libbuild.build()
+    cfg = synth.PREFILL
+    chunk, info = workload.build_prefill(cfg, seed=0, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        chunk.run()                                # sizes workspaces, sets kernel attributes
+    torch.cuda.synchronize()
+    assert csa2.device_error() == 0
+    st0 = chunk.steps[0]
+    nL = len(st0.layers)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(a.steps)]
+
+    def one(e=None):
+        for gi in range(len(chunk.groups)):
+            if gi == 0 and e is not None:
+                e[0].record(stream)
+                chunk.run_compress(0)
+                e[1].record(stream)
+                st0.run_index(0)
+                e[2].record(stream)
+                for i in range(nL):
+                    st0.run_attn(i)
+                e[3].record(stream)
+            else:
+                chunk.run_group(gi)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            one()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for j in range(a.steps):
+            one(evs[j])
+        t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert csa2.device_error() == 0
+    ms = t0.elapsed_time(t1) / a.steps
+    comp_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    idx_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / nL
+    Q, L = info["Q"], info["layers"]
+    fl = info["flops"]
+    chunk_flops = info["groups"] * (fl["compress"] + fl["index"]) + L * fl["attn"]
+    peak, peak_kind = bf16_peak_sustained()
+    attn_tf = fl["attn"] / (attn_ms / 1000.0) / 1e12
+    chunk_tf = chunk_flops / (ms / 1000.0) / 1e12
+    # end to end: the chunk's inputs (hidden states, Main Q, indexer Q and weights, window
+    # rows) copied from pinned host memory, the chunk, the last layer's output read back
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t) for t in chunk.inputs]
+    out_last = chunk.steps[-1].out[-1]
+    host_out = torch.empty(out_last.shape, dtype=out_last.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(2, a.steps // 4)
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        u0.record(stream)
+        for _ in range(e2e_steps):
+            for dev_t, host_t in zip(chunk.inputs, host_in):
+                dev_t.copy_(host_t, non_blocking=True)
+            one()
+            host_out.copy_(out_last, non_blocking=True)
+        u1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = u0.elapsed_time(u1) / e2e_steps
+    line = {"metric": "CSA2 encoder prefill chunk query-layers/s (8,192 causal queries x 18 layers)",
+            "value": Q * L / (ms / 1000.0), "unit": "query-layers/s", "n_gpus": 1, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"prefill: T={info['T']} tokens at m={info['m']} ({info['NE']} entries) per "
+                                   f"group, {info['groups']} groups x [compress, Full index, attention x "
+                                   f"{nL}] for Q={Q} causal query tokens, d_kv={info['d']}, Hq={info['Hq']}, "
+                                   f"indexer {info['H_i']}x{info['d_ik']}, Top-{info['k']}, SWA {info['W']}",
+                       "l2": "inputs larger than L2 (671 MB of H and 537 MB of Main Q per layer)"},
+            "roofline": {"bound": "tensor", "kernel": "k_attn_tc (csa2_sparse_attn, one layer of 8,192 queries; "
+                                                      "mean of the 6 layers of group 0)",
+                         "achieved": attn_tf, "peak": peak, "unit": "TFLOP/s", "frac": attn_tf / peak,
+                         "traffic": None, "peak_source": peak_kind + " (sustained)", "flop_per_launch": fl["attn"],
+                         "ms": attn_ms},
+            "chunk": {"flop": chunk_flops, "achieved_tflops": chunk_tf, "frac": chunk_tf / peak,
+                      "ms_compress": comp_ms, "ms_index_full": idx_ms, "ms_attn_layer": attn_ms},
+            "clocks": clk, "gpu_launches": a.steps * info["groups"] * (2 + 3 + nL),
+            "e2e": {"value": Q * L / (e2e_ms / 1000.0), "unit": "query-layers/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}}
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(a):
+    """The batched paged decode sweep: batch B in 1, 2, 4, ..., 256 sequences, each context
+    drawn uniformly from {4K, 64K, 256K, 1M} entries, one 20-layer decoder step (with the
+    append) per timed iteration.  Every iteration is timed alone by events after a write
+    of a buffer twice the L2 size, so small batches are not served from L2."""
+    import numpy as np
+    libbuild.build()
+    ctx = [4096, 65536, 262144, 1048576]
+    peak, peak_kind = peaks()
+    flush = torch.empty(2 * 129 * 2 ** 20 // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    rows = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    launches = 0
+    for B in (1, 2, 4, 8, 16, 32, 64, 128, 256):
+        r = np.random.default_rng(1000 + B)
+        Ns = r.choice(ctx, size=B)
+        step, info = workload.build_decode(synth.DEC1M, Ns=Ns, seed=2000 + B)
+        nbytes = workload.algorithmic_bytes(info)["total"]
+        with torch.cuda.stream(stream):
+            step.run()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            step.run()
+        with torch.cuda.stream(stream):
+            for _ in range(a.warmup):
+                gr.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1.0)
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        assert csa2.device_error() == 0
+        ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+        modes = info["schedule"]
+        launches += a.steps * (3 + 2 * list(modes).count(FULL) + list(modes).count(REINDEX) + len(modes))
+        gbs = nbytes / (ms / 1000.0) / 1e9
+        rows.append({"B": B, "contexts": {str(c): int((Ns == c).sum()) for c in ctx}, "ms_per_step": ms,
+                     "query_layers_per_s": B * info["layers"] / (ms / 1000.0), "algorithmic_bytes": nbytes,
+                     "achieved_gbs": gbs, "frac": gbs / peak})
+        del step, gr
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    last = rows[-1]
+    line = {"metric": METRIC, "value": last["query_layers_per_s"], "unit": "query-layers/s", "n_gpus": 1,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": last["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "sweep: batched paged 20-layer decode step, contexts drawn from {4K, 64K, 256K, 1M} "
+                                   "entries, batch 1..256 (value, ms_per_step: batch 256)",
+                       "l2": "a 258 MB buffer written before every timed step"},
+            "roofline": {"bound": "hbm", "kernel": "whole 20-layer step (all kernels), batch 256",
+                         "achieved": last["achieved_gbs"], "peak": peak, "unit": "GB/s", "frac": last["frac"],
+                         "traffic": None, "peak_source": peak_kind},
+            "sweep": rows, "clocks": clk, "gpu_launches": launches}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="decode128k", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-queries", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
+    a.steps_default = a.steps is None
+    if a.steps is None:
+        a.steps = 2000
     a.warmup = max(a.warmup, 3)
     if a.impl == "reference":
         run_reference(a)
@@ -250,6 +430,16 @@ def main():
 
     if a.workload == "prefill_compress":
         run_prefill_compress(a)
+        return
+    if a.workload == "sweep":
+        if a.steps_default:
+            a.steps = 20
+        run_sweep(a)
+        return
+    if a.workload == "prefill":
+        if a.steps_default:
+            a.steps = 10
+        run_prefill(a)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -105,6 +105,88 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
     return step, info
 
 
+class PrefillChunk:
+    """The encoder prefill chunk: T tokens of one sequence at compression ratio m, then
+    3 groups [Full, Reuse x 5] for the last Q tokens as causal queries.  Each group has its
+    own hidden states, compressor weights and Main KV cache (T / m entries): the group's
+    first layer compresses its chunk, its Full index step scores the causal range of every
+    query (the Q queries form one group: one tensor-core product), and its six layers
+    attend with their own Main Q over the group's Top-k and their own FP8 window (the
+    query's last W tokens)."""
+
+    def __init__(self, groups, steps, inputs):
+        self.groups = groups          # per group: dict(cache, H, W_kv, W_z, W_ik)
+        self.steps = steps            # per group: DecodeStep over the group's cache
+        self.inputs = inputs          # the device tensors a chunk reads from the host
+
+    def run_compress(self, gi):
+        G = self.groups[gi]
+        csa2.compress_quant(G["cache"], G["seq"], G["entry"], m=G["m"], H=G["H"], W_kv=G["W_kv"], W_z=G["W_z"],
+                            pos=G["pos"], rope_cos=G["cos"], rope_sin=G["sin"], W_ik=G["W_ik"], ws=G["ws"])
+
+    def run_group(self, gi):
+        self.run_compress(gi)
+        st = self.steps[gi]
+        for i in range(len(st.layers)):
+            st.run_layer(i)
+
+    def run(self):
+        for gi in range(len(self.groups)):
+            self.run_group(gi)
+
+
+def build_prefill(cfg, seed=0, device="cuda", n_groups=3, reuse=5):
+    """The encoder prefill chunk of cfg (T, m, Q, ...).  Inputs follow the recipes of the
+    module docstring; the query tokens are the last Q of the chunk, token t seeing the
+    (t + 1) // m entries complete at t.  Returns (PrefillChunk, info)."""
+    T, m, d, d_model, d_ik, d_rope = (cfg[x] for x in ("T", "m", "d", "d_model", "d_ik", "d_rope"))
+    Hq, H_i, Q, W, k, NB, P = (cfg[x] for x in ("Hq", "H_i", "Q", "W", "k", "NB", "P"))
+    NE = T // m
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    gc = torch.Generator()
+    gc.manual_seed(seed)
+    cos, sin = (torch.from_numpy(t).to(device) for t in synth.rope_tables(T, d_rope))
+    tq = torch.arange(T - Q, T, dtype=torch.int32, device=device)
+    n_vis = ((tq + 1) // m).to(torch.int32)
+    seq_q = torch.zeros(Q, dtype=torch.int32, device=device)
+    schedule = [FULL] + [REUSE] * reuse
+    # Main Q and the FP8 window rows of the group's layers (one set, shared by the groups:
+    # every tensor is larger than L2, so sharing changes no traffic)
+    lay = []
+    for mode in schedule:
+        lay.append(dict(mode=mode, q=_randn_bf16((Q, Hq, d), g, device), swa=_fp8_rows(T, d, g, device),
+                        swa_scale=(torch.rand(T, generator=g, device=device) * 0.015 + 0.005).float(),
+                        swa_start=(tq - (W - 1)).to(torch.int32),
+                        swa_len=torch.full((Q,), W, dtype=torch.int32, device=device)))
+    groups, steps = [], []
+    inputs = [L["q"] for L in lay] + [L["swa"] for L in lay]
+    for _ in range(n_groups):
+        pt = torch.randperm(NE // 64, generator=gc).to(torch.int32).reshape(1, -1)
+        cache = csa2.PagedCache.allocate(1, NE, d, d_ik, device, pt)
+        G = dict(cache=cache, m=m, H=_randn_bf16((T, d_model), g, device),
+                 W_kv=_randn_bf16((d_model, d), g, device, 1 / math.sqrt(d_model)),
+                 W_z=_randn_bf16((d_model, d), g, device, 1 / math.sqrt(d_model)),
+                 W_ik=_randn_bf16((d, d_ik), g, device, 1 / math.sqrt(d)),
+                 seq=torch.zeros(NE, dtype=torch.int32, device=device),
+                 entry=torch.arange(NE, dtype=torch.int32, device=device),
+                 pos=torch.arange(NE, dtype=torch.int32, device=device) * m + m - 1,
+                 cos=cos, sin=sin, ws=csa2.Workspace(device))
+        layers = [dict(L) for L in lay]
+        layers[0]["q_idx"] = _randn_bf16((Q, H_i, d_ik), g, device)
+        layers[0]["w"] = torch.randn((Q, H_i), generator=g, device=device) / math.sqrt(H_i)
+        steps.append(DecodeStep(cache, seq_q, n_vis, NE, layers, NB, P, k, W, group=Q))
+        groups.append(G)
+        inputs += [G["H"], layers[0]["q_idx"], layers[0]["w"]]
+    n_sum = int(n_vis.sum().item())
+    info = dict(T=T, m=m, NE=NE, Q=Q, groups=n_groups, layers=n_groups * len(schedule), d=d, d_model=d_model,
+                d_ik=d_ik, H_i=H_i, Hq=Hq, W=W, k=k, NB=NB, P=P, n_vis_sum=n_sum,
+                flops=dict(compress=2.0 * T * d_model * 2 * d + 2.0 * NE * d * d_ik,
+                           index=2.0 * H_i * d_ik * n_sum,
+                           attn=4.0 * Q * Hq * (k + W) * d))
+    return PrefillChunk(groups, steps, inputs), info
+
+
 def algorithmic_bytes(info):
     """Bytes a decode step must move at minimum (each byte read or written once):
 
@@ -118,17 +200,25 @@ def algorithmic_bytes(info):
     """
     B, N, d, d_ik, H_i, Hq, W, k = (info[x] for x in ("B", "N", "d", "d_ik", "H_i", "Hq", "W", "k"))
     pool = info["NB"] * info["P"]
-    per_q = {}
-    per_q["full"] = N * 2 * d_ik // info.get("G", 1) + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
-    per_q["reindex"] = min(N, pool) * 2 * d_ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
-    per_q["attn"] = k * (d // 2 + d // 16) + W * (d + 4) + 2 * Hq * d * 2 + 4 * k
+    G = info.get("G", 1)
+
+    def per_query(n):
+        q = {}
+        q["full"] = n * 2 * d_ik // G + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
+        q["reindex"] = min(n, pool) * 2 * d_ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
+        q["attn"] = k * (d // 2 + d // 16) + W * (d + 4) + 2 * Hq * d * 2 + 4 * k
+        return q
+
+    per_q = per_query(N)
     tot = 0
-    for mode in info["schedule"]:
-        if mode == FULL:
-            tot += B * per_q["full"]
-        elif mode == REINDEX:
-            tot += B * per_q["reindex"]
-        tot += B * per_q["attn"]
+    for n in info.get("Ns") or [N] * (B // G):      # each sequence at its own length
+        q = per_query(n)
+        for mode in info["schedule"]:
+            if mode == FULL:
+                tot += G * q["full"]
+            elif mode == REINDEX:
+                tot += G * q["reindex"]
+            tot += G * q["attn"]
     app = 0
     if info.get("append", True):
         app = B * (info["d_model"] * 2 + d // 2 + d // 16 + 2 * d_ik) + info["d_model"] * d * 2 + d * d_ik * 2
