@@ -397,7 +397,8 @@ struct Misc {                                   // small per-CTA state, after th
   alignas(16) float2 rml[NCH][HQ / NCH];   // (row max in log2 units, row sum) of each chunk
                                            // for this CTA's 16 heads
   alignas(16) float2 rml_out[NCH][HQ / NCH];   // this chunk's pairs for each owner's heads
-  uint64_t mbar[10];              // 0: MMA1, 1..4: MMA2 quarters, 6: quarter 0's columns read
+  uint64_t mbar[10];              // 0: MMA1, 1..4: MMA2 quarters, 5: dims 0..255 of every key
+                                  // written (by the 8 data warps), 6: quarter 0's columns read
                                   // by the 8 data warps, 7: Q landed, 8: the other chunks'
                                   // blocks of this CTA's heads landed, 9: the raw rows landed
   uint32_t tslot;
@@ -477,7 +478,8 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     tc::tmem_alloc(&ms.tslot, TMEM_COLS);
     if (tid == ISSUER) {
 #pragma unroll
-      for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
+      for (int i = 0; i < 5; ++i) tc::mbar_init(&mbar[i], 1);
+      tc::mbar_init(&mbar[5], NW / 32);
       tc::mbar_init(&mbar[6], NW / 32);
       tc::mbar_init(&mbar[7], 1);
       tc::mbar_init(&mbar[8], 1);
@@ -570,51 +572,35 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
     ok_flag = 0;
   }
-  // ---- raw rows into registers; step i of a thread reads 16-byte piece (i + rot) of its
-  //      part, which spreads a quarter warp over the banks.  Every thread has its bytes
-  //      before any dequantised row overwrites the staging area. --------------------------
-  uint4 cw[8], sv, wv[4];
-  const int rot_f = lane & 7, rot_s = part >> 1;
+  // ---- raw rows into registers.  Thread (fkey, half) dequantises, in phase ph, dims
+  //      [256 ph + 128 half, + 128) of its key: four 16-byte pieces of codes (32 dims each)
+  //      and 8 scale bytes.  Step i reads piece (i + key) mod 4, which spreads a quarter warp
+  //      over the banks.  Every thread has its bytes before any dequantised row overwrites
+  //      the staging area. ------------------------------------------------------------------
+  uint4 cw[8], wv[4];
+  uint2 sv[2];
+  const int rot_f = (lane >> 1) & 3, rot_s = part >> 1;
   if (!tc::mbar_wait_warp(&mbar[9], 0, MAX_POLL)) {
     if (lane == 0) raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
     ok_flag = 0;
   }
   {
-    const uint8_t* cs = sKV + STG + fkey * 256 + half * 128;
+    const uint8_t* cs = sKV + STG + fkey * 256 + half * 64;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cw[i] = *reinterpret_cast<const uint4*>(cs + 16 * ((i + rot_f) & 7));
-    sv = *reinterpret_cast<const uint4*>(sKV + STG + STG_CODES + fkey * 32 + half * 16);
+    for (int ph = 0; ph < 2; ++ph) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cw[4 * ph + i] = *reinterpret_cast<const uint4*>(cs + 128 * ph + 16 * ((i + rot_f) & 3));
+      sv[ph] = *reinterpret_cast<const uint2*>(sKV + STG + STG_CODES + fkey * 32 + 16 * ph + 8 * half);
+    }
     const uint8_t* ws = sKV + STG + STG_CODES + STG_SCALES + (part >> 2) * (STG_SWA / 2) + (tid >> 3) * 256 +
                         (part & 3) * 64;
 #pragma unroll
     for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const uint4*>(ws + 16 * ((i + rot_s) & 3));
   }
   asm volatile("bar.sync 5, %0;" :: "n"(NW) : "memory");
-  // ---- dequantise into the K-major KV tile --------------------------------------------------
-  if (fok) {
-    const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {               // 16 code bytes = 32 dims = scale groups 2c, 2c+1
-      const int c = (i + rot_f) & 7;
-      const uint32_t sc2 = c < 2 ? sw[0] : c < 4 ? sw[1] : c < 6 ? sw[2] : sw[3];
-      const uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sc2 >> (16 * (c & 1))));
-      const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
-      const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-      uint32_t o[16];
-#pragma unroll
-      for (int wi = 0; wi < 4; ++wi)
-#pragma unroll
-        for (int bi = 0; bi < 4; ++bi)
-          o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
-      const int ch0 = half * 32 + c * 4;
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-        *reinterpret_cast<uint4*>(sKV + kvoff(fkey, ch0 + t)) = make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < 32; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(fkey, half * 32 + t)) = make_uint4(0, 0, 0, 0);
-  }
+  // ---- dequantise into the K-major KV tile: the window rows (every dim), then the FP4 rows
+  //      in two phases of 256 dims.  Once every warp has written phase 0 (mbarrier 5), the
+  //      products over those dims start while phase 1 is written. ----------------------------
   if (sok) {
     // E4M3 (exact in fp16) times the row scale split as sc_hi + sc_lo (fp16 each): one
     // multiply and one fused multiply-add in fp16, within 2^-11 of the exact product
@@ -643,21 +629,66 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
     for (int t = 0; t < 8; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(skey, part * 8 + t)) = make_uint4(0, 0, 0, 0);
   }
+#pragma unroll
+  for (int ph = 0; ph < 2; ++ph) {
+    const uint32_t sw[2] = {sv[ph].x, sv[ph].y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {               // 16 code bytes = 32 dims = scale groups 2j, 2j+1
+      const int j = (i + rot_f) & 3;
+      const int ch0 = 32 * ph + 16 * half + 4 * j;
+      if (fok) {
+        const uint32_t sc2 = j < 2 ? sw[0] : sw[1];
+        const uint32_t sh = e4m3x2_to_f16x2((uint16_t)(sc2 >> (16 * (j & 1))));
+        const uint32_t s0 = (sh & 0xffffu) * 0x10001u, s1 = (sh >> 16) * 0x10001u;
+        const uint32_t words[4] = {cw[4 * ph + i].x, cw[4 * ph + i].y, cw[4 * ph + i].z, cw[4 * ph + i].w};
+        uint32_t o[16];
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi)
+#pragma unroll
+          for (int bi = 0; bi < 4; ++bi)
+            o[wi * 4 + bi] = hmul2_u32(e2m1x2_to_f16x2((words[wi] >> (8 * bi)) & 0xffu), wi < 2 ? s0 : s1);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          *reinterpret_cast<uint4*>(sKV + kvoff(fkey, ch0 + t)) = make_uint4(o[4 * t], o[4 * t + 1], o[4 * t + 2], o[4 * t + 3]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) *reinterpret_cast<uint4*>(sKV + kvoff(fkey, ch0 + t)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (ph == 0) {                              // dims 0..255 of every key (and Q) are written
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&mbar[5]);
+    }
+  }
   }  // worker
+  // ---- MMA1: S = Q K^T, the K steps over dims 0..255 once phase 0 is written, the rest
+  //      after the block barrier below ---------------------------------------------------
+  constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
+  auto issue_s = [&](uint32_t tmem_s, int ks0, int ks1) {
+#pragma unroll 4
+    for (int ks = ks0; ks < ks1; ++ks) {
+      const uint64_t ad = tc::smem_desc_sw128(q_a + (ks >> 2) * QATOM + (ks & 3) * 32, 16, 1024);
+      const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
+      tc::mma_f16_ss(tmem_s, ad, bd, id1, ks > 0);
+    }
+  };
+  if (tid == ISSUER) {
+    if (tc::mbar_wait(&mbar[5], 0, MAX_POLL)) {
+      tc::fence_after_sync();
+      if (ok_flag) issue_s(ms.tslot + COL_S, 0, DIM / 32);
+    } else {
+      raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
+      ok_flag = 0;
+    }
+  }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = ms.tslot;
-  // ---- MMA1: S = Q K^T -----------------------------------------------------------------
   if (tid == ISSUER && ok_flag) {
-    constexpr uint32_t id1 = tc::idesc_f16(64, NK, 0, 0, 0);
-#pragma unroll 4
-    for (int ks = 0; ks < DIM / 16; ++ks) {
-      const uint64_t ad = tc::smem_desc_sw128(q_a + (ks >> 2) * QATOM + (ks & 3) * 32, 16, 1024);
-      const uint64_t bd = tc::smem_desc_sw128(kv_a + (ks >> 2) * ATOM + (ks & 3) * 32, 16, 1024);
-      tc::mma_f16_ss(tb + COL_S, ad, bd, id1, ks > 0);
-    }
+    issue_s(tb + COL_S, DIM / 32, DIM / 16);
     tc::mma_commit(&mbar[0]);
     ok_flag = wait_mma(&mbar[0], 0) ? 1 : 0;
   }
