@@ -114,8 +114,6 @@ csa2_status check_full(const csa2_index_full_args* a) {
   REQUIRE(a->group >= 0, CSA2_ERR_INVALID_ARG, "group must be >= 0 (got %d)", a->group);
   if (a->group > 1) {
     REQUIRE(a->B % a->group == 0, CSA2_ERR_INVALID_ARG, "B (%d) must be a multiple of group (%d)", a->B, a->group);
-    if (a->group <= 8)
-      REQUIRE(a->H_i <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "group 2..8 needs H_i <= 8 (got %d)", a->H_i);
   }
   return CSA2_OK;
 }
@@ -207,10 +205,8 @@ csa2_status csa2_index_full_noalloc(const csa2_index_full_args* a, void* stream)
   size_t have = 0;
   cudaError_t e = csa2::index_noalloc_scratch(&scratch, &have);
   if (e != cudaSuccess) return cuda_status(e, "csa2_index_full_noalloc: scratch address lookup");
-  // the fixed scratch holds the pool scores only: a large group scans its queries one by one
-  csa2_index_full_args b = *a;
-  if (csa2::full_scores_tc_supported(b)) b.group = 1;
-  return cuda_status(csa2::launch_index_full(b, scratch, static_cast<cudaStream_t>(stream)),
+  // the fixed scratch holds the pool scores only: no tensor-core score matrix
+  return cuda_status(csa2::launch_index_full(*a, scratch, static_cast<cudaStream_t>(stream), false),
                      "csa2_index_full_noalloc");
 }
 

@@ -817,13 +817,28 @@ static void launch_scan_dk(const ScanParams& sp, int nhg, long long units, cudaS
   }
 }
 
-size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
-  // pool scores, then (tensor-core scoring of a large group) the score matrix
-  const size_t pool = (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
-  return pool + (full_scores_tc_supported(a) ? full_scores_tc_bytes(a) : 0);
+// The tensor-core scoring streams every row once per group of queries and scores it against
+// all of their heads; a single query with 8 heads keeps the scan, whose mma.sync scoring
+// already runs at the memory rate (and writes no score matrix).  CSA2_INDEX_FULL=scan or
+// =tc overrides the choice (for comparison measurements).
+bool full_scores_tc_chosen(const csa2_index_full_args& a) {
+  static int force = -2;
+  if (force == -2) {
+    const char* e = getenv("CSA2_INDEX_FULL");
+    force = (e && e[0] == 't') ? 1 : (e && e[0] == 's') ? 0 : -1;
+  }
+  if (force == 0 || !full_scores_tc_supported(a)) return false;
+  const int G = a.group > 1 ? a.group : 1;
+  return force == 1 || G * a.H_i >= 16;
 }
 
-cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st) {
+size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
+  // pool scores, then (tensor-core scoring) the score matrix
+  const size_t pool = (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
+  return pool + (full_scores_tc_chosen(a) ? full_scores_tc_bytes(a) : 0);
+}
+
+cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st, bool allow_tc) {
   if (a.B == 0) return cudaSuccess;
   const int stride = a.num_blocks * a.per_block;
   ScanParams sp{};
@@ -842,15 +857,17 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   sp.B = a.B;
   const int nhg = (a.H_i + 7) / 8;
   const int group = a.group > 1 ? a.group : 1;
-  const long long units = ((long long)(a.B / group) * a.num_blocks + 7) / 8;   // CTAs of 8 blocks' work
-  if (full_scores_tc_supported(a)) {              // many queries of one sequence: a dense product
+  // CTAs of 8 blocks' work: per group of queries (grouped scan) or per query
+  const long long units_g = ((long long)(a.B / group) * a.num_blocks + 7) / 8;
+  const long long units = ((long long)a.B * a.num_blocks + 7) / 8;
+  if (allow_tc && full_scores_tc_chosen(a)) {     // groups of queries of one sequence: a dense product
     float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (size_t)a.B * a.num_blocks * a.per_block *
                                                                         sizeof(float));
     cudaError_t e = launch_full_scores_tc(a, S, static_cast<float*>(ws), st);
     if (e != cudaSuccess) return e;
-  } else if (group > 1 && group <= 8) {
-    if (a.cache.d_ik == 128) launch_scan_group<128>(sp, group, units, st);
-    else launch_scan_group<64>(sp, group, units, st);
+  } else if (group > 1 && group <= 8 && a.H_i <= 8) {
+    if (a.cache.d_ik == 128) launch_scan_group<128>(sp, group, units_g, st);
+    else launch_scan_group<64>(sp, group, units_g, st);
   } else if (a.cache.d_ik == 128) {
     launch_scan_dk<128>(sp, nhg, units, st);
   } else {

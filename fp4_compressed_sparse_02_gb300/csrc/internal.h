@@ -31,7 +31,10 @@ uint32_t read_clear_error_score();
 
 // index.cu
 size_t index_full_workspace_bytes(const csa2_index_full_args& a);
-cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st);
+// allow_tc = false keeps the scan (the workspace then holds the pool scores only)
+cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st, bool allow_tc = true);
+// whether the Full call scores on the tensor cores (supported and chosen for this shape)
+bool full_scores_tc_chosen(const csa2_index_full_args& a);
 size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a);
 cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st);
 uint32_t read_clear_error_index();

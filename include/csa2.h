@@ -149,18 +149,21 @@ csa2_status csa2_compress_quant_workspace(const csa2_compress_args* args, size_t
  * Supported: H_i in 1..32, d_ik in {64, 128}, per_block in 1..32, NB*per_block <= 16384,
  * k in 1..2048, max_n <= max_pages*64.
  *
- * group (0 or 1: every query scans alone): queries g*group .. g*group+group-1 belong to one
+ * group (0 or 1: every query alone): queries g*group .. g*group+group-1 belong to one
  * sequence (equal seq_of; a mismatch sets CSA2_DEVERR_SEQ); n_vis may differ within a group;
- * needs B % group == 0.
- *   2..8: the queries are scanned together, each indexer-K row read once for all of them --
- *         e.g. the 1 + 5 positions of a speculative-decoding verification step (H_i <= 8).
- *         Results are those of scanning every query alone.
- *   >= 32, a multiple of 32, with H_i = 8, d_ik = 128, per_block <= 16 and max_n <= 64*NB --
- *         e.g. the causal queries of a prefill chunk: the scores are one tensor-core product
- *         of the group's indexer Q against the cache's indexer K (float32 accumulation in
- *         another order, so near-ties may resolve differently), written to the workspace
- *         (B * max_n floats more), then each block keeps its best.  Other large groups scan
- *         query by query; csa2_index_full_noalloc always does.
+ * needs B % group == 0.  Each indexer-K row is then read once for the whole group -- e.g. the
+ * 1 + 5 positions of a speculative-decoding verification step, or the causal queries of a
+ * prefill chunk.
+ * Tensor-core scoring: with H_i in {8, 16, 32}, d_ik = 128, per_block <= 16 and 16-byte
+ * aligned q_idx, w and idx_k, the scores are one tcgen05 product of a group's indexer Q
+ * (group x H_i columns, at most 256; a larger group must be a multiple of 256 / H_i)
+ * against the cache's indexer K, float32 accumulation, written to the workspace (B * max_n
+ * floats more), after which each block keeps its best.  It is taken whenever group x H_i >=
+ * 16 (so also by single queries with 16 or 32 heads); a single 8-head query keeps the
+ * scan.  The accumulation order differs from the scan's, so near-ties may resolve
+ * differently.  Otherwise groups of 2..8 queries with H_i <= 8 are scanned together (the
+ * results of scanning every query alone), and other groups query by query.
+ * csa2_index_full_noalloc never takes the tensor-core scoring.
  * -------------------------------------------------------------------------- */
 typedef struct csa2_index_full_args {
   size_t struct_size;

@@ -116,9 +116,33 @@ def test_full_grouped_queries(d_ik, H_i, NB, group):
     cache, K, q, w = _setup(r, nseq, int(n_vis.max()), d_ik, H_i, B)
     got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, group)
     assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 8
-    alone = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
-    for x, y in zip(got, alone):
-        np.testing.assert_array_equal(x, y)
+    if not _tensor_core_scored(d_ik, H_i, group):
+        # the grouped scan gives the results of scanning every query alone, bit for bit
+        alone = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+        for x, y in zip(got, alone):
+            np.testing.assert_array_equal(x, y)
+
+
+def _tensor_core_scored(d_ik, H_i, group):
+    return d_ik == 128 and H_i in (8, 16, 32) and max(group, 1) * H_i >= 16
+
+
+@pytest.mark.parametrize("H_i,G,NB,ends", [(32, 1, 2048, (20000, 131072 // 2 + 3, 5000)),
+                                           (16, 1, 256, (9001, 3000)),
+                                           (32, 6, 512, (40000, 7001)),
+                                           (8, 6, 2048, (150001, 20000))])
+def test_full_tensor_core_decode(H_i, G, NB, ends):
+    # single queries with 16 or 32 heads, and verification groups of 6: one tcgen05 product
+    # per group; blocks of more than 64 entries (long contexts) take the warp-per-block
+    # selection
+    r = np.random.default_rng(80 + H_i + G + NB)
+    P, k, d_ik = 8, 512, 128
+    n_vis = np.array([e - G + 1 + t for e in ends for t in range(G)], dtype=np.int32)
+    seq_of = np.repeat(np.arange(len(ends)), G).astype(np.int32)
+    cache, K, q, w = _setup(r, len(ends), int(n_vis.max()), d_ik, H_i, len(n_vis))
+    got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, G)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 4 * len(n_vis)
+    assert (got[1][n_vis >= NB * P] == NB * P).all()
 
 
 @pytest.mark.parametrize("ends,NB", [((3000, 2200), 256), ((1500, 700), 256), ((9000, 5000), 2048)])
