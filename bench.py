@@ -57,7 +57,8 @@ def bf16_peak():
 PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
             ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu"),
             ("k_select_cl_reindex", "decode128k"): ("k_select_cl_reindex_decode128k.md", "index.cu"),
-            ("k_proj_tc", "prefill_compress"): ("k_proj_tc_prefill_compress.md", "proj_tc.cu")}
+            ("k_proj_tc", "prefill_compress"): ("k_proj_tc_prefill_compress.md", "proj_tc.cu"),
+            ("k_score_tc", "decode128k_hi32"): ("k_score_tc_decode128k_hi32.md", "score_tc.cu")}
 
 
 def profiled_traffic(kernel, workload_name):
@@ -599,9 +600,13 @@ def main():
         full_bytes = B * nbytes["per_query"]["full"]
         full_gbs = full_bytes / (full_ms / 1000.0) / 1e9
         step_gbs = nbytes["total"] / (ms_step / 1000.0) / 1e9
-        # kernels per step: compressor append 3, Full indexer 2 (scan, select), Reindex 1,
-        # attention 1 per layer
-        launches = 3 + 2 * list(modes).count(FULL) + list(modes).count(REINDEX) + len(modes)
+        # the Full call scores on the tensor cores when a group's heads fill >= 16 columns
+        tc_full = info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and info["H_i"] * info.get("G", 1) >= 16
+        full_kernels = "k_score_tc + k_block_topp + k_select_cl" if tc_full else "k_full_scan + k_select_cl"
+        # kernels per step: compressor append 3, Full indexer 2 (scan, select) or 3 (score,
+        # block top-P, select), Reindex 1, attention 1 per layer
+        launches = (3 + (3 if tc_full else 2) * list(modes).count(FULL) + list(modes).count(REINDEX) +
+                    len(modes))
         line = {
             "metric": METRIC, "value": value, "unit": "query-layers/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -618,9 +623,10 @@ def main():
                          "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
                          "traffic": profiled_traffic("k_attn_tc", a.workload), "peak_source": peak_kind,
                          "algorithmic_bytes": attn_bytes, "ms": attn_ms},
-            "roofline_index_full": {"bound": "hbm", "kernel": "k_full_scan + k_select (csa2_index_full)",
+            "roofline_index_full": {"bound": "hbm", "kernel": full_kernels + " (csa2_index_full)",
                                     "achieved": full_gbs, "peak": peak, "unit": "GB/s", "frac": full_gbs / peak,
-                                    "traffic": profiled_traffic("k_full_scan", a.workload),
+                                    "traffic": profiled_traffic(full_kernels.split(" ")[0], a.workload),
+                                    "traffic_kernel": full_kernels.split(" ")[0],
                                     "algorithmic_bytes": full_bytes, "ms": full_ms},
             "step_hbm": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": step_gbs, "frac": step_gbs / peak},
             "clocks": clk,

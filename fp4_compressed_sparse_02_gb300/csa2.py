@@ -161,9 +161,10 @@ def compress_quant(cache: PagedCache, seq, entry, *, m=1, C=None, Z=None, H=None
 def index_full(cache: PagedCache, q_idx, w, seq_of, n_vis, max_n, num_blocks=2048, per_block=8, k=512,
                relu=True, out=None, ws=None, group=1):
     """Full-mode indexer.  q_idx bf16 [B, H_i, d_ik], w float32 [B, H_i], seq_of / n_vis
-    int32 [B].  group > 1: queries g*group .. g*group+group-1 share one sequence and scan it
-    together (each cache row read once; results as if scanned alone).  Returns (pool
-    [B, NB*P], pool_len [B], topk [B, k], topk_len [B])."""
+    int32 [B].  group > 1: queries g*group .. g*group+group-1 share one sequence, whose
+    indexer-K rows are read once for all of them (tensor-core scoring when group x H_i >= 16
+    and the shape allows it; see include/csa2.h).  Returns (pool [B, NB*P], pool_len [B],
+    topk [B, k], topk_len [B])."""
     B, H_i, _ = q_idx.shape
     dev = q_idx.device
     if out is None:

@@ -189,6 +189,26 @@ def test_full_tensor_core_group_many_queries():
     assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got) <= 32
 
 
+@pytest.mark.parametrize("relu", [True, False])
+def test_full_tensor_core_edges(relu):
+    # tensor-core scoring with ragged and degenerate groups: queries with no entry, one
+    # entry, fewer than a tile, a block each or fewer than per_block; groups whose queries
+    # end in different tiles; 16 heads, two queries a tile (N = 32)
+    r = np.random.default_rng(90 + relu)
+    NB, P, k, d_ik, H_i, G = 64, 8, 64, 128, 16, 2
+    n_vis = np.array([0, 1, 5, 127, 128, 129, 64, 511, 512, 513, 3000, 0], dtype=np.int32)
+    seq_of = np.repeat(np.arange(len(n_vis) // G), G).astype(np.int32)
+    cache, K, q, w = _setup(r, len(n_vis) // G, int(n_vis.max()), d_ik, H_i, len(n_vis))
+    got = _run_full_group(cache, q, w, seq_of, n_vis, NB, P, k, G)
+    if not relu:
+        got = csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(n_vis), int(n_vis.max()),
+                              NB, P, k, False, group=G)
+        assert csa2.device_error() == 0
+        got = tuple(t.cpu().numpy() for t in got)
+    assert _compare_full(K, q, w, seq_of, n_vis, NB, P, k, got, relu) <= 4
+    assert (got[1] == np.minimum(n_vis, NB * P)).all()
+
+
 def test_exact_ties_break_to_lower_index():
     # a cache of only three distinct rows: scores tie exactly in large groups, so the
     # selection must follow the lower-index rule bit for bit.
