@@ -36,7 +36,8 @@ constexpr int BN_MAX = 256;                // columns (queries x heads) at most
 constexpr int DK = 128;
 constexpr int A_BYTES = BM * DK * 2;       // 32 KB: two 64-dim halves of 16 KB
 constexpr int STAGES = 4;
-constexpr int SMEM_MAX = BN_MAX * DK * 2 + STAGES * A_BYTES + 256;
+constexpr int W_BYTES = 4 * BN_MAX * 4;      // each epilogue warp's copy of the unit's head weights
+constexpr int SMEM_MAX = BN_MAX * DK * 2 + STAGES * A_BYTES + 256 + W_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t MAX_POLL = 1u << 24;
 }  // namespace stc
@@ -223,11 +224,16 @@ __global__ void __launch_bounds__(stc::THREADS, 1)
   } else {                                           // ---- epilogue
     constexpr int QPC = 32 / HI;                     // queries per 32 columns
     const int q4 = warp & 3;                         // TMEM lane quarter
+    float* sW = reinterpret_cast<float*>(smem + B_BYTES + STAGES * A_BYTES + 256) + q4 * BN_MAX;
     int tl = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       int qt, t0, t1, seq;
       unit_span(p, u, qt, t0, t1, seq);
+      // the unit's head weights (QT x HI floats), once per unit
+      __syncwarp();
+      for (int i = lane; i < p.QT * HI; i += 32) sW[i] = __ldg(p.w + (long long)qt * p.QT * HI + i);
+      __syncwarp();
       for (int t = t0; t < t1; ++t, ++tl) {
         const int buf = tl & 1;
         ok = tc::mbar_wait_warp(&accf[buf], (uint32_t)((tl >> 1) & 1), MAX_POLL);
@@ -248,11 +254,11 @@ __global__ void __launch_bounds__(stc::THREADS, 1)
             const int qi = qc * QPC + k;
             if (qi >= p.QT) break;
             const int b = qt * p.QT + qi;
-            const float4* wp = reinterpret_cast<const float4*>(p.w + (long long)b * HI);
+            const float4* wp = reinterpret_cast<const float4*>(sW + qi * HI);
             float sc = 0.f;
 #pragma unroll
             for (int h4 = 0; h4 < HI / 4; ++h4) {
-              const float4 w4 = __ldg(wp + h4);
+              const float4 w4 = wp[h4];
               const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -513,7 +519,7 @@ cudaError_t launch_full_scores_tc(const csa2_index_full_args& a, float* S, float
   p.nchunks = (p.ntiles + p.chunk - 1) / p.chunk;
   p.units = (a.B / p.QT) * p.nchunks;
   p.S = S;
-  const int smem = p.BN * DK * 2 + STAGES * A_BYTES + 256;
+  const int smem = p.BN * DK * 2 + STAGES * A_BYTES + 256 + W_BYTES;
   CUtensorMap kmap, qmap;                            // idx_k rows (64-row boxes: one page), Q rows (BN)
   if (!bf16_map(&kmap, a.cache.idx_k, (long long)a.cache.num_pages * 64, DK, 64) ||
       !bf16_map(&qmap, a.q_idx, (long long)a.B * a.H_i, DK, p.BN))

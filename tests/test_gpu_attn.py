@@ -85,6 +85,35 @@ def _offset16(t):
     return v
 
 
+def test_attn_many_queries():
+    # many more queries than one wave of clusters: against the oracle, and bit for bit
+    # against the same queries in batches of one wave; some queries have no selected slot,
+    # no window row, or neither.
+    r = np.random.default_rng(4242)
+    B = 640
+    c = _case(r, B, 64, 512, 512, 128, n=3000)
+    c["tlen"][5] = 0
+    c["topk"][5] = -1
+    c["swa_len"][5] = 0
+    c["tlen"][6] = 0
+    c["topk"][6] = -1
+    c["swa_len"][7] = 0
+    c["swa_len"][8] = 77
+    got, lse = _run(c)
+    ref, rlse = _oracle(c)
+    _assert_close(got, ref)
+    fin = np.isfinite(rlse)
+    np.testing.assert_allclose(lse[fin], rlse[fin], rtol=1e-4, atol=1e-4)
+    assert (~np.isfinite(lse[~fin])).all() and (got[5] == 0).all()
+    for lo in range(0, B, 30):
+        hi = min(B, lo + 30)
+        part = {key: (v[lo:hi] if isinstance(v, np.ndarray) and v.ndim >= 1 and v.shape[0] == B else v)
+                for key, v in c.items()}
+        g2, l2 = _run(part)
+        np.testing.assert_array_equal(g2, got[lo:hi])
+        np.testing.assert_array_equal(l2, lse[lo:hi])
+
+
 def test_attn_16_byte_aligned_arrays():
     # codes and window rows that are only 16-byte aligned take the 16-byte gather loads
     r = np.random.default_rng(77)
