@@ -239,6 +239,21 @@ def run_prefill_compress(a):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's value of x (the slowest rank's time); x itself on one rank."""
+    if world <= 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.item()
+
+
+def whole_job_rate(units_per_rank, world, steps, ms_total):
+    """Units all ranks processed per second, over the slowest rank's time (weak scaling: every
+    rank processes its own batch)."""
+    return units_per_rank * world * steps / (ms_total / 1000.0)
+
+
 def bf16_peak_sustained():
     """Dense bf16 tensor peak of this GPU held for seconds under the power cap, TFLOP/s."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -518,14 +533,11 @@ def main():
     ms_total = t_start.elapsed_time(t_end)
     full_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 3.0
-    if world > 1:
-        t = torch.tensor([ms_total], device=f"cuda:{local}")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = t.item()
+    ms_total = max_over_ranks(ms_total, world, f"cuda:{local}")
     ms_step = ms_total / a.steps
     B = info["B"]
     ql = B * info["layers"] * world
-    value = ql * a.steps / (ms_total / 1000.0)
+    value = whole_job_rate(B * info["layers"], world, a.steps, ms_total)
 
     # end to end: per step, copy the step's inputs from pinned host memory, run the step,
     # read the last layer's output back.  The device inputs and outputs are double-buffered:
@@ -587,11 +599,8 @@ def main():
     e1.record(d2h_st)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=f"cuda:{local}")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = t.item()
-    e2e_val = ql / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e2e_ms, world, f"cuda:{local}")
+    e2e_val = whole_job_rate(B * info["layers"], world, 1, e2e_ms)
 
     if rank == 0:
         peak, peak_kind = peaks()
