@@ -477,13 +477,15 @@ def main():
         step.run()
     torch.cuda.synchronize()
     # The timed loop replays one graph that holds S consecutive steps (few launch gaps).
-    # Inside every captured step, external event-record nodes bracket the layer-0 Full
+    # In the first captured step, external event-record nodes bracket the layer-0 Full
     # indexer call (scan + select) and the three back-to-back Reuse-layer attention calls
-    # (layers 1..3), so the last replay of the timed region gives S samples of each.
+    # (layers 1..3); the last replay of the timed region gives one sample of each.  (An event
+    # node between two kernels turns their programmatic launch edge into a full one, so the
+    # other S - 1 steps carry none.)
     modes = info["schedule"]
     assert modes[0] == FULL and list(modes[1:4]) == [REUSE] * 3
     S = next(d for d in (10, 5, 4, 2, 1) if a.steps % d == 0)
-    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(S)]
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]]
 
     def one_step(e):
         step.run_append()
@@ -501,7 +503,10 @@ def main():
     g_multi = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_multi, stream=stream):
         for j in range(S):
-            one_step(evs[j])
+            if j == 0:
+                one_step(evs[0])
+            else:
+                step.run()
     g_one = torch.cuda.CUDAGraph()                 # one step, for the end-to-end loop
     with torch.cuda.graph(g_one, stream=stream):
         step.run()
