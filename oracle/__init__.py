@@ -23,7 +23,7 @@ Sources (cited by short name throughout):
                 "confirmed" list (selected entries + windowed KV into one attention).
 
 Every function states which passage it follows.  Readings taken where the sources
-are silent are marked READING and listed in the design doc.
+are silent are marked READING at the place they are taken.
 
 Parity status per function (pins live in tests/test_oracle_*.py):
   formats.*            pinned (exhaustive / library cross-checks / golden tables)
