@@ -404,7 +404,7 @@ def run_sweep(a):
         assert csa2.device_error() == 0
         ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
         modes = info["schedule"]
-        launches += a.steps * (3 + 2 * list(modes).count(FULL) + list(modes).count(REINDEX) + len(modes))
+        launches += a.steps * (2 + 2 * list(modes).count(FULL) + list(modes).count(REINDEX) + len(modes))
         gbs = nbytes / (ms / 1000.0) / 1e9
         rows.append({"B": B, "contexts": {str(c): int((Ns == c).sum()) for c in ctx}, "ms_per_step": ms,
                      "query_layers_per_s": B * info["layers"] / (ms / 1000.0), "algorithmic_bytes": nbytes,
@@ -617,9 +617,10 @@ def main():
         # the Full call scores on the tensor cores when a group's heads fill >= 16 columns
         tc_full = info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and info["H_i"] * info.get("G", 1) >= 16
         full_kernels = "k_score_tc + k_block_topp + k_select_cl" if tc_full else "k_full_scan + k_select_cl"
-        # kernels per step: compressor append 3, Full indexer 2 (scan, select) or 3 (score,
-        # block top-P, select), Reindex 1, attention 1 per layer
-        launches = (3 + (3 if tc_full else 2) * list(modes).count(FULL) + list(modes).count(REINDEX) +
+        # kernels per step: compressor append 2 (projection; quantisation + indexer K), Full
+        # indexer 2 (scan, select) or 3 (score, block top-P, select), Reindex 1, attention 1
+        # per layer
+        launches = (2 + (3 if tc_full else 2) * list(modes).count(FULL) + list(modes).count(REINDEX) +
                     len(modes))
         line = {
             "metric": METRIC, "value": value, "unit": "query-layers/s", "n_gpus": world, "steps": a.steps,

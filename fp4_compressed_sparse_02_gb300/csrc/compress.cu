@@ -275,14 +275,9 @@ __device__ __forceinline__ void load16_sum(const float* p, long long stride, int
   }
 }
 
-__global__ void __launch_bounds__(256) k_quant(QuantParams p) {
-  pdl_wait();
-  pdl_trigger();
-  const int gpr = p.d / 16;                           // 16-channel groups per entry
-  long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  long long g = gid / gpr;
-  const int q = (int)(gid % gpr);
-  if (g >= p.G) return;
+// Group q (16 channels) of entry g: pooled row, RoPE, FP4 codes and scale into the cache;
+// with deq, also the dequantised values (code x scale, float32) into deq[16 q ..].
+__device__ __forceinline__ void quant_group(const QuantParams& p, long long g, int q, float* deq) {
   const int c0 = q * 16;
   float y[16];
   if (p.m == 1) {
@@ -333,11 +328,33 @@ __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
   }
   uint32_t w0, w1, sbyte;
   fp4_group16(y, w0, w1, sbyte);
+  if (deq) {                                          // as the indexer-K projection reads it back
+    const float sc = e4m3_to_f32((uint8_t)sbyte);
+    const uint32_t wd[2] = {w0, w1};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t h2 = e2m1x2_to_f16x2((wd[i >> 2] >> (8 * (i & 3))) & 0xffu);
+      const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+      deq[c0 + 2 * i] = __low2float(hv) * sc;
+      deq[c0 + 2 * i + 1] = __high2float(hv) * sc;
+    }
+  }
   long long row = entry_row(p.cache, __ldg(p.seq + g), __ldg(p.entry + g), &g_err_compress);
   if (row < 0) return;
   uint2* cd = reinterpret_cast<uint2*>(p.cache.codes + row * (p.d / 2) + q * 8);
   *cd = make_uint2(w0, w1);
   p.cache.scales[row * (p.d / 16) + q] = (uint8_t)sbyte;
+}
+
+__global__ void __launch_bounds__(256) k_quant(QuantParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const int gpr = p.d / 16;                           // 16-channel groups per entry
+  long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  long long g = gid / gpr;
+  const int q = (int)(gid % gpr);
+  if (g >= p.G) return;
+  quant_group(p, g, q, nullptr);
 }
 
 // ---------------------------------------------------------------------------------
@@ -347,18 +364,21 @@ __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
 // partials are summed in warp order, so the result does not depend on scheduling.
 // ---------------------------------------------------------------------------------
 template <int E, int DIK>
+__device__ __forceinline__ void index_k_product(const csa2_cache& cache, const long long* rows, const float* deq,
+                                                float* part, const uint16_t* __restrict__ Wik);
+
+template <int E, int DIK>
 __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __restrict__ seq,
                                                  const int* __restrict__ entry, int G,
                                                  const uint16_t* __restrict__ Wik) {
   pdl_wait();
   pdl_trigger();
-  constexpr int CPL = DIK / 32;                  // columns per lane: 4 or 2
   extern __shared__ float ik_sm[];
   const int d = cache.d;
   float* deq = ik_sm;                            // [E][d]
   float* part = ik_sm + E * d;                   // [8][E][DIK]
   __shared__ long long rows[E];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int g0 = blockIdx.x * E;
   if (tid < E) {
     const int g = g0 + tid;
@@ -381,6 +401,17 @@ __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __
     deq[e * d + 2 * cb + 1] = v1;
   }
   __syncthreads();
+  index_k_product<E, DIK>(cache, rows, deq, part, Wik);
+}
+
+// idx_k of E entries from their dequantised rows deq[E][d] (shared memory), with `part`
+// [8][E][DIK] floats of shared scratch; 256 threads.
+template <int E, int DIK>
+__device__ __forceinline__ void index_k_product(const csa2_cache& cache, const long long* rows, const float* deq,
+                                                float* part, const uint16_t* __restrict__ Wik) {
+  constexpr int CPL = DIK / 32;
+  const int d = cache.d;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float acc[E][CPL];
 #pragma unroll
   for (int e = 0; e < E; ++e)
@@ -426,6 +457,30 @@ __global__ void __launch_bounds__(256) k_index_k(csa2_cache cache, const int* __
     const __nv_bfloat16 hb = __float2bfloat16_rn(sum);
     cache.idx_k[r * DIK + j] = *reinterpret_cast<const uint16_t*>(&hb);
   }
+}
+
+// The decode append's two steps in one launch, one CTA per entry: its 16-channel groups are
+// quantised (as k_quant) by the first d/16 threads, which also leave the dequantised row in
+// shared memory; then the indexer-K projection of that row (as k_index_k).
+template <int DIK>
+__global__ void __launch_bounds__(256) k_quant_index_k(QuantParams p, const uint16_t* __restrict__ Wik) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float qk_sm[];
+  float* deq = qk_sm;                            // [d]
+  float* part = qk_sm + p.d;                     // [8][DIK]
+  __shared__ long long rows[1];
+  const long long g = blockIdx.x;
+  if (threadIdx.x < p.d / 16) quant_group(p, g, threadIdx.x, deq);
+  if (threadIdx.x == 0) rows[0] = entry_row(p.cache, __ldg(p.seq + g), __ldg(p.entry + g), &g_err_compress);
+  __syncthreads();
+  index_k_product<1, DIK>(p.cache, rows, deq, part, Wik);
+}
+
+template <int DIK>
+static cudaError_t launch_quant_index_k(const QuantParams& qp, const uint16_t* Wik, cudaStream_t st) {
+  const size_t sm = ((size_t)qp.d + 8 * DIK) * sizeof(float);
+  return launch_k(k_quant_index_k<DIK>, (unsigned)qp.G, 256, sm, st, qp, Wik);
 }
 
 template <int E, int DIK>
@@ -565,6 +620,13 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   qp.cache = a.cache;
   qp.y_out = a.y_out;
   long long threads = (long long)G * (d / 16);
+  if (a.W_ik && G > 0 && G < 2048 && !index_k_tc_supported(a, G) && d / 16 <= 256) {
+    // a few entries (the decode append): quantisation and indexer K in one launch
+    cudaError_t e = a.cache.d_ik == 128 ? launch_quant_index_k<128>(qp, a.W_ik, st)
+                                        : launch_quant_index_k<64>(qp, a.W_ik, st);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   if (threads > 0) launch_k(k_quant, (unsigned)((threads + 255) / 256), 256, 0, st, qp);
   cudaError_t e = launch_index_k_any(a, G, st);
   if (e != cudaSuccess) return e;

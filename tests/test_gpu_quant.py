@@ -162,11 +162,12 @@ def test_compress_projection(h_dtype, m, T, d_model):
     _check_index_k(ikg[same], ref["idx_k"][same], ref["codes"][same], ref["scales"][same], Wik)
 
 
-@pytest.mark.parametrize("G", [777, 2100])
-def test_index_k_of_bit_exact_entries(G):
-    # G >= 2048 takes the 8-entries-per-CTA indexer-K kernel (ragged last CTA at 2100)
+@pytest.mark.parametrize("G,d,d_ik", [(1, 512, 128), (37, 512, 128), (200, 128, 64), (777, 512, 128),
+                                      (2100, 512, 128)])
+def test_index_k_of_bit_exact_entries(G, d, d_ik):
+    # a few entries (the decode append) quantise and project in one launch; 777 and 2100 take
+    # the tensor-core projection
     r = np.random.default_rng(400 + G)
-    d, d_ik = 512, 128
     C = r.standard_normal((G, d)).astype(np.float32)
     Wik = synth.bf16_normal(r, (d, d_ik), 1 / np.sqrt(d))
     seq, entry, pt = _layout(r, G, 2)
@@ -177,7 +178,7 @@ def test_index_k_of_bit_exact_entries(G):
     np.testing.assert_array_equal(codes, ref["codes"])
     ik = bf16_host_bits(cache.idx_k)[pt[seq, entry // 64], entry % 64]
     _check_index_k(ik, ref["idx_k"], ref["codes"], ref["scales"], Wik)
-    assert (ik == ref["idx_k"]).mean() > 0.99
+    assert (ik == ref["idx_k"]).mean() > (0.99 if G >= 100 else 0.95)
 
 
 def test_bad_page_id_sets_error_word_and_skips():
