@@ -523,13 +523,13 @@ static int pick_splits(int T, int d_model, int N) {
   return s;
 }
 
-// The indexer-K projection of the G new entries (when W_ik is given).
+// The indexer-K projection of the G new entries (when W_ik is given) after k_quant: the
+// tensor-core kernel, else 8 entries per CTA (fewer than 2,048 entries without the tensor-core
+// kernel take k_quant_index_k instead).
 static cudaError_t launch_index_k_any(const csa2_compress_args& a, int G, cudaStream_t st) {
   if (!a.W_ik || G <= 0) return cudaSuccess;
-  const bool many = G >= 2048;
   if (index_k_tc_supported(a, G)) return launch_index_k_tc(a, G, st);
-  if (a.cache.d_ik == 128) return many ? launch_index_k<8, 128>(a, G, st) : launch_index_k<1, 128>(a, G, st);
-  return many ? launch_index_k<8, 64>(a, G, st) : launch_index_k<1, 64>(a, G, st);
+  return a.cache.d_ik == 128 ? launch_index_k<8, 128>(a, G, st) : launch_index_k<8, 64>(a, G, st);
 }
 
 size_t compress_workspace_bytes(const csa2_compress_args& a) {
