@@ -54,13 +54,52 @@ def run_query(x, N, cfg):
                                 1 / np.sqrt(cfg["d"]))
 
 
+class LayerSteps:
+    """The decode schedule one query-layer at a time, over a small pool of queries: step i runs
+    layer i mod 20 of query (i div 20) mod len(pool) (the query's append with its layer 0),
+    carrying the layer state (pool, top-k) as the 20-layer step does.  Every 20 steps form
+    whole query-steps, so a run of any length times the same mix of layers."""
+
+    def __init__(self, xs, N, cfg):
+        self.xs, self.N, self.cfg = xs, N, cfg
+        self.i = 0
+        self.pool = self.topk = None
+
+    def step(self):
+        from oracle import attention, indexer
+        nl = len(schedule.decoder_schedule())
+        x = self.xs[(self.i // nl) % len(self.xs)]
+        li = self.i % nl
+        self.i += 1
+        cfg, N = self.cfg, self.N
+        if li == 0:
+            app = compress.compress_quant_from_hidden(x["H"], x["Wkv"], None, 1, np.array([N - 1]), x["cos"],
+                                                      x["sin"], cfg["d_rope"], x["Wik"])
+            x["codes"][N - 1] = app["codes"][0]
+            x["scales"][N - 1] = app["scales"][0]
+            x["K"][N - 1] = formats.bf16_value(app["idx_k"][0])
+        L = x["layers"][li]
+        if L["mode"] == schedule.FULL:
+            self.pool, self.topk, _ = indexer.full(L["q_idx"], L["w"], x["K"], cfg["NB"], cfg["P"], cfg["k"])
+        elif L["mode"] == schedule.REINDEX:
+            self.topk, _ = indexer.reindex(L["q_idx"], L["w"], x["K"], self.pool, cfg["k"])
+        else:
+            self.topk = indexer.reuse(self.topk)
+        return attention.sparse_attention(L["q"], x["codes"], x["scales"], self.topk, L["swa_rows"], L["swa_scale"],
+                                          L["swa_start"], L["swa_len"], 1 / np.sqrt(cfg["d"]))
+
+
 def time_sample(N, queries, cfg, seed=0):
+    """Each query is generated, timed through one query-step and dropped, so memory holds
+    one sequence at a time; only the query-steps are timed."""
     r = np.random.default_rng(seed)
-    xs = [make_query(r, N, cfg) for _ in range(queries)]
-    t0 = time.perf_counter()
-    for x in xs:
+    dt = 0.0
+    for _ in range(queries):
+        x = make_query(r, N, cfg)
+        t0 = time.perf_counter()
         run_query(x, N, cfg)
-    dt = time.perf_counter() - t0
+        dt += time.perf_counter() - t0
+        del x
     layers = len(schedule.decoder_schedule())
     return dict(seconds=dt, query_layers=queries * layers, value=queries * layers / dt)
 
