@@ -104,15 +104,39 @@ def time_sample(N, queries, cfg, seed=0):
     return dict(seconds=dt, query_layers=queries * layers, value=queries * layers / dt)
 
 
+def _worker(args):
+    """One process's share: its own seeded queries, each generated then timed alone."""
+    N, queries, cfg, seed = args
+    return time_sample(N, queries, cfg, seed)["seconds"]
+
+
+def time_sample_parallel(N, queries, cfg, procs, seed=0):
+    """The same sample spread over `procs` single-threaded processes (spawned, so no state is
+    inherited): each process times its own queries, and the rate counts every query-layer
+    over the slowest process's timed seconds."""
+    import multiprocessing as mp
+    per = [queries // procs + (1 if i < queries % procs else 0) for i in range(procs)]
+    jobs = [(N, n, cfg, seed * 1000 + i) for i, n in enumerate(per) if n > 0]
+    with mp.get_context("spawn").Pool(len(jobs)) as pool:
+        secs = pool.map(_worker, jobs)
+    layers = len(schedule.decoder_schedule())
+    dt = max(secs)
+    return dict(seconds=dt, query_layers=queries * layers, value=queries * layers / dt, procs=len(jobs))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--N", type=int, default=131072)
     ap.add_argument("--queries", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--config", default="DEC128K")
+    ap.add_argument("--procs", type=int, default=1, help="processes (one single-threaded oracle each)")
     a = ap.parse_args()
     cfg = dict(getattr(synth, a.config))
-    res = time_sample(a.N, a.queries, cfg, a.seed)
+    if a.procs > 1:
+        res = time_sample_parallel(a.N, a.queries, cfg, a.procs, a.seed)
+    else:
+        res = time_sample(a.N, a.queries, cfg, a.seed)
     print(json.dumps(res))
 
 
