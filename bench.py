@@ -1,7 +1,10 @@
 """CSA2 decode benchmark: query-layers/s of the 20-layer decoder step on one GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode128k|decode1m|decode128k_hi32|decode128k_verify6|prefill_compress|prefill|sweep]
-               [--impl gb300|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode1m|decode128k|decode128k_hi32|decode128k_verify6|prefill_compress|prefill|sweep]
+               [--impl gb300|reference] [--batch B]
+
+The default workload is decode1m (N = 1,048,576 visible entries, B = 64 sequences), the
+1M-context end of the metric's 128K-1M range; decode128k is the 128K end (B = 32).
 
 A step = one decode token for B independent sequences of N visible entries: the new
 token's entry is compressed into the cache (m = 1), then the decoder schedule
@@ -127,12 +130,42 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(N, queries, config_name):
+def host_cpu():
+    """Host cores this process may use, all online cores, and the CPU model name (lscpu)."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        usable = os.cpu_count() or 1
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return usable, os.cpu_count() or usable, model
+
+
+def mem_available():
+    try:
+        for ln in open("/proc/meminfo"):
+            if ln.startswith("MemAvailable:"):
+                return int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline(N, config_name):
     """The oracle on the host's cores, on a bounded sample of the workload: single-threaded,
-    and one single-threaded process per core (the reported value)."""
+    and one single-threaded process per usable core (the reported value).  The process count
+    is limited only by the cores this process may run on, the sample's queries and the host
+    memory one oracle sequence needs (about 2 KB per entry in float64)."""
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
 
-    def run(procs):
+    def run(procs, queries):
         r = subprocess.run([sys.executable, "-m", "oracle.timing", "--N", str(N), "--queries", str(queries),
                             "--config", config_name, "--procs", str(procs)], cwd=ROOT, env=env, capture_output=True,
                            text=True, timeout=900)
@@ -140,20 +173,30 @@ def cpu_baseline(N, queries, config_name):
             return None, (r.stderr.strip().splitlines()[-1] if r.stderr else "failed")
         return json.loads(r.stdout.strip().splitlines()[-1]), None
 
-    one, err = run(1)
+    usable, online, model = host_cpu()
+    per_proc = 2200 * N                            # bytes of one oracle sequence at its peak
+    avail = mem_available()
+    mem_cap = max(1, int(0.6 * avail) // per_proc) if avail else usable
+    procs = max(1, min(usable, mem_cap))
+    # about 10-30 s of oracle work: a 1M-entry query-step costs ~8x a 128K one
+    q1 = 16 if N <= 262144 else 4
+    queries = max(2 * procs, 32) if N <= 262144 else 2 * procs
+    host = {"nproc": usable, "online_cpus": online, "model": model,
+            "mem_available_gb": round(avail / 1e9, 1) if avail else None}
+    one, err = run(1, q1)
     if one is None:
-        return {"error": err}
-    sample = f"{queries} query-steps (1 query x 20 layers each, own sequence of N={N} entries), float64 numpy"
-    procs = max(1, min(os.cpu_count() or 1, 16, queries))
-    many, err = run(procs) if procs > 1 else (None, None)
-    single = {"value": one["value"], "cores": 1, "seconds": one["seconds"]}
+        return {"error": err, "host": host}
+    single = {"value": one["value"], "cores": 1, "seconds": one["seconds"], "queries": q1}
+    desc = f"query-steps (1 query x 20 layers each, its own sequence of N={N} entries), float64 numpy"
+    many, err = run(procs, queries) if procs > 1 else (None, None)
     if many is None:
         return {"value": one["value"], "unit": "query-layers/s", "cores": 1, "kind": "oracle",
-                "sample": sample + f", {one['seconds']:.1f} s single-threaded"}
+                "sample": f"{q1} {desc}, {one['seconds']:.1f} s single-threaded", "host": host}
+    cap = "" if procs == usable else f" (memory limits the processes to {procs} of {usable} cores)"
     return {"value": many["value"], "unit": "query-layers/s", "cores": many["procs"], "kind": "oracle",
-            "sample": sample + f", spread over {many['procs']} single-threaded processes "
-                               f"(the slowest timed {many['seconds']:.1f} s)",
-            "single_thread": single}
+            "sample": f"{queries} {desc}, spread over {many['procs']} single-threaded processes{cap} "
+                      f"(the slowest timed {many['seconds']:.1f} s)",
+            "single_thread": single, "host": host}
 
 
 def run_reference(a):
@@ -453,9 +496,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="decode128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="decode1m", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--cpu-queries", type=int, default=64)
+    ap.add_argument("--batch", type=int, default=None, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     a = ap.parse_args()
     a.steps_default = a.steps is None
@@ -489,7 +532,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     libbuild.build()
     cfg = WORKLOADS[a.workload]
-    step, info = workload.build_decode(cfg, seed=1000 + rank, device=f"cuda:{local}")
+    step, info = workload.build_decode(cfg, B=a.batch, seed=1000 + rank, device=f"cuda:{local}")
     nbytes = workload.algorithmic_bytes(info)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -498,16 +541,18 @@ def main():
     with torch.cuda.stream(stream):
         step.run()
     torch.cuda.synchronize()
-    # The timed loop replays one graph that holds S consecutive steps (few launch gaps).
-    # In the first captured step, external event-record nodes bracket the layer-0 Full
-    # indexer call (scan + select) and the three back-to-back Reuse-layer attention calls
-    # (layers 1..3); the last replay of the timed region gives one sample of each.  (An event
-    # node between two kernels turns their programmatic launch edge into a full one, so the
-    # other S - 1 steps carry none.)
+    # The timed loop replays graphs that each hold S consecutive steps (few launch gaps).
+    # In the first captured step of each graph, external event-record nodes bracket the
+    # layer-0 Full indexer call (scan + select), the three back-to-back Reuse-layer attention
+    # calls (layers 1..3) and the layer-4 Reindex call.  NG such graphs, each with its own
+    # events, are replayed in turn, so the timed region gives up to NG samples of each.  (An
+    # event node between two kernels turns their programmatic launch edge into a full one, so
+    # the other S - 1 steps of a graph carry none.)
     modes = info["schedule"]
-    assert modes[0] == FULL and list(modes[1:4]) == [REUSE] * 3
+    assert modes[0] == FULL and list(modes[1:4]) == [REUSE] * 3 and modes[4] == REINDEX
     S = next(d for d in (10, 5, 4, 2, 1) if a.steps % d == 0)
-    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]]
+    NG = max(1, min(5, a.steps // S))
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)] for _ in range(NG)]
 
     def one_step(e):
         step.run_append()
@@ -519,16 +564,23 @@ def main():
         for i in (1, 2, 3):
             step.run_layer(i)
         e[3].record(stream)
-        for i in range(4, len(step.layers)):
+        step.run_index(4)
+        e[4].record(stream)
+        step.run_attn(4)
+        e[5].record(stream)
+        for i in range(5, len(step.layers)):
             step.run_layer(i)
 
-    g_multi = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_multi, stream=stream):
-        for j in range(S):
-            if j == 0:
-                one_step(evs[0])
-            else:
-                step.run()
+    g_multi = []
+    for gi in range(NG):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(S):
+                if j == 0:
+                    one_step(evs[gi])
+                else:
+                    step.run()
+        g_multi.append(g)
     g_one = torch.cuda.CUDAGraph()                 # one step, for the end-to-end loop
     with torch.cuda.graph(g_one, stream=stream):
         step.run()
@@ -538,8 +590,8 @@ def main():
             torch.distributed.barrier()
 
     with torch.cuda.stream(stream):
-        for _ in range((a.warmup + S - 1) // S):
-            g_multi.replay()
+        for r_ in range((a.warmup + S - 1) // S):
+            g_multi[r_ % NG].replay()
     torch.cuda.synchronize()
 
     t_start = torch.cuda.Event(enable_timing=True)
@@ -551,8 +603,8 @@ def main():
     time.sleep(0.3)
     with torch.cuda.stream(stream):
         t_start.record(stream)
-        for _ in range(a.steps // S):
-            g_multi.replay()
+        for r_ in range(a.steps // S):
+            g_multi[r_ % NG].replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -560,6 +612,7 @@ def main():
     ms_total = t_start.elapsed_time(t_end)
     full_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) / 3.0
+    reindex_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
     ms_total = max_over_ranks(ms_total, world, f"cuda:{local}")
     ms_step = ms_total / a.steps
     B = info["B"]
@@ -635,6 +688,8 @@ def main():
         attn_gbs = attn_bytes / (attn_ms / 1000.0) / 1e9
         full_bytes = B * nbytes["per_query"]["full"]
         full_gbs = full_bytes / (full_ms / 1000.0) / 1e9
+        reindex_bytes = B * nbytes["per_query"]["reindex"]
+        reindex_gbs = reindex_bytes / (reindex_ms / 1000.0) / 1e9
         step_gbs = nbytes["total"] / (ms_step / 1000.0) / 1e9
         # the Full call scores on the tensor cores when a group's heads fill >= 16 columns
         tc_full = info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and info["H_i"] * info.get("G", 1) >= 16
@@ -644,6 +699,28 @@ def main():
         # per layer
         launches = (2 + (3 if tc_full else 2) * list(modes).count(FULL) + list(modes).count(REINDEX) +
                     len(modes))
+        n_full = list(modes).count(FULL)
+        n_reindex = list(modes).count(REINDEX)
+        roof = {
+            "attn": {"bound": "hbm", "kernel": "k_attn_tc (csa2_sparse_attn, one layer; mean of 3 back-to-back)",
+                     "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
+                     "traffic": profiled_traffic("k_attn_tc", a.workload), "peak_source": peak_kind,
+                     "algorithmic_bytes": attn_bytes, "ms": attn_ms, "launches_per_step": len(modes),
+                     "share_of_step": len(modes) * attn_ms / ms_step},
+            "index_full": {"bound": "hbm", "kernel": full_kernels + " (csa2_index_full)",
+                           "achieved": full_gbs, "peak": peak, "unit": "GB/s", "frac": full_gbs / peak,
+                           "traffic": profiled_traffic(full_kernels.split(" ")[0], a.workload),
+                           "traffic_kernel": full_kernels.split(" ")[0], "peak_source": peak_kind,
+                           "algorithmic_bytes": full_bytes, "ms": full_ms, "launches_per_step": n_full,
+                           "share_of_step": n_full * full_ms / ms_step},
+            "index_reindex": {"bound": "hbm", "kernel": "k_select_cl (csa2_index_reindex, scoring fused in)",
+                              "achieved": reindex_gbs, "peak": peak, "unit": "GB/s", "frac": reindex_gbs / peak,
+                              "traffic": profiled_traffic("k_select_cl_reindex", a.workload),
+                              "traffic_kernel": "k_select_cl", "peak_source": peak_kind,
+                              "algorithmic_bytes": reindex_bytes, "ms": reindex_ms, "launches_per_step": n_reindex,
+                              "share_of_step": n_reindex * reindex_ms / ms_step},
+        }
+        dominant = max(roof, key=lambda k_: roof[k_]["share_of_step"])
         line = {
             "metric": METRIC, "value": value, "unit": "query-layers/s", "n_gpus": world, "steps": a.steps,
             "warmup": a.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -656,23 +733,19 @@ def main():
                        "N": info["N"], "B": B, "layers": info["layers"], "d_kv": info["d"], "Hq": info["Hq"],
                        "indexer": f"{info['H_i']}x{info['d_ik']}", "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB algorithmic bytes per step"},
-            "roofline": {"bound": "hbm", "kernel": "k_attn_tc (csa2_sparse_attn, one layer; mean of 3 back-to-back)",
-                         "achieved": attn_gbs, "peak": peak, "unit": "GB/s", "frac": attn_gbs / peak,
-                         "traffic": profiled_traffic("k_attn_tc", a.workload), "peak_source": peak_kind,
-                         "algorithmic_bytes": attn_bytes, "ms": attn_ms},
-            "roofline_index_full": {"bound": "hbm", "kernel": full_kernels + " (csa2_index_full)",
-                                    "achieved": full_gbs, "peak": peak, "unit": "GB/s", "frac": full_gbs / peak,
-                                    "traffic": profiled_traffic(full_kernels.split(" ")[0], a.workload),
-                                    "traffic_kernel": full_kernels.split(" ")[0],
-                                    "algorithmic_bytes": full_bytes, "ms": full_ms},
-            "step_hbm": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": step_gbs, "frac": step_gbs / peak},
+            "roofline": dict(roof[dominant], dominant_of=sorted(roof), event_samples=len(evs)),
+            "roofline_attn": roof["attn"],
+            "roofline_index_full": roof["index_full"],
+            "roofline_index_reindex": roof["index_reindex"],
+            "step_hbm": {"algorithmic_bytes": nbytes["total"], "achieved_gbs": step_gbs, "frac": step_gbs / peak,
+                         "peak": peak, "peak_source": peak_kind},
             "clocks": clk,
             "gpu_launches": a.steps * launches,
             "e2e": {"value": e2e_val, "unit": "query-layers/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
         }
         if not a.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(info["N"], a.cpu_queries, SYNTH_NAME[a.workload])
+            line["cpu_baseline"] = cpu_baseline(info["N"], SYNTH_NAME[a.workload])
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -355,9 +355,10 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 // a thread-block cluster.
 //   shared : KV tile 160 keys x 512 dims fp16 (K-major, 128-byte swizzle)      160 KB
 //            Q 64 heads x 512 dims fp16 (K-major, 128-byte swizzle)               64 KB
-//            Q arrives by TMA (bf16, 64-dim x 16-head boxes, each CTA fetching 16 heads
-//            and multicasting them to the cluster) issued at kernel start; the data
-//            threads convert it to fp16 in place while their gathers are in flight.
+//            Q arrives by TMA (bf16, eight 64-dim x 64-head boxes, every CTA loading the
+//            query's whole Q for itself; L2 serves the other three CTAs' reads) issued at
+//            kernel start; the data threads convert it to fp16 in place while their
+//            gathers are in flight.
 //   TMEM   : S = Q K^T (fp32, 160 columns)                              cols   0..159
 //            P = softmax numerators (fp16 pairs, A operand)             cols   0..79
 //            O quarter q = P V[:, 128q..] (fp32)      q0: 256..383, q1: 384..511,
@@ -466,11 +467,11 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   const int kh = warp >> 2;
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-  // Q: CTA r of the cluster fetches heads [16 r, 16 r + 16) and multicasts them to all four,
-  // so every CTA's mbarrier 7 must be initialised before anyone's copy is issued: warp 8
-  // initialises, arrives on a cluster barrier and waits on it before issuing; the data warps
-  // arrive at once and wait for that phase only after issuing their gathers.  Warp 8 also
-  // allocates TMEM (and frees it at the end).
+  // Warp 8 allocates TMEM (and frees it at the end); its lane 0 initialises the mbarriers and
+  // at once issues this CTA's own load of Q.  The start-up cluster barrier orders every CTA's
+  // mbarrier initialisation before the bulk copies other CTAs later complete on them (the
+  // merge blocks): warp 8 arrives after initialising and waits at once; the data warps arrive
+  // at once and wait for that phase only before issuing their gathers.
   const bool worker = tid < NW;
   if (worker) {
     tc::cluster_arrive_relaxed();
@@ -488,17 +489,13 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       tc::mbar_arrive_expect_tx(&mbar[9], STG_CODES + STG_SCALES + (p.swa_max > 0 ? STG_SWA : 0));
       tc::fence_proxy_async_smem();             // the initialised barriers, seen by the TMA unit
       ok_flag = 1;
+      tc::mbar_arrive_expect_tx(&mbar[7], SM_Q);
+#pragma unroll
+      for (int a = 0; a < DIM / 64; ++a) tc::tma_load_2d(sQ + a * QATOM, &qmap, 64 * a, b * HQ, &mbar[7]);
     }
     __syncwarp();
     tc::cluster_arrive_relaxed();               // after fence.mbarrier_init (in mbar_init)
     tc::cluster_wait();
-    if (tid == ISSUER) {
-      const int r = (int)tc::cluster_ctarank();
-      tc::mbar_arrive_expect_tx(&mbar[7], SM_Q);
-#pragma unroll
-      for (int a = 0; a < DIM / 64; ++a)
-        tc::tma_load_2d_multicast(sQ + a * QATOM + r * 2048, &qmap, 64 * a, b * HQ + 16 * r, &mbar[7], 0xF);
-    }
   }
   if (worker) {
   // ---- each thread resolves the keys it dequantises: FP4 slot fkey (2 threads per key)
@@ -1012,11 +1009,11 @@ static cudaError_t run_attn_tc(const csa2_attn_args& a, AttnParams& ap, cudaStre
     attr_set = true;
   }
   ap.nchunk = tca::NCH;
-  CUtensorMap qmap, cmap, smap, wmap;            // q as [B * 64 heads][512] bf16, 16 heads x 64 dims boxes;
+  CUtensorMap qmap, cmap, smap, wmap;            // q as [B * 64 heads][512] bf16, 64 heads x 64 dims boxes;
                                                 // code / scale rows (one-row boxes, gathered 4 at a time);
                                                 // window rows (32 rows x 256 bytes)
   const long long rows = (long long)a.cache.num_pages * 64;
-  if (!bf16_map(&qmap, a.q, (long long)a.B * tca::HQ, tca::DIM, tca::HQ / tca::NCH) ||
+  if (!bf16_map(&qmap, a.q, (long long)a.B * tca::HQ, tca::DIM, tca::HQ) ||
       !u8_map(&cmap, a.cache.codes, rows, tca::DIM / 2, tca::DIM / 2, 1) ||
       !u8_map(&smap, a.cache.scales, rows, tca::DIM / 16, tca::DIM / 16, 1))
     return cudaErrorInvalidValue;

@@ -262,18 +262,6 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* map, int x, i
       : "memory");
 }
 
-// 2-D tiled TMA load of the box at (x, y) into the same shared-memory offset of every CTA
-// in `mask` of the cluster, each CTA's mbarrier at `mbar`'s offset receiving the bytes.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const void* tmap, int x, int y, uint64_t* mbar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%4, %5}], [%2], %3;"
-      :: "r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(tmap), "r"((uint32_t)__cvta_generic_to_shared(mbar)),
-         "h"(mask), "r"(x), "r"(y)
-      : "memory");
-}
-
 // Wait for phase `parity` to complete, giving up after max_iter polls.  Returns false on
 // timeout (the caller records an error and stops issuing work).
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global memory
