@@ -58,8 +58,44 @@ __device__ __forceinline__ uint32_t swz(int row, int ch, int rowbytes) {
   return (uint32_t)(row * rowbytes + ((ch ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
-  float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
+// ---- operand ranges ---------------------------------------------------------------------
+// The products run on fp16 operands.  fp16 holds every FP4 x E4M3 value and every E4M3 value
+// exactly, so the key tile holds the FP4 rows dequantised and the window rows as their raw
+// E4M3 values: the keys are exact.  A window row's float32 scale c_r is applied in float32
+// instead, to its logit (S column r times c_r) and to its probability in the P.V product
+// (p_r c_r 2^-G, G a per-CTA power of two that keeps every p_r c_r 2^-G <= 1; undone on the
+// partial output).  So the logits carry no rounding of the keys, which their size would
+// amplify.  q (bf16) is scaled per head by a power of two that puts its largest magnitude in
+// [2^14, 2^15) before the fp16 rounding (exact; undone on the logits).
+
+// 2^e as float32, e in [-126, 127]
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// the shift F with (nonnegative float bits `mx`) * 2^-F in [2^14, 2^15); 0 for mx == 0.
+// Clamped to [-100, 100]: beyond that the values are far below (or the logits far beyond)
+// anything the float32 softmax resolves.
+__device__ __forceinline__ int pow2_shift(uint32_t mx) {
+  if (mx == 0u) return 0;
+  const int e = (int)((mx >> 23) & 0xffu) - 127 - 14;
+  return max(-100, min(100, e));
+}
+
+// the G with (positive float bits `mx`) * 2^-G in [0.5, 1); 0 for mx == 0.  Clamped to
+// [-126, 126] (2^-G stays a normal float32).
+__device__ __forceinline__ int pfactor_shift(uint32_t mx) {
+  if (mx == 0u) return 0;
+  return max(-126, min(126, (int)((mx >> 23) & 0xffu) - 126));
+}
+
+// largest |x| of eight bf16 values, as a bf16 magnitude bit pattern
+__device__ __forceinline__ uint32_t bf16x8_absmax(uint4 v) {
+  const uint32_t M = 0x7fff7fffu;
+  const uint32_t m = __vmaxu2(__vmaxu2(v.x & M, v.y & M), __vmaxu2(v.z & M, v.w & M));
+  return max(m & 0xffffu, m >> 16);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t v, float s) {
+  const float lo = __uint_as_float(v << 16) * s, hi = __uint_as_float(v & 0xffff0000u) * s;
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
@@ -94,6 +130,8 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
   __shared__ long long keyrow[KC];
   __shared__ float keyscale[KC];
   __shared__ int keykind[KC];       // 0 none, 1 FP4 entry, 2 SWA row
+  __shared__ float qf[C::HP];       // 2^F of each head's Q normalisation
+  __shared__ uint32_t kvmax[ATHREADS / 32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -113,6 +151,7 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
         if (e >= 0) {
           row = entry_row(p.cache, __ldg(p.seq_of + b), e, &g_err_attn);
           kind = row >= 0 ? 1 : 0;
+          sc = kind ? 1.f : 0.f;
         }
       }
     } else if (j - p.k < p.swa_max) {
@@ -132,22 +171,54 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
     keykind[tid] = kind;
     keyscale[tid] = sc;
   }
-  // ---- 2. Q (bf16 -> fp16), rows >= Hq are zero ------------------------------
-  for (int i = tid; i < C::HP * (DIM / 8); i += ATHREADS) {
-    const int h = i / (DIM / 8), ch = i % (DIM / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (h < p.Hq) v = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + h) * DIM) + ch);
-    uint4 o = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                         bf16x2_to_f16x2(v.w));
-    *reinterpret_cast<uint4*>(sQ + swz(h, ch, C::ROWB)) = o;
+  // ---- 2. Q (bf16 -> fp16, scaled per head), rows >= Hq are zero: warp w converts heads
+  //      w, w + 16, ..., lane l the head's 16-byte chunks l and l + 32 ---------------------
+  {
+    constexpr int CH = DIM / 8, CPL = (CH + 31) / 32;
+    for (int h = warp; h < C::HP; h += ATHREADS / 32) {
+      uint4 v[CPL];
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int ch = lane + 32 * j;
+        v[j] = make_uint4(0, 0, 0, 0);
+        if (h < p.Hq && ch < CH) v[j] = __ldg(reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + h) * DIM) + ch);
+        m = max(m, bf16x8_absmax(v[j]));
+      }
+      const int F = pow2_shift(__reduce_max_sync(AFULL, m) << 16);
+      const float sc = exp2i(-F);
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int ch = lane + 32 * j;
+        if (ch < CH)
+          *reinterpret_cast<uint4*>(sQ + swz(h, ch, C::ROWB)) =
+              make_uint4(bf16x2_to_f16x2_scaled(v[j].x, sc), bf16x2_to_f16x2_scaled(v[j].y, sc),
+                         bf16x2_to_f16x2_scaled(v[j].z, sc), bf16x2_to_f16x2_scaled(v[j].w, sc));
+      }
+      if (lane == 0) qf[h] = exp2i(F);
+    }
   }
   __syncthreads();
-  // ---- 3. gather + dequantise the 128 keys (4 threads per key) -----------------
+  // ---- 3. the chunk's probability factor 2^-G: every key's float32 factor c (FP4 entry 1,
+  //      window row its scale), maximised over the CTA ---------------------------------------
+  const int key = tid >> 2, qtr = tid & 3;
+  const int kind = keykind[key];
+  const long long row = keyrow[key];
+  constexpr int DQ = DIM / 4;                   // dims per thread
   {
-    const int key = tid >> 2, qtr = tid & 3;
-    const int kind = keykind[key];
-    const long long row = keyrow[key];
-    constexpr int DQ = DIM / 4;                 // dims per thread
+    uint32_t mloc = kind == 0 ? 0u : __float_as_uint(fabsf(keyscale[key]));
+    mloc = __reduce_max_sync(AFULL, mloc);
+    if (lane == 0) kvmax[warp] = mloc;
+  }
+  __syncthreads();
+  uint32_t kvm = 0;
+#pragma unroll
+  for (int w = 0; w < ATHREADS / 32; ++w) kvm = max(kvm, kvmax[w]);
+  const int G = pfactor_shift(kvm);
+  const float sG = exp2i(-G), fG = exp2i(G);
+  // ---- 4. gather + dequantise the 128 keys (4 threads per key): FP4 rows exactly, window
+  //      rows as their E4M3 values (both exact in fp16) ---------------------------------------
+  {
     if (kind == 1) {
       const uint8_t* cp = p.cache.codes + row * (DIM / 2) + qtr * (DQ / 2);
       const uint8_t* sp = p.cache.scales + row * (DIM / 16) + qtr * (DQ / 16);
@@ -174,7 +245,6 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
       }
     } else if (kind == 2) {
       const uint8_t* rp = p.swa + row * DIM + qtr * DQ;
-      const float sc = keyscale[key];
 #pragma unroll
       for (int cc = 0; cc < DQ / 16; ++cc) {      // 16 bytes = 16 dims = 2 smem chunks
         uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + cc * 16));
@@ -183,12 +253,7 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi)
 #pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
-            __half2 hv = *reinterpret_cast<__half2*>(&h2);
-            __half2 r = __floats2half2_rn(__low2float(hv) * sc, __high2float(hv) * sc);
-            outw[wi * 2 + hi] = *reinterpret_cast<uint32_t*>(&r);
-          }
+          for (int hi = 0; hi < 2; ++hi) outw[wi * 2 + hi] = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
         const int ch0 = (qtr * DQ + cc * 16) / 8;
         *reinterpret_cast<uint4*>(sKV + swz(key, ch0, C::ROWB)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         *reinterpret_cast<uint4*>(sKV + swz(key, ch0 + 1, C::ROWB)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
@@ -237,18 +302,21 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
       }
     }
   }
-  // ---- 5. chunk-local softmax -------------------------------------------------
+  // ---- 5. chunk-local softmax (logits in log2 units: the head's Q factor and the key's c
+  //      applied) ----------------------------------------------------------------------------
   // thread holds rows r0 = mt*16+g, r1 = r0+8; keys kbase + 8t + 2c + {0,1}
   const int r0 = mt * 16 + g, r1 = r0 + 8;
+  const float lsc0 = p.scale_log2 * qf[r0], lsc1 = p.scale_log2 * qf[r1];
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
   for (int t = 0; t < MT; ++t) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int key = kbase + 8 * t + 2 * c + e;
-      const bool valid = keykind[key] != 0;
-      float v0 = valid ? sacc[t][e] * p.scale_log2 : -INFINITY;
-      float v1 = valid ? sacc[t][2 + e] * p.scale_log2 : -INFINITY;
+      const int kk = kbase + 8 * t + 2 * c + e;
+      const bool valid = keykind[kk] != 0;
+      const float ck = keyscale[kk];
+      float v0 = valid ? sacc[t][e] * lsc0 * ck : -INFINITY;
+      float v1 = valid ? sacc[t][2 + e] * lsc1 * ck : -INFINITY;
       sacc[t][e] = v0;
       sacc[t][2 + e] = v1;
       mx0 = fmaxf(mx0, v0);
@@ -273,18 +341,20 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
   float l0 = 0.f, l1 = 0.f;
 #pragma unroll
   for (int t = 0; t < MT; ++t) {
-    const int key = kbase + 8 * t + 2 * c;
+    const int kk = kbase + 8 * t + 2 * c;
     float e00 = (m0 == -INFINITY) ? 0.f : exp2f(sacc[t][0] - m0);
     float e01 = (m0 == -INFINITY) ? 0.f : exp2f(sacc[t][1] - m0);
     float e10 = (m1 == -INFINITY) ? 0.f : exp2f(sacc[t][2] - m1);
     float e11 = (m1 == -INFINITY) ? 0.f : exp2f(sacc[t][3] - m1);
-    __half2 h0 = __floats2half2_rn(e00, e01);
-    __half2 h1 = __floats2half2_rn(e10, e11);
-    l0 += __low2float(h0) + __high2float(h0);
-    l1 += __low2float(h1) + __high2float(h1);
+    l0 += e00 + e01;
+    l1 += e10 + e11;
+    // the P.V weights p c 2^-G (<= 1; an invalid key has p = 0 and c = 0)
+    const float c0 = keyscale[kk] * sG, c1 = keyscale[kk + 1] * sG;
+    __half2 h0 = __floats2half2_rn(e00 * c0, e01 * c1);
+    __half2 h1 = __floats2half2_rn(e10 * c0, e11 * c1);
     // P[row][key..key+1]: chunk key/8, element offset (key%8)*2 bytes
-    *reinterpret_cast<__half2*>(sP + swz(r0, key >> 3, C::PROWB) + (key & 7) * 2) = h0;
-    *reinterpret_cast<__half2*>(sP + swz(r1, key >> 3, C::PROWB) + (key & 7) * 2) = h1;
+    *reinterpret_cast<__half2*>(sP + swz(r0, kk >> 3, C::PROWB) + (kk & 7) * 2) = h0;
+    *reinterpret_cast<__half2*>(sP + swz(r1, kk >> 3, C::PROWB) + (kk & 7) * 2) = h1;
   }
   l0 += __shfl_xor_sync(AFULL, l0, 1);
   l1 += __shfl_xor_sync(AFULL, l1, 1);
@@ -311,32 +381,34 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
       if constexpr (C::NTO == 1) {
         // two k-steps' worth is not needed: one n-tile, keys 16ks..16ks+15
         uint32_t b0, b1, b2, b3;
-        const int key = 16 * ks + (mi & 1) * 8 + r8;
-        ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(key, dbase / 8, C::ROWB));
+        const int kk = 16 * ks + (mi & 1) * 8 + r8;
+        ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(kk, dbase / 8, C::ROWB));
         mma_f16_16816(oacc[0], a0, a1, a2, a3, b0, b1);
       } else {
 #pragma unroll
         for (int np = 0; np < C::NTO / 2; ++np) {
           uint32_t b0, b1, b2, b3;
-          const int key = 16 * ks + (mi & 1) * 8 + r8;
-          ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(key, (dbase + 16 * np) / 8 + (mi >> 1), C::ROWB));
+          const int kk = 16 * ks + (mi & 1) * 8 + r8;
+          ldmatrix_x4_trans(b0, b1, b2, b3, kvs + swz(kk, (dbase + 16 * np) / 8 + (mi >> 1), C::ROWB));
           mma_f16_16816(oacc[2 * np], a0, a1, a2, a3, b0, b1);
           mma_f16_16816(oacc[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
       }
     }
   }
-  // ---- 7. partial outputs -----------------------------------------------------
+  // ---- 7. partial outputs (the probability factor 2^-G undone) ------------------------
   const long long pbase = ((long long)b * p.nchunk + chunk) * p.Hq;
   if (r0 < p.Hq) {
     float* o = p.opart + (pbase + r0) * DIM + dbase + 2 * c;
 #pragma unroll
-    for (int t = 0; t < C::NTO; ++t) *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][0], oacc[t][1]);
+    for (int t = 0; t < C::NTO; ++t)
+      *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][0] * fG, oacc[t][1] * fG);
   }
   if (r1 < p.Hq) {
     float* o = p.opart + (pbase + r1) * DIM + dbase + 2 * c;
 #pragma unroll
-    for (int t = 0; t < C::NTO; ++t) *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][2], oacc[t][3]);
+    for (int t = 0; t < C::NTO; ++t)
+      *reinterpret_cast<float2*>(o + 8 * t) = make_float2(oacc[t][2] * fG, oacc[t][3] * fG);
   }
   if (dg == 0 && c == 0) {
     float s0 = 0.f, s1 = 0.f;
@@ -392,12 +464,17 @@ constexpr int QATOM = HQ / 8 * 1024;            // bytes per 64-dim K-atom of th
 constexpr int SM_KV = NK * DIM * 2;             // 163840
 constexpr int SM_Q = HQ * DIM * 2;              // 65536
 struct Misc {                                   // small per-CTA state, after the tiles
-  int keyok[NK];
+  alignas(16) float kc[NK];      // each key's logit factor c: 1 (FP4 entry), the row scale
+                                 // (window row), NaN (no key)
+  int8_t qfe[HQ];                // F of each head's Q normalisation (q scaled by 2^-F)
   float pmax[2][HQ];
   float psum[2][HQ];
   alignas(16) float2 rml[NCH][HQ / NCH];   // (row max in log2 units, row sum) of each chunk
                                            // for this CTA's 16 heads
   alignas(16) float2 rml_out[NCH][HQ / NCH];   // this chunk's pairs for each owner's heads
+  alignas(16) float ecs[NCH][4];          // [c][0]: 2^G of chunk c (its P.V weights carry 2^-G)
+  alignas(16) float ec_out[4];            // [0]: this chunk's 2^G, sent to the other owners
+  uint32_t kvmax[NW / 32];                // each data warp's largest key factor c (float bits)
   uint64_t mbar[10];              // 0: MMA1, 1..4: MMA2 quarters, 5: dims 0..255 of every key
                                   // written (by the 8 data warps), 6: quarter 0's columns read
                                   // by the 8 data warps, 7: Q landed, 8: the other chunks'
@@ -418,7 +495,7 @@ constexpr int STG_CODES = 32768, STG_SCALES = 4096, STG_SWA = 16384;
 constexpr int STG = SM_KV - (STG_CODES + STG_SCALES + STG_SWA);
 static_assert(STG % 1024 == 0, "staging alignment");
 constexpr int QBLK = BLK / 4;                   // its part of one O quarter (128 dims), 4 KB
-constexpr uint32_t RECV_BYTES = (NCH - 1) * (4 * QBLK + HQ / NCH * 8);   // from the 3 other chunks
+constexpr uint32_t RECV_BYTES = (NCH - 1) * (4 * QBLK + HQ / NCH * 8 + 16);   // from the 3 other chunks
 
 __device__ __forceinline__ uint32_t col_o(int q) { return q == 0 ? 256u : q == 1 ? 384u : q == 2 ? 128u : 256u; }
 
@@ -446,7 +523,6 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   uint8_t* sKV = smem;
   uint8_t* sQ = smem + SM_KV;
   Misc& ms = *reinterpret_cast<Misc*>(smem + SM_KV + SM_Q);
-  int* keyok = ms.keyok;
   float (*pmax)[HQ] = ms.pmax;
   float (*psum)[HQ] = ms.psum;
   uint64_t* mbar = ms.mbar;
@@ -473,6 +549,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   // merge blocks): warp 8 arrives after initialising and waits at once; the data warps arrive
   // at once and wait for that phase only before issuing their gathers.
   const bool worker = tid < NW;
+  float sG = 1.f;                               // 2^-G: this chunk's P.V weights are p c 2^-G
   if (worker) {
     tc::cluster_arrive_relaxed();
   } else {
@@ -553,17 +630,24 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       tc::tma_load_2d(sKV + STG + STG_CODES + STG_SCALES + STG_SWA / 2, &wmap, 256, wrow0, &mbar[9]);
     }
   }
-  if (half == 0) keyok[fkey] = fok;
-  if (part == 0) keyok[skey] = sok;
-  // ---- Q -> fp16 in place while the rows are in flight.  Chunk idx = tid + i NW is
-  //      16-byte chunk idx % 64 of head idx / 64. -------------------------------------------
+  if (half == 0) ms.kc[fkey] = fok ? 1.f : __int_as_float(0x7fc00000);
+  if (part == 0) ms.kc[skey] = sok ? ssc : __int_as_float(0x7fc00000);
+  // ---- Q -> fp16 in place, scaled per head, while the rows are in flight.  Warp w converts
+  //      heads w, w + 8, ..., lane l the head's 16-byte chunks l and l + 32. ------------------
   if (tc::mbar_wait_warp(&mbar[7], 0, MAX_POLL)) {
 #pragma unroll
-    for (int i = 0; i < SM_Q / 16 / NW; ++i) {
-      const int idx = tid + i * NW, h = idx >> 6, ch = idx & 63;
-      uint4* qp = reinterpret_cast<uint4*>(sQ + tileoff(h, ch, QATOM));
-      const uint4 v = *qp;
-      *qp = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    for (int i = 0; i < HQ / (NW / 32); ++i) {
+      const int h = warp + (NW / 32) * i;
+      uint4* q0 = reinterpret_cast<uint4*>(sQ + tileoff(h, lane, QATOM));
+      uint4* q1 = reinterpret_cast<uint4*>(sQ + tileoff(h, lane + 32, QATOM));
+      const uint4 v0 = *q0, v1 = *q1;
+      const int F = pow2_shift(__reduce_max_sync(0xffffffffu, max(bf16x8_absmax(v0), bf16x8_absmax(v1))) << 16);
+      const float sc = exp2i(-F);
+      *q0 = make_uint4(bf16x2_to_f16x2_scaled(v0.x, sc), bf16x2_to_f16x2_scaled(v0.y, sc),
+                       bf16x2_to_f16x2_scaled(v0.z, sc), bf16x2_to_f16x2_scaled(v0.w, sc));
+      *q1 = make_uint4(bf16x2_to_f16x2_scaled(v1.x, sc), bf16x2_to_f16x2_scaled(v1.y, sc),
+                       bf16x2_to_f16x2_scaled(v1.z, sc), bf16x2_to_f16x2_scaled(v1.w, sc));
+      if (lane == 0) ms.qfe[h] = (int8_t)F;
     }
   } else {
     raise_error(&g_err_attn, CSA2_DEVERR_TIMEOUT);
@@ -594,16 +678,33 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
     for (int i = 0; i < 4; ++i) wv[i] = *reinterpret_cast<const uint4*>(ws + 16 * ((i + rot_s) & 3));
   }
+  // the chunk's P.V factor 2^-G: the largest key factor c of its keys (1 for an FP4 entry,
+  // the row scale for a window row), maximised over the data warps
+  {
+    uint32_t mloc = fok ? __float_as_uint(1.f) : 0u;
+    if (sok) mloc = max(mloc, __float_as_uint(fabsf(ssc)));
+    mloc = __reduce_max_sync(0xffffffffu, mloc);
+    if (lane == 0) ms.kvmax[warp] = mloc;
+  }
   asm volatile("bar.sync 5, %0;" :: "n"(NW) : "memory");
+  {
+    uint32_t kvm = 0;
+#pragma unroll
+    for (int w = 0; w < NW / 32; ++w) kvm = max(kvm, ms.kvmax[w]);
+    const int G = pfactor_shift(kvm);
+    sG = exp2i(-G);
+    if (tid == 0) {
+      ms.ec_out[0] = exp2i(G);
+      ms.ecs[tc::cluster_ctarank()][0] = exp2i(G);
+      tc::fence_proxy_async_smem();             // ec_out is read by a bulk copy later
+    }
+  }
   // ---- dequantise into the K-major KV tile: the window rows (every dim), then the FP4 rows
   //      in two phases of 256 dims.  Once every warp has written phase 0 (mbarrier 5), the
   //      products over those dims start while phase 1 is written. ----------------------------
   if (sok) {
-    // E4M3 (exact in fp16) times the row scale split as sc_hi + sc_lo (fp16 each): one
-    // multiply and one fused multiply-add in fp16, within 2^-11 of the exact product
-    const __half shi = __float2half_rn(ssc);
-    const __half slo = __float2half_rn(ssc - __half2float(shi));
-    const __half2 shi2 = __halves2half2(shi, shi), slo2 = __halves2half2(slo, slo);
+    // the row's E4M3 values, exact in fp16 (its scale is applied in float32 to its logit and
+    // to its P.V weight)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {               // 16 bytes = 16 dims = 2 chunks
       const int c = (i + rot_s) & 3;
@@ -612,12 +713,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
 #pragma unroll
       for (int wi = 0; wi < 4; ++wi)
 #pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
-          const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-          const __half2 r = __hfma2(hv, slo2, __hmul2(hv, shi2));
-          o[wi * 2 + hi] = *reinterpret_cast<const uint32_t*>(&r);
-        }
+        for (int hi = 0; hi < 2; ++hi) o[wi * 2 + hi] = e4m3x2_to_f16x2((uint16_t)(words[wi] >> (16 * hi)));
       const int ch0 = part * 8 + c * 2;
       *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(sKV + kvoff(skey, ch0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -704,16 +800,18 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
     tc::tmem_ld16x2_32<40>(tb + lane_base + COL_S + 80 * kh, r);
     tc::tmem_ld16x2_8<40>(tb + lane_base + COL_S + 80 * kh + 32, r + 32);
     tc::tmem_ld_wait();
-    const int4* ok4 = reinterpret_cast<const int4*>(keyok + 80 * kh + 40 * sub);
+    // logits in log2 units: the head's Q factor 2^F and each key's factor c applied
+    const float4* kc4 = reinterpret_cast<const float4*>(ms.kc + 80 * kh + 40 * sub);
+    const float lsc = p.scale_log2 * exp2i(ms.qfe[head]);
     float mx = -INFINITY;
 #pragma unroll
     for (int j4 = 0; j4 < 10; ++j4) {
-      const int4 v = ok4[j4];
-      const int okv[4] = {v.x, v.y, v.z, v.w};
+      const float4 v = kc4[j4];
+      const float cv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int j = 4 * j4 + t;
-        e[j] = okv[t] ? __uint_as_float(r[j]) * p.scale_log2 : -INFINITY;
+        e[j] = cv[t] == cv[t] ? __uint_as_float(r[j]) * lsc * cv[t] : -INFINITY;
         mx = fmaxf(mx, e[j]);
       }
     }
@@ -727,18 +825,24 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   tc::fence_after_sync();
   if (ok_flag) {
     const float m = fmaxf(pmax[0][head], pmax[1][head]);
+    const float4* kc4 = reinterpret_cast<const float4*>(ms.kc + 80 * kh + 40 * sub);
     float l = 0.f;
     uint32_t pk[20];
 #pragma unroll
-    for (int j = 0; j < 40; j += 2) {
-      float x0 = 0.f, x1 = 0.f;
+    for (int j4 = 0; j4 < 10; ++j4) {
+      const float4 v = kc4[j4];
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
       if (m != -INFINITY) {
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x0) : "f"(e[j] - m));
-        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x1) : "f"(e[j + 1] - m));
+#pragma unroll
+        for (int t = 0; t < 4; ++t) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(x[t]) : "f"(e[4 * j4 + t] - m));
       }
-      const __half2 hp = __floats2half2_rn(x0, x1);
-      pk[j >> 1] = *reinterpret_cast<const uint32_t*>(&hp);
-      l += __low2float(hp) + __high2float(hp);
+      l += (x[0] + x[1]) + (x[2] + x[3]);
+      // the P.V weights p c 2^-G (<= 1); no key: 0
+      const float w0 = v.x == v.x ? x[0] * v.x * sG : 0.f, w1 = v.y == v.y ? x[1] * v.y * sG : 0.f;
+      const float w2 = v.z == v.z ? x[2] * v.z * sG : 0.f, w3 = v.w == v.w ? x[3] * v.w * sG : 0.f;
+      const __half2 h01 = __floats2half2_rn(w0, w1), h23 = __floats2half2_rn(w2, w3);
+      pk[2 * j4] = *reinterpret_cast<const uint32_t*>(&h01);
+      pk[2 * j4 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
     }
     // P column = key / 2: this thread's 40 keys are columns [40 kh + 20 sub, + 20)
     tc::tmem_st16x2_16<20>(tb + lane_base + COL_S + 40 * kh, pk);
@@ -836,9 +940,11 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
         if (kh == 0 && lane == 0) {
           const uint32_t dmb = tc::mapa(smem_u32(&mbar[8]), owner);
           tc::bulk_copy_to_cluster(tc::mapa(q_a + rank * BLK + q * QBLK, owner), blk, QBLK, dmb);
-          if (q == 0)
+          if (q == 0) {
             tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.rml[rank][0]), owner), &ms.rml_out[owner][0],
                                      HQ / NCH * 8, dmb);
+            tc::bulk_copy_to_cluster(tc::mapa(smem_u32(&ms.ecs[rank][0]), owner), &ms.ec_out[0], 16, dmb);
+          }
         }
       }
     }
@@ -872,7 +978,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
       }
       const float inv = (L > 0.f) ? 1.f / L : 0.f;
 #pragma unroll
-      for (int c = 0; c < NCH; ++c) wts[tid * NCH + c] = w4[c] * inv;
+      for (int c = 0; c < NCH; ++c) wts[tid * NCH + c] = w4[c] * inv * ms.ecs[c][0];   // x 2^G of chunk c
       if (p.lse) p.lse[(long long)b * HQ + h] = (L > 0.f) ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();

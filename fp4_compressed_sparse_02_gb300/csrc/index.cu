@@ -16,6 +16,8 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -943,30 +945,68 @@ cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cud
 // ---------------------------------------------------------------------------------
 // Fixed scratch for csa2_index_full_noalloc: the pool scores live in this array
 // instead of a caller workspace.  Host code cannot use the symbol as a device address,
-// so the address is looked up once per device with that device current.
+// so the address is looked up with the device current, once per CUDA context: the
+// array's address belongs to the context the library's module is loaded in, so the cache
+// is keyed by the context's unique id (a new context after cudaDeviceReset, or a second
+// context on the same device, gets its own lookup).
 // ---------------------------------------------------------------------------------
 static __device__ __align__(256) float g_noalloc_scores[CSA2_NOALLOC_MAX_SCORES];
 
 namespace {
-constexpr int kMaxDevices = 256;
+constexpr int kMaxContexts = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxContexts] = {};
+void* g_noalloc_addr[kMaxContexts] = {};
+int g_noalloc_n = 0;
+
+typedef CUresult (*PFN_ctx_current)(CUcontext*);
+typedef CUresult (*PFN_ctx_id)(CUcontext, unsigned long long*);
+
+// unique id of the calling thread's current context; false when the driver cannot say
+bool current_context_id(unsigned long long* id) {
+  static PFN_ctx_current get_current = nullptr;
+  static PFN_ctx_id get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_ctx_current>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_ctx_id>(fn);
+    tried = true;
+  }
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 }  // namespace
 
 cudaError_t index_noalloc_scratch(void** ptr, size_t* bytes) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scores);
-    if (e != cudaSuccess) return e;
-    g_noalloc_addr[dev] = p;
-  }
-  *ptr = g_noalloc_addr[dev];
   *bytes = sizeof(g_noalloc_scores);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  unsigned long long id = 0;
+  const bool have_id = current_context_id(&id);
+  if (have_id)
+    for (int i = 0; i < g_noalloc_n; ++i)
+      if (g_noalloc_ctx[i] == id) {
+        *ptr = g_noalloc_addr[i];
+        return cudaSuccess;
+      }
+  // no context current yet (the lookup below creates the primary one) or a new context
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scores);
+  if (e != cudaSuccess) return e;
+  if (have_id && g_noalloc_n < kMaxContexts) {      // remembered; past 64 contexts looked up each call
+    g_noalloc_ctx[g_noalloc_n] = id;
+    g_noalloc_addr[g_noalloc_n] = p;
+    ++g_noalloc_n;
+  }
+  *ptr = p;
   return cudaSuccess;
 }
 

@@ -204,13 +204,21 @@ csa2_status csa2_index_full_workspace(const csa2_index_full_args* args, size_t* 
  * the library, CSA2_NOALLOC_MAX_SCORES floats (4 MiB).  Every GPU that loads the
  * library holds that array until the process exits.  The call itself allocates nothing.
  *
- * Arguments, outputs and results are exactly those of csa2_index_full.  Limits and
- * rules of the shared array:
+ * Arguments and outputs are those of csa2_index_full, and so are the results whenever
+ * csa2_index_full scans (group x H_i < 16, or a shape the tensor-core scoring does not
+ * take): this call always scans, because the fixed array holds the pool scores only, not
+ * the tensor-core score matrix.  Where csa2_index_full scores on the tensor cores instead
+ * (group x H_i >= 16 with H_i in {8, 16, 32}, see above), the two calls accumulate the
+ * float32 scores in different orders, so an entry whose score ties another's to within
+ * rounding may be kept by one call and not the other; both results satisfy the same
+ * near-tie rule against the exact scores.  Limits and rules of the shared array:
  *   - B * num_blocks * per_block must not exceed CSA2_NOALLOC_MAX_SCORES (with the
  *     16,384-candidate pool that is B <= 64); larger calls return
  *     CSA2_ERR_UNSUPPORTED_SHAPE and launch nothing.
- *   - The first call on a device looks up the array's device address for that device
- *     (the device must be current); make that first call before any stream capture.
+ *   - The array's device address belongs to a CUDA context.  The first call in a context
+ *     (the device's primary one, another one made current, or a new one after
+ *     cudaDeviceReset) looks it up with the device current; make that first call before
+ *     any stream capture.
  *   - All calls on a device share the one array and it keeps the previous call's
  *     contents.  Nothing in it needs to start at zero (every score is written before it
  *     is read), but calls that overlap on the GPU -- on two streams, or from two host
@@ -258,9 +266,13 @@ csa2_status csa2_index_reindex_workspace(const csa2_index_reindex_args* args, si
  *   l_s = softmax_scale * q[b][h] . kv_s;  p = softmax_S(l);  out[b][h] = sum_s p_s kv_s
  *   kv_s = dequant FP4 entry (exact) or E4M3 row * swa_scale[row].
  *   lse[b][h] = log(sum_s exp(l_s)) (natural log); empty S gives out = 0, lse = -inf.
- * The GPU computes the products in fp16 tensor-core MMAs with float32 accumulation
- * (FP4 and E4M3 values are exact in fp16; the SWA row scale and q are rounded to
- * fp16; |q| and |kv| must stay below 65504).
+ * Precision: the products run on fp16 tensor-core operands with float32 accumulation.
+ * The keys are exact there (the dequantised FP4 entries and the window rows' E4M3 values);
+ * a window row's scale is applied in float32 to its logit and to its weight in P.V; each
+ * head's q is scaled by a power of two before its fp16 rounding (exact for every bf16
+ * element within 2^-28 of the head's largest), and the probabilities are fp16 (2^-12
+ * relative).  Inputs: any finite bf16 q, any E4M3 scale byte but the NaN patterns 0x7F /
+ * 0xFF, any finite swa_scale; the logits softmax_scale * q . kv must be finite in float32.
  * Supported: Hq in {8, 16, 32, 64}, d in {128, 512}, k + swa_max <= 4096.
  * -------------------------------------------------------------------------- */
 typedef struct csa2_attn_args {

@@ -214,3 +214,105 @@ def test_bounded_wait_times_out_reports_and_context_survives():
     out, _ = _run(c)
     ref, _ = _oracle(c)
     _assert_close(out, ref)
+
+
+# ---- the whole input range ------------------------------------------------------------
+# The default generator keeps every input in a moderate range.  These cases sweep what the
+# formats allow: every finite E4M3 byte in the window rows (subnormals and 128..448 among
+# them), row scales from 2^-24 to 2^7, every FP4 scale byte 0x00..0x7E (0 included) and bf16
+# Q whose magnitudes span 2^-30..2^15 (and a query far beyond the fp16 range).  The outputs
+# then span many orders of magnitude, so the comparison is per query head: relative L2
+# <= 2e-3, and max-abs <= 1e-2 x max(1, max |o_ref|) of that head (the 1e-2 is an absolute
+# bound for outputs of unit scale, relative above it).
+
+_E4M3_FINITE = np.array([v for v in range(256) if (v & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def _assert_close_per_head(got, ref, what=""):
+    B, H, _ = ref.shape
+    for b in range(B):
+        for h in range(H):
+            g, o = got[b, h].astype(np.float64), ref[b, h]
+            no = np.linalg.norm(o)
+            if no == 0:
+                assert not g.any(), f"{what} b={b} h={h}: expected zeros"
+                continue
+            e = np.linalg.norm(g - o) / no
+            assert e <= ATTN_REL_L2, f"{what} b={b} h={h}: rel-L2 {e:.3g} (|o| ~ {np.abs(o).max():.3g})"
+            assert np.abs(g - o).max() <= ATTN_MAX_ABS * max(1.0, np.abs(o).max()), f"{what} b={b} h={h}: max-abs"
+
+
+def _lse_close(lse, rlse):
+    fin = np.isfinite(rlse)
+    np.testing.assert_allclose(lse[fin], rlse[fin], rtol=1e-4, atol=1e-4)
+    assert np.isneginf(lse[~fin]).all()
+
+
+def _q_log_uniform(r, shape, lo, hi):
+    """bf16 values with random signs and magnitudes 2^u, u uniform in [lo, hi]."""
+    mag = np.exp2(r.uniform(lo, hi, size=shape))
+    sgn = np.where(r.random(shape) < 0.5, -1.0, 1.0)
+    return synth.bf16_bits_from_f32((sgn * mag).astype(np.float32))
+
+
+SHAPES = [(5, 64, 512, 512, 128), (6, 8, 128, 64, 32)]   # tensor-core kernel; general-shape kernel
+
+
+@pytest.mark.parametrize("B,Hq,d,k,W", SHAPES)
+def test_attn_window_rows_full_range(B, Hq, d, k, W):
+    r = np.random.default_rng(600 + d)
+    c = _case(r, B, Hq, d, k, W, n=3000)
+    rows = c["swa"].shape[0]
+    c["swa"] = r.choice(_E4M3_FINITE, size=(rows, d))
+    c["swa_scale"] = np.exp2(r.uniform(-24, 7, size=rows)).astype(np.float32)
+    # queries 1 and 3 attend to their window only; query 3's window is quiet (every row
+    # scale in 2^-24 .. 2^-20), query 4's the loudest the range allows (2^6 .. 2^7)
+    for b in (1, 3):
+        c["tlen"][b] = 0
+        c["topk"][b] = -1
+    s3, s4 = int(c["swa_start"][3]), int(c["swa_start"][4])
+    c["swa_scale"][s3:s3 + W] = np.exp2(r.uniform(-24, -20, size=W))
+    c["swa_scale"][s4:s4 + W] = np.exp2(r.uniform(6, 7, size=W))
+    out, lse = _run(c)
+    ref, rlse = _oracle(c)
+    _assert_close_per_head(out, ref, "window rows")
+    _lse_close(lse, rlse)
+
+
+@pytest.mark.parametrize("B,Hq,d,k,W", SHAPES)
+def test_attn_fp4_scale_bytes_full_range(B, Hq, d, k, W):
+    r = np.random.default_rng(700 + d)
+    c = _case(r, B, Hq, d, k, W, n=3000)
+    for s in range(len(c["scales"])):
+        c["scales"][s] = r.integers(0, 0x7F, size=c["scales"][s].shape, dtype=np.uint8)   # 0x00..0x7E
+        c["scales"][s][::7] = 0                                                          # all-zero groups
+    # sequence 1's entries are all tiny (scale bytes 0x00..0x08: scales 0 .. 2^-6); its
+    # queries 1 and 3 see no window
+    c["scales"][1] = r.integers(0, 9, size=c["scales"][1].shape, dtype=np.uint8)
+    c["swa_len"][1] = 0
+    c["swa_len"][3] = 0
+    pt = c["cache"].page_table.cpu().numpy()
+    c["cache"].scales.copy_(to_dev(logical_to_paged(c["scales"], pt, c["cache"].num_pages, d // 16, np.uint8)))
+    out, lse = _run(c)
+    ref, rlse = _oracle(c)
+    _assert_close_per_head(out, ref, "FP4 scales")
+    _lse_close(lse, rlse)
+
+
+@pytest.mark.parametrize("B,Hq,d,k,W", SHAPES)
+def test_attn_q_full_range(B, Hq, d, k, W):
+    r = np.random.default_rng(800 + d)
+    c = _case(r, B, Hq, d, k, W, n=3000)
+    # query 0: every element's magnitude log-uniform in 2^-30 .. 2^15; query 1: each head
+    # scaled as a whole by 2^e, e uniform in -30 .. 15; query 2: tiny heads only
+    # (2^-30 .. 2^-20); query 3: beyond the fp16 range (2^16 .. 2^40)
+    c["q"][0] = _q_log_uniform(r, (Hq, d), -30, 15)
+    base = formats.bf16_value(synth.bf16_normal(r, (Hq, d)))
+    e = r.uniform(-30, 15, size=(Hq, 1))
+    c["q"][1] = synth.bf16_bits_from_f32((base * np.exp2(np.floor(e))).astype(np.float32))
+    c["q"][2] = _q_log_uniform(r, (Hq, d), -30, -20)
+    c["q"][3] = _q_log_uniform(r, (Hq, d), 16, 40)
+    out, lse = _run(c)
+    ref, rlse = _oracle(c)
+    _assert_close_per_head(out, ref, "Q range")
+    _lse_close(lse, rlse)
