@@ -47,13 +47,26 @@ class AttnArgs(ctypes.Structure):
                 ("out", c_vp), ("out_dtype", c_i32), ("lse", c_vp)]
 
 
+class AppendArgs(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_size_t), ("B", c_i32), ("m", c_i32), ("d_model", c_i32),
+                ("h_dtype", c_i32), ("H", c_vp), ("W_kv", c_vp), ("W_z", c_vp), ("d_rope", c_i32),
+                ("rope_max_pos", c_i32), ("rope_cos", c_vp), ("rope_sin", c_vp), ("seq", c_vp), ("tok_pos", c_vp),
+                ("pend", c_vp), ("W_ik", c_vp), ("cache", Cache), ("y_out", c_vp)]
+
+
+class SwaQuantArgs(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_size_t), ("R", c_i32), ("d", c_i32), ("x_dtype", c_i32), ("x", c_vp),
+                ("row_idx", c_vp), ("swa", c_vp), ("swa_scale", c_vp), ("swa_rows", c_i32)]
+
+
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_WORKSPACE_TOO_SMALL",
           4: "ERR_CUDA", 5: "ERR_DEVICE_CHECK"}
 
 EXPORTS = ["csa2_compress_quant", "csa2_compress_quant_workspace", "csa2_index_full",
            "csa2_index_full_workspace", "csa2_index_reindex", "csa2_index_reindex_workspace",
            "csa2_sparse_attn", "csa2_sparse_attn_workspace", "csa2_last_error_message",
-           "csa2_get_device_error", "csa2_version", "csa2_index_full_noalloc", "csa2_selftest_wait_timeout"]
+           "csa2_get_device_error", "csa2_version", "csa2_index_full_noalloc", "csa2_selftest_wait_timeout",
+           "csa2_swa_quant", "csa2_compress_append", "csa2_compress_append_workspace"]
 
 _lib = None
 
@@ -73,7 +86,8 @@ def lib():
         raise ImportError(f"{LIB_PATH} is missing: build it with "
                           "`python -m fp4_compressed_sparse_02_gb300.build` (needs nvcc)")
     L = ctypes.CDLL(LIB_PATH)
-    pairs = [("csa2_compress_quant", CompressArgs), ("csa2_index_full", IndexFullArgs),
+    pairs = [("csa2_compress_quant", CompressArgs), ("csa2_compress_append", AppendArgs),
+             ("csa2_index_full", IndexFullArgs),
              ("csa2_index_reindex", IndexReindexArgs), ("csa2_sparse_attn", AttnArgs)]
     for name, st in pairs:
         f = getattr(L, name)
@@ -82,6 +96,8 @@ def lib():
         g = getattr(L, name + "_workspace")
         g.argtypes = [ctypes.POINTER(st), ctypes.POINTER(ctypes.c_size_t)]
         g.restype = c_i32
+    L.csa2_swa_quant.argtypes = [ctypes.POINTER(SwaQuantArgs), c_vp]
+    L.csa2_swa_quant.restype = c_i32
     L.csa2_index_full_noalloc.argtypes = [ctypes.POINTER(IndexFullArgs), c_vp]
     L.csa2_index_full_noalloc.restype = c_i32
     L.csa2_last_error_message.argtypes = []

@@ -158,6 +158,31 @@ def compress_quant(cache: PagedCache, seq, entry, *, m=1, C=None, Z=None, H=None
     _call("csa2_compress_quant", a, ws, cache.codes.device)
 
 
+def compress_append(cache: PagedCache, H, seq, tok_pos, W_kv, *, m=1, W_z=None, pend=None, rope_cos=None,
+                    rope_sin=None, W_ik=None, y_out=None, ws=None):
+    """The decode-time append: H [B, d_model] (bf16 or float32) holds one new token of each
+    of B distinct sequences seq[b] at position tok_pos[b].  At m > 1 a token that does not
+    complete its group waits in pend (float32 [num_seqs, 2, m, d], kept by the caller
+    between calls); the completing token writes entry tok_pos // m."""
+    B, d_model = H.shape
+    _expect(H, _B16 + _F32, "H")
+    _expect(pend, _F32, "pend")
+    for t, n in [(seq, "seq"), (tok_pos, "tok_pos")]:
+        _expect(t, _I32, n)
+    a = _lib.AppendArgs()
+    a.struct_size = ctypes.sizeof(_lib.AppendArgs)
+    a.B, a.m, a.d_model = B, m, d_model
+    a.h_dtype = F32 if H.dtype == torch.float32 else BF16
+    a.H, a.W_kv, a.W_z = _ptr(H), _ptr(W_kv), _ptr(W_z)
+    a.d_rope = 0 if rope_cos is None else rope_cos.shape[1] * 2
+    a.rope_max_pos = rope_cos.shape[0] if rope_cos is not None else 0
+    a.rope_cos, a.rope_sin = _ptr(rope_cos), _ptr(rope_sin)
+    a.seq, a.tok_pos, a.pend, a.W_ik = _ptr(seq), _ptr(tok_pos), _ptr(pend), _ptr(W_ik)
+    a.cache = cache.c_struct()
+    a.y_out = _ptr(y_out)
+    _call("csa2_compress_append", a, ws, cache.codes.device)
+
+
 def index_full(cache: PagedCache, q_idx, w, seq_of, n_vis, max_n, num_blocks=2048, per_block=8, k=512,
                relu=True, out=None, ws=None, group=1):
     """Full-mode indexer.  q_idx bf16 [B, H_i, d_ik], w float32 [B, H_i], seq_of / n_vis
@@ -234,6 +259,24 @@ def sparse_attn(cache: PagedCache, q, seq_of, topk, topk_len, swa, swa_scale, sw
     a.lse = _ptr(lse)
     _call("csa2_sparse_attn", a, ws, dev)
     return out, lse
+
+
+def swa_quant(x, swa, swa_scale, row_idx=None):
+    """FP8 window rows (a bounded replay's rebuilt SWA window): each row of x (bf16 or
+    float32 [R, d]) becomes E4M3 bytes with one float32 scale amax/448, written to
+    swa[row_idx[r]] / swa_scale[row_idx[r]] (row r when row_idx is None)."""
+    R, d = x.shape
+    _expect(x, _B16 + _F32, "x")
+    _expect(swa, _U8, "swa")
+    _expect(swa_scale, _F32, "swa_scale")
+    _expect(row_idx, _I32, "row_idx")
+    a = _lib.SwaQuantArgs()
+    a.struct_size = ctypes.sizeof(_lib.SwaQuantArgs)
+    a.R, a.d = R, d
+    a.x_dtype = F32 if x.dtype == torch.float32 else BF16
+    a.x, a.row_idx, a.swa, a.swa_scale = _ptr(x), _ptr(row_idx), _ptr(swa), _ptr(swa_scale)
+    a.swa_rows = swa.shape[0]
+    _lib.check(_lib.lib().csa2_swa_quant(ctypes.byref(a), _stream()))
 
 
 def device_error():

@@ -88,6 +88,31 @@ csa2_status check_compress(const csa2_compress_args* a) {
   return CSA2_OK;
 }
 
+csa2_status check_append(const csa2_append_args* a) {
+  REQUIRE(a, CSA2_ERR_INVALID_ARG, "args is NULL");
+  REQUIRE(a->struct_size == sizeof(csa2_append_args), CSA2_ERR_INVALID_ARG, "struct_size mismatch");
+  REQUIRE(a->B >= 0, CSA2_ERR_INVALID_ARG, "B < 0");
+  REQUIRE(a->m >= 1 && a->m <= 8, CSA2_ERR_UNSUPPORTED_SHAPE, "m must be in 1..8 (got %d)", a->m);
+  csa2_status s = check_cache(a->cache, true, a->W_ik != nullptr);
+  if (s != CSA2_OK) return s;
+  REQUIRE(a->h_dtype == CSA2_BF16 || a->h_dtype == CSA2_F32, CSA2_ERR_INVALID_ARG, "bad h_dtype");
+  REQUIRE(a->d_model > 0 && a->d_model % 32 == 0, CSA2_ERR_UNSUPPORTED_SHAPE,
+          "d_model must be a positive multiple of 32 (got %d)", a->d_model);
+  REQUIRE(a->d_rope == 0 || a->d_rope == 32 || a->d_rope == 64, CSA2_ERR_UNSUPPORTED_SHAPE,
+          "d_rope must be 0, 32 or 64 (got %d)", a->d_rope);
+  REQUIRE(a->d_rope <= a->cache.d, CSA2_ERR_UNSUPPORTED_SHAPE, "d_rope > d");
+  if (a->B > 0) {
+    REQUIRE(a->H && a->W_kv && a->seq && a->tok_pos, CSA2_ERR_INVALID_ARG, "H/W_kv/seq/tok_pos is NULL");
+    REQUIRE(a->m == 1 || (a->W_z && a->pend), CSA2_ERR_INVALID_ARG, "W_z and pend are required when m > 1");
+    if (a->d_rope)
+      REQUIRE(a->rope_cos && a->rope_sin && a->rope_max_pos > 0, CSA2_ERR_INVALID_ARG,
+              "RoPE tables are NULL or rope_max_pos <= 0");
+    REQUIRE(((uintptr_t)a->H & 15) == 0 && ((uintptr_t)a->W_kv & 15) == 0 && ((uintptr_t)a->W_z & 15) == 0,
+            CSA2_ERR_INVALID_ARG, "H, W_kv and W_z must be 16-byte aligned");
+  }
+  return CSA2_OK;
+}
+
 csa2_status check_index_common(int B, int H_i, const uint16_t* q, const float* w, const csa2_cache& c,
                                const int32_t* seq_of, int k, int* topk, int* topk_len) {
   REQUIRE(B >= 0, CSA2_ERR_INVALID_ARG, "B < 0");
@@ -151,6 +176,23 @@ csa2_status check_attn(const csa2_attn_args* a) {
   return CSA2_OK;
 }
 
+csa2_status check_swa_quant(const csa2_swa_quant_args* a) {
+  REQUIRE(a, CSA2_ERR_INVALID_ARG, "args is NULL");
+  REQUIRE(a->struct_size == sizeof(csa2_swa_quant_args), CSA2_ERR_INVALID_ARG, "struct_size mismatch");
+  REQUIRE(a->R >= 0, CSA2_ERR_INVALID_ARG, "R < 0");
+  REQUIRE(a->d == 128 || a->d == 512, CSA2_ERR_UNSUPPORTED_SHAPE, "d must be 128 or 512 (got %d)", a->d);
+  REQUIRE(a->x_dtype == CSA2_BF16 || a->x_dtype == CSA2_F32, CSA2_ERR_INVALID_ARG, "bad x_dtype");
+  if (a->R > 0) {
+    REQUIRE(a->x && a->swa && a->swa_scale, CSA2_ERR_INVALID_ARG, "x/swa/swa_scale is NULL");
+    REQUIRE(a->swa_rows > 0, CSA2_ERR_INVALID_ARG, "swa_rows must be positive");
+    REQUIRE(a->row_idx || a->R <= a->swa_rows, CSA2_ERR_INVALID_ARG, "R > swa_rows without row_idx");
+    REQUIRE(((uintptr_t)a->x & 15) == 0, CSA2_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    REQUIRE(((uintptr_t)a->swa & (a->d == 512 ? 15 : 3)) == 0, CSA2_ERR_INVALID_ARG,
+            "swa must be 16-byte (d = 512) or 4-byte (d = 128) aligned");
+  }
+  return CSA2_OK;
+}
+
 csa2_status check_ws(size_t need, void* ws, size_t have) {
   REQUIRE(have >= need, CSA2_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need, have);
   REQUIRE(need == 0 || ws, CSA2_ERR_INVALID_ARG, "workspace is NULL");
@@ -176,6 +218,22 @@ csa2_status csa2_compress_quant(const csa2_compress_args* a, void* ws, size_t ws
   if (s != CSA2_OK) return s;
   if (a->T == 0) return ok();
   return cuda_status(csa2::launch_compress(*a, ws, static_cast<cudaStream_t>(stream)), "csa2_compress_quant");
+}
+
+csa2_status csa2_compress_append_workspace(const csa2_append_args* a, size_t* bytes) {
+  csa2_status s = check_append(a);
+  if (s != CSA2_OK) return s;
+  REQUIRE(bytes, CSA2_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = csa2::append_workspace_bytes(*a);
+  return ok();
+}
+
+csa2_status csa2_compress_append(const csa2_append_args* a, void* ws, size_t ws_bytes, void* stream) {
+  csa2_status s = check_append(a);
+  if (s != CSA2_OK) return s;
+  s = check_ws(csa2::append_workspace_bytes(*a), ws, ws_bytes);
+  if (s != CSA2_OK) return s;
+  return cuda_status(csa2::launch_append(*a, ws, static_cast<cudaStream_t>(stream)), "csa2_compress_append");
 }
 
 csa2_status csa2_index_full_workspace(const csa2_index_full_args* a, size_t* bytes) {
@@ -240,6 +298,12 @@ csa2_status csa2_sparse_attn(const csa2_attn_args* a, void* ws, size_t ws_bytes,
   s = check_ws(csa2::attn_workspace_bytes(*a), ws, ws_bytes);
   if (s != CSA2_OK) return s;
   return cuda_status(csa2::launch_attn(*a, ws, static_cast<cudaStream_t>(stream)), "csa2_sparse_attn");
+}
+
+csa2_status csa2_swa_quant(const csa2_swa_quant_args* a, void* stream) {
+  csa2_status s = check_swa_quant(a);
+  if (s != CSA2_OK) return s;
+  return cuda_status(csa2::launch_swa_quant(*a, static_cast<cudaStream_t>(stream)), "csa2_swa_quant");
 }
 
 const char* csa2_last_error_message(void) { return g_msg; }

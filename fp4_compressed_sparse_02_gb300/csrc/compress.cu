@@ -275,9 +275,11 @@ __device__ __forceinline__ void load16_sum(const float* p, long long stride, int
   }
 }
 
-// Group q (16 channels) of entry g: pooled row, RoPE, FP4 codes and scale into the cache;
-// with deq, also the dequantised values (code x scale, float32) into deq[16 q ..].
-__device__ __forceinline__ void quant_group(const QuantParams& p, long long g, int q, float* deq) {
+// Group q (16 channels) of entry g: pooled row, RoPE at position ps, FP4 codes and scale into
+// entry en of sequence sq; with deq, also the dequantised values (code x scale, float32) into
+// deq[16 q ..].
+__device__ __forceinline__ void quant_group_at(const QuantParams& p, long long g, int q, float* deq, int ps, int sq,
+                                               int en) {
   const int c0 = q * 16;
   float y[16];
   if (p.m == 1) {
@@ -310,7 +312,6 @@ __device__ __forceinline__ void quant_group(const QuantParams& p, long long g, i
   // RoPE on channels [d - d_rope, d): pairs (2i, 2i+1) of that slice
   const int rb = p.d - p.d_rope;
   if (p.d_rope > 0 && c0 >= rb) {
-    int ps = __ldg(p.pos + g);
     if (ps < 0 || ps >= p.rope_max_pos) {
       raise_error(&g_err_compress, CSA2_DEVERR_POS);
     } else {
@@ -339,11 +340,16 @@ __device__ __forceinline__ void quant_group(const QuantParams& p, long long g, i
       deq[c0 + 2 * i + 1] = __high2float(hv) * sc;
     }
   }
-  long long row = entry_row(p.cache, __ldg(p.seq + g), __ldg(p.entry + g), &g_err_compress);
+  long long row = entry_row(p.cache, sq, en, &g_err_compress);
   if (row < 0) return;
   uint2* cd = reinterpret_cast<uint2*>(p.cache.codes + row * (p.d / 2) + q * 8);
   *cd = make_uint2(w0, w1);
   p.cache.scales[row * (p.d / 16) + q] = (uint8_t)sbyte;
+}
+
+__device__ __forceinline__ void quant_group(const QuantParams& p, long long g, int q, float* deq) {
+  const int ps = (p.d_rope > 0 && q * 16 >= p.d - p.d_rope) ? __ldg(p.pos + g) : 0;
+  quant_group_at(p, g, q, deq, ps, __ldg(p.seq + g), __ldg(p.entry + g));
 }
 
 __global__ void __launch_bounds__(256) k_quant(QuantParams p) {
@@ -483,6 +489,68 @@ static cudaError_t launch_quant_index_k(const QuantParams& qp, const uint16_t* W
   return launch_k(k_quant_index_k<DIK>, (unsigned)qp.G, 256, sm, st, qp, Wik);
 }
 
+// ---------------------------------------------------------------------------------
+// The decode-time append at compression ratio m: one new token per CTA.  The token's C and
+// Z rows (the summed projection partials) go to slot t % m of its sequence's pending group
+// (pend[s]: C rows [m][d], then Z rows [m][d]); the token that completes the group (t % m
+// == m - 1) then pools the group's m rows, applies RoPE at its own position t, quantises
+// and writes entry t / m, and projects its indexer K.  At m = 1 every token completes its
+// group and reads its row straight from the partials.
+// ---------------------------------------------------------------------------------
+struct AppendParams {
+  QuantParams q;                                 // partials of the B tokens, RoPE, cache
+  const int* tok_pos;
+  float* pend;                                   // [num_seqs][2][m][d] (m > 1)
+  float* y_out;                                  // [B][d] or null
+};
+
+template <int DIK>
+__global__ void __launch_bounds__(256) k_append_quant_index_k(AppendParams ap, const uint16_t* __restrict__ Wik) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float qk_sm[];
+  float* deq = qk_sm;                            // [d]
+  float* part = qk_sm + ap.q.d;                  // [8][DIK]
+  __shared__ long long rows[1];
+  const int b = blockIdx.x, tid = threadIdx.x, d = ap.q.d, m = ap.q.m;
+  const int s = __ldg(ap.q.seq + b), t = __ldg(ap.tok_pos + b);
+  if (s < 0 || s >= ap.q.cache.num_seqs || t < 0) {           // the same for the whole CTA
+    if (tid == 0) raise_error(&g_err_compress, t < 0 ? CSA2_DEVERR_POS : CSA2_DEVERR_SEQ);
+    return;
+  }
+  const int j = t % m, g = t / m;
+  QuantParams qp = ap.q;
+  qp.y_out = ap.y_out ? ap.y_out + (long long)b * d : nullptr;
+  if (m == 1) {
+    qp.Cp = ap.q.Cp + (long long)b * ap.q.ldc;   // this token's partials (group 0 below)
+  } else {
+    float* grp = ap.pend + (long long)s * 2 * m * d;
+    for (int i = tid; i < d; i += blockDim.x) {
+      const float* cp = ap.q.Cp + (long long)b * ap.q.ldc + i;
+      const float* zp = ap.q.Zp + (long long)b * ap.q.ldc + i;
+      float c = cp[0], z = zp[0];
+      for (int k = 1; k < ap.q.nsplit; ++k) {
+        c += cp[k * ap.q.split_stride];
+        z += zp[k * ap.q.split_stride];
+      }
+      grp[(long long)j * d + i] = c;
+      grp[(long long)(m + j) * d + i] = z;
+    }
+    if (j < m - 1) return;                       // the group is not complete yet
+    __syncthreads();                             // the group's rows, written by this CTA, are visible
+    qp.Cp = grp;
+    qp.Zp = grp + (long long)m * d;
+    qp.split_stride = 0;
+    qp.nsplit = 1;
+    qp.ldc = d;
+  }
+  if (tid < d / 16) quant_group_at(qp, 0, tid, Wik ? deq : nullptr, t, s, g);
+  if (Wik == nullptr) return;
+  if (tid == 0) rows[0] = entry_row(qp.cache, s, g, &g_err_compress);
+  __syncthreads();
+  index_k_product<1, DIK>(qp.cache, rows, deq, part, Wik);
+}
+
 template <int E, int DIK>
 static cudaError_t launch_index_k(const csa2_compress_args& a, int G, cudaStream_t st) {
   const size_t sm = ((size_t)E * a.cache.d + 8 * E * DIK) * sizeof(float);
@@ -532,14 +600,72 @@ static cudaError_t launch_index_k_any(const csa2_compress_args& a, int G, cudaSt
   return a.cache.d_ik == 128 ? launch_index_k<8, 128>(a, G, st) : launch_index_k<8, 64>(a, G, st);
 }
 
-size_t compress_workspace_bytes(const csa2_compress_args& a) {
-  if (!a.W_kv) return 0;
+// bytes of the unfused projection's output (its split-K partials)
+static size_t project_ws_bytes(const csa2_compress_args& a) {
   int N = a.cache.d * (a.m > 1 ? 2 : 1);
-  if (project_tc_fused(a)) return 0;
   if (project_tc_supported(a)) return (size_t)a.T * N * sizeof(float);
   int s = !use_small(a) ? pick_splits(a.T, a.d_model, N)
           : (a.h_dtype == CSA2_BF16 ? mma_splits(a.d_model, N) : small_splits(a.T, a.d_model, N));
   return (size_t)s * a.T * N * sizeof(float);
+}
+
+size_t compress_workspace_bytes(const csa2_compress_args& a) {
+  if (!a.W_kv) return 0;
+  if (project_tc_fused(a)) return 0;
+  return project_ws_bytes(a);
+}
+
+// C|Z = H.[W_kv|W_z] of the a.T rows into `out` (float32 split-K partials, no pooling); sets
+// the partial layout of qp.
+static cudaError_t project_rows(const csa2_compress_args& a, float* out, cudaStream_t st, QuantParams& qp) {
+  const int d = a.cache.d;
+  int N = d * (a.m > 1 ? 2 : 1);
+  int s;
+  if (project_tc_supported(a)) {
+    s = 1;
+    cudaError_t e = launch_project_tc(a, out, false, st);
+    if (e != cudaSuccess) return e;
+  } else if (use_small(a) && a.h_dtype == CSA2_BF16) {
+    s = mma_splits(a.d_model, N);
+    const int ks = a.d_model / s;
+    const size_t sm = (size_t)64 * (ks * 2 + 16) + (size_t)ks * 144;
+    cudaError_t e = cudaFuncSetAttribute(k_project_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    launch_k(k_project_mma, dim3(N / 64, s), 128, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z, out, a.T,
+                                                    a.d_model, d, N, ks);
+  } else if (use_small(a)) {
+    s = small_splits(a.T, a.d_model, N);
+    const int ks = a.d_model / s;
+    const size_t sm = (size_t)ks * (128 + 4 * a.T);
+    cudaError_t e;
+    if (a.h_dtype == CSA2_F32) {
+      e = cudaFuncSetAttribute(k_project_small<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      if (e != cudaSuccess) return e;
+      launch_k(k_project_small<float>, dim3(N / 64, s), 256, sm, st, static_cast<const float*>(a.H), a.W_kv, a.W_z,
+                                                               out, a.T, a.d_model, d, N, ks);
+    } else {
+      e = cudaFuncSetAttribute(k_project_small<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      if (e != cudaSuccess) return e;
+      launch_k(k_project_small<uint16_t>, dim3(N / 64, s), 256, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv,
+                                                                  a.W_z, out, a.T, a.d_model, d, N, ks);
+    }
+  } else {
+    s = pick_splits(a.T, a.d_model, N);
+    int kps = ((a.d_model / s + PBK - 1) / PBK) * PBK;
+  dim3 grid(N / PBN, (a.T + PBM - 1) / PBM, s);
+  if (a.h_dtype == CSA2_F32)
+    launch_k(k_project<float>, grid, 256, 0, st, static_cast<const float*>(a.H), a.W_kv, a.W_z, out,
+                                           a.T, a.d_model, d, N, kps);
+  else
+    launch_k(k_project<uint16_t>, grid, 256, 0, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z,
+                                              out, a.T, a.d_model, d, N, kps);
+  }
+  qp.Cp = out;
+  qp.Zp = out + d;
+  qp.split_stride = (long long)a.T * N;
+  qp.nsplit = s;
+  qp.ldc = N;
+  return cudaGetLastError();
 }
 
 cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t st) {
@@ -547,59 +673,14 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   const int G = a.T / a.m;
   QuantParams qp{};
   if (a.W_kv) {
-    int N = d * (a.m > 1 ? 2 : 1);
-    float* out = static_cast<float*>(ws);
-    int s;
     if (project_tc_fused(a)) {
       // projection, pooling, RoPE and FP4 in one kernel; then the indexer K
       cudaError_t e = launch_project_tc(a, nullptr, true, st);
       if (e != cudaSuccess) return e;
       return launch_index_k_any(a, G, st);
     }
-    if (project_tc_supported(a)) {
-      s = 1;
-      cudaError_t e = launch_project_tc(a, out, false, st);
-      if (e != cudaSuccess) return e;
-    } else if (use_small(a) && a.h_dtype == CSA2_BF16) {
-      s = mma_splits(a.d_model, N);
-      const int ks = a.d_model / s;
-      const size_t sm = (size_t)64 * (ks * 2 + 16) + (size_t)ks * 144;
-      cudaError_t e = cudaFuncSetAttribute(k_project_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      if (e != cudaSuccess) return e;
-      launch_k(k_project_mma, dim3(N / 64, s), 128, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z, out, a.T,
-                                                      a.d_model, d, N, ks);
-    } else if (use_small(a)) {
-      s = small_splits(a.T, a.d_model, N);
-      const int ks = a.d_model / s;
-      const size_t sm = (size_t)ks * (128 + 4 * a.T);
-      cudaError_t e;
-      if (a.h_dtype == CSA2_F32) {
-        e = cudaFuncSetAttribute(k_project_small<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-        launch_k(k_project_small<float>, dim3(N / 64, s), 256, sm, st, static_cast<const float*>(a.H), a.W_kv, a.W_z,
-                                                                 out, a.T, a.d_model, d, N, ks);
-      } else {
-        e = cudaFuncSetAttribute(k_project_small<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-        launch_k(k_project_small<uint16_t>, dim3(N / 64, s), 256, sm, st, static_cast<const uint16_t*>(a.H), a.W_kv,
-                                                                    a.W_z, out, a.T, a.d_model, d, N, ks);
-      }
-    } else {
-    s = pick_splits(a.T, a.d_model, N);
-    int kps = ((a.d_model / s + PBK - 1) / PBK) * PBK;
-    dim3 grid(N / PBN, (a.T + PBM - 1) / PBM, s);
-    if (a.h_dtype == CSA2_F32)
-      launch_k(k_project<float>, grid, 256, 0, st, static_cast<const float*>(a.H), a.W_kv, a.W_z, out,
-                                             a.T, a.d_model, d, N, kps);
-    else
-      launch_k(k_project<uint16_t>, grid, 256, 0, st, static_cast<const uint16_t*>(a.H), a.W_kv, a.W_z,
-                                                out, a.T, a.d_model, d, N, kps);
-    }
-    qp.Cp = out;
-    qp.Zp = out + d;
-    qp.split_stride = (long long)a.T * N;
-    qp.nsplit = s;
-    qp.ldc = N;
+    cudaError_t e = project_rows(a, static_cast<float*>(ws), st, qp);
+    if (e != cudaSuccess) return e;
   } else {
     qp.Cp = a.C;
     qp.Zp = a.Z;
@@ -631,6 +712,132 @@ cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t 
   cudaError_t e = launch_index_k_any(a, G, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------
+// FP8 rows with one float32 scale per row (the SWA window rows a bounded replay rebuilds):
+// s = amax / 448, byte = E4M3_RNE_satfinite(x / s), float32 divisions.  One warp per row,
+// lane l holding the row's elements [l d/32, (l + 1) d/32).
+// ---------------------------------------------------------------------------------
+template <int D, typename XT>
+__global__ void __launch_bounds__(256) k_swa_quant(const XT* __restrict__ x, const int* __restrict__ row_idx, int R,
+                                                   uint8_t* __restrict__ swa, float* __restrict__ swa_scale,
+                                                   int swa_rows) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int PL = D / 32;                     // elements per lane: 16 (d = 512) or 4 (d = 128)
+  const int lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= R) return;
+  float v[PL];
+  const XT* xp = x + r * D + lane * PL;
+  if constexpr (sizeof(XT) == 4) {
+#pragma unroll
+    for (int i = 0; i < PL / 4; ++i) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(xp) + i);
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PL / 4; ++i) {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(xp) + i);
+      v[4 * i] = __uint_as_float(u.x << 16); v[4 * i + 1] = __uint_as_float(u.x & 0xffff0000u);
+      v[4 * i + 2] = __uint_as_float(u.y << 16); v[4 * i + 3] = __uint_as_float(u.y & 0xffff0000u);
+    }
+  }
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < PL; ++i) a = fmaxf(a, fabsf(v[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float sc = __fdiv_rn(a, 448.0f);
+  uint32_t w[PL / 4];
+#pragma unroll
+  for (int i = 0; i < PL / 4; ++i) {
+    w[i] = 0u;
+    if (sc > 0.f)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) w[i] |= cvt_e4m3(__fdiv_rn(v[4 * i + j], sc)) << (8 * j);
+  }
+  const long long dst = row_idx ? (long long)__ldg(row_idx + r) : r;
+  if (dst < 0 || dst >= swa_rows) {
+    if (lane == 0) raise_error(&g_err_compress, CSA2_DEVERR_SWA_RANGE);
+    return;
+  }
+  uint8_t* o = swa + dst * D + lane * PL;
+  if constexpr (PL == 16) {
+    *reinterpret_cast<uint4*>(o) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    *reinterpret_cast<uint32_t*>(o) = w[0];
+  }
+  if (lane == 0) swa_scale[dst] = sc;
+}
+
+cudaError_t launch_swa_quant(const csa2_swa_quant_args& a, cudaStream_t st) {
+  if (a.R == 0) return cudaSuccess;
+  const unsigned grid = (unsigned)((a.R + 7) / 8);
+  if (a.d == 512) {
+    if (a.x_dtype == CSA2_F32)
+      return launch_k(k_swa_quant<512, float>, grid, 256, 0, st, static_cast<const float*>(a.x), a.row_idx, a.R,
+                      a.swa, a.swa_scale, a.swa_rows);
+    return launch_k(k_swa_quant<512, uint16_t>, grid, 256, 0, st, static_cast<const uint16_t*>(a.x), a.row_idx, a.R,
+                    a.swa, a.swa_scale, a.swa_rows);
+  }
+  if (a.x_dtype == CSA2_F32)
+    return launch_k(k_swa_quant<128, float>, grid, 256, 0, st, static_cast<const float*>(a.x), a.row_idx, a.R,
+                    a.swa, a.swa_scale, a.swa_rows);
+  return launch_k(k_swa_quant<128, uint16_t>, grid, 256, 0, st, static_cast<const uint16_t*>(a.x), a.row_idx, a.R,
+                  a.swa, a.swa_scale, a.swa_rows);
+}
+
+// ---------------------------------------------------------------------------------
+// The decode-time append (csa2_compress_append)
+// ---------------------------------------------------------------------------------
+static csa2_compress_args append_view(const csa2_append_args& a) {
+  csa2_compress_args c{};
+  c.struct_size = sizeof(c);
+  c.T = a.B;
+  c.m = a.m;
+  c.d_model = a.d_model;
+  c.h_dtype = a.h_dtype;
+  c.H = a.H;
+  c.W_kv = a.W_kv;
+  c.W_z = a.W_z;
+  c.d_rope = a.d_rope;
+  c.rope_max_pos = a.rope_max_pos;
+  c.rope_cos = a.rope_cos;
+  c.rope_sin = a.rope_sin;
+  c.seq = a.seq;
+  c.W_ik = a.W_ik;
+  c.cache = a.cache;
+  return c;
+}
+
+size_t append_workspace_bytes(const csa2_append_args& a) { return a.B > 0 ? project_ws_bytes(append_view(a)) : 0; }
+
+cudaError_t launch_append(const csa2_append_args& a, void* ws, cudaStream_t st) {
+  if (a.B == 0) return cudaSuccess;
+  const csa2_compress_args c = append_view(a);
+  AppendParams ap{};
+  cudaError_t e = project_rows(c, static_cast<float*>(ws), st, ap.q);
+  if (e != cudaSuccess) return e;
+  ap.q.G = a.B;
+  ap.q.m = a.m;
+  ap.q.d = a.cache.d;
+  ap.q.d_rope = a.d_rope;
+  ap.q.rope_max_pos = a.rope_max_pos;
+  ap.q.rope_cos = a.rope_cos;
+  ap.q.rope_sin = a.rope_sin;
+  ap.q.seq = a.seq;
+  ap.q.cache = a.cache;
+  ap.tok_pos = a.tok_pos;
+  ap.pend = a.pend;
+  ap.y_out = a.y_out;
+  if (a.W_ik && a.cache.d_ik == 64)
+    return launch_k(k_append_quant_index_k<64>, (unsigned)a.B, 256, ((size_t)a.cache.d + 8 * 64) * sizeof(float), st,
+                    ap, a.W_ik);
+  return launch_k(k_append_quant_index_k<128>, (unsigned)a.B, 256, ((size_t)a.cache.d + 8 * 128) * sizeof(float), st,
+                  ap, a.W_ik);
 }
 
 uint32_t read_clear_error_compress() {

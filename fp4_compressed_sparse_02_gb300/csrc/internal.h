@@ -13,6 +13,9 @@ namespace csa2 {
 size_t compress_workspace_bytes(const csa2_compress_args& a);
 cudaError_t launch_compress(const csa2_compress_args& a, void* ws, cudaStream_t st);
 uint32_t read_clear_error_compress();
+cudaError_t launch_swa_quant(const csa2_swa_quant_args& a, cudaStream_t st);
+size_t append_workspace_bytes(const csa2_append_args& a);
+cudaError_t launch_append(const csa2_append_args& a, void* ws, cudaStream_t st);
 
 // proj_tc.cu: tensor-core projection for many bf16 tokens (out[T][d or 2d], fp32)
 bool project_tc_supported(const csa2_compress_args& a);

@@ -133,6 +133,54 @@ csa2_status csa2_compress_quant(const csa2_compress_args* args, void* workspace,
 csa2_status csa2_compress_quant_workspace(const csa2_compress_args* args, size_t* bytes);
 
 /* ------------------------------------------------------------------------------
+ * csa2_compress_append -- the decode-time cache append: one new token for each of B
+ * sequences, at compression ratio m (deep dive 3.1: every m tokens become one Main KV
+ * entry -- the encoder's m = 2, the decoder's m = 1).
+ *
+ * An entry exists once all m of its tokens exist, so a token that does not complete its
+ * group waits: for the token at position t = tok_pos[b] of sequence s = seq[b],
+ *   C = H[b].W_kv and Z = H[b].W_z (float32) are stored as row t % m of the sequence's
+ *   pending group pend[s] (C rows [m][d], then Z rows [m][d]);
+ *   if t % m == m - 1 the group is complete: its m rows are pooled, rotated at position t
+ *   and quantised exactly as csa2_compress_quant does for m consecutive rows, written as
+ *   entry t / m of sequence s, and its indexer K projected (when W_ik != NULL).
+ * pend holds each sequence's waiting tokens between calls; the caller keeps it (no
+ * initialisation is needed: a group's rows are written before they are read, as long as
+ * every sequence's tokens are appended in order).  At m = 1 pend is not used.  The tokens
+ * of one call must belong to distinct sequences.  y_out (optional, [B][d] float32)
+ * receives the pre-quantisation row of each token that completes a group; the rows of
+ * the other tokens are left unchanged.
+ * Device checks: seq outside [0, cache.num_seqs) sets CSA2_DEVERR_SEQ, a negative tok_pos
+ * CSA2_DEVERR_POS, and that token is skipped.
+ * Supported: as csa2_compress_quant's projection mode (m in 1..8, d in {128, 512},
+ * d_model % 32 == 0, bf16 or f32 H).
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_append_args {
+  size_t struct_size;
+  int32_t B;                   /* new tokens, each of a different sequence */
+  int32_t m;                   /* compression ratio */
+  int32_t d_model;
+  csa2_dtype h_dtype;
+  const void* H;               /* device [B][d_model] hidden state of each new token */
+  const uint16_t* W_kv;        /* device bf16 [d_model][d] */
+  const uint16_t* W_z;         /* device bf16 [d_model][d], required when m > 1 */
+  int32_t d_rope;              /* 0 disables RoPE */
+  int32_t rope_max_pos;
+  const float* rope_cos;       /* device f32 [rope_max_pos][d_rope/2] */
+  const float* rope_sin;
+  const int32_t* seq;          /* device [B] sequence of each token */
+  const int32_t* tok_pos;      /* device [B] position of each token in its sequence */
+  float* pend;                 /* device f32 [cache.num_seqs][2][m][d] (m > 1; NULL at m = 1) */
+  const uint16_t* W_ik;        /* device bf16 [d][d_ik], NULL = do not write idx_k */
+  csa2_cache cache;            /* destination planes */
+  float* y_out;                /* device f32 [B][d] or NULL */
+} csa2_append_args;
+
+csa2_status csa2_compress_append(const csa2_append_args* args, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+csa2_status csa2_compress_append_workspace(const csa2_append_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
  * csa2_index_full -- Full-mode hierarchical sparse indexer.
  * deep dive 3.3: the first Full indexer scans the whole causally visible range, keeps
  * the best positions of each block; 2,048 blocks x 8 = a 16,384-candidate shared pool;
@@ -300,6 +348,34 @@ typedef struct csa2_attn_args {
 csa2_status csa2_sparse_attn(const csa2_attn_args* args, void* workspace,
                              size_t workspace_bytes, void* stream);
 csa2_status csa2_sparse_attn_workspace(const csa2_attn_args* args, size_t* bytes);
+
+/* ------------------------------------------------------------------------------
+ * csa2_swa_quant -- FP8 window rows with one float32 scale per row: the step that
+ * rebuilds a layer's SWA window when its last tokens are replayed (deep dive 3.4, "SWA
+ * Bounded Replay": SWA KV stays FP8; the replayed tokens' window is recomputed rather
+ * than kept).  The replayed rows themselves (the layer's projections of those tokens'
+ * hidden states) are inputs.  For each input row r:
+ *   a = max_i |x[r][i]|;  s = a / 448 (float32 division, correctly rounded);
+ *   s == 0 -> every byte 0;  else byte_i = E4M3_RNE_satfinite(x[r][i] / s)  (float32
+ *   division);  swa[dst][i] = byte_i, swa_scale[dst] = s,  dst = row_idx[r] (or r).
+ * csa2_sparse_attn then attends over the rebuilt window (k = 0 for the window alone).
+ * A dst outside [0, swa_rows) sets CSA2_DEVERR_SWA_RANGE and that row is skipped.
+ * Supported: d in {128, 512}; x bf16 or f32, 16-byte aligned; swa 16-byte aligned
+ * (d = 512) or 4-byte aligned (d = 128).  Needs no workspace.
+ * -------------------------------------------------------------------------- */
+typedef struct csa2_swa_quant_args {
+  size_t struct_size;
+  int32_t R;                   /* rows to quantise */
+  int32_t d;                   /* row width */
+  csa2_dtype x_dtype;          /* CSA2_BF16 or CSA2_F32 */
+  const void* x;               /* device [R][d] */
+  const int32_t* row_idx;      /* device [R] destination row of each input row, or NULL = r */
+  uint8_t* swa;                /* device E4M3 [swa_rows][d] */
+  float* swa_scale;            /* device f32 [swa_rows] */
+  int32_t swa_rows;
+} csa2_swa_quant_args;
+
+csa2_status csa2_swa_quant(const csa2_swa_quant_args* args, void* stream);
 
 /* ------------------------------------------------------------------------------
  * Helpers

@@ -106,3 +106,28 @@ def compress_quant_from_hidden(H, W_kv, W_z, m, pos, cos_tab, sin_tab, d_rope, W
     C = project(H, W_kv)
     Z = project(H, W_z) if (m > 1 and W_z is not None) else None
     return compress_quant(C, Z, m, pos, cos_tab, sin_tab, d_rope, W_ik)
+
+
+def append_token(pending, h, t, W_kv, W_z, m, cos_tab, sin_tab, d_rope, W_ik=None):
+    """The decode-time append of one new token of a sequence at compression ratio m.
+
+    [deep-dive §3.1] every m tokens become one entry (encoder m = 2).  READING (C2): an
+    entry exists once all m of its tokens exist, so a token that does not complete its
+    group waits in the sequence's pending list; the token at position t with t % m == m - 1
+    completes group g = t // m, which is then compressed exactly as compress_quant does
+    for the m tokens together, at the RoPE position of the group's last token, t.
+
+    pending: the sequence's list of (C, Z) rows of its waiting tokens (updated in place).
+    h: the token's hidden state [d_model].  Returns None while the group is incomplete,
+    else (g, the compress_quant result of that one entry).
+    """
+    C = project(np.asarray(h)[None, :], W_kv)[0]
+    Z = project(np.asarray(h)[None, :], W_z)[0] if (m > 1 and W_z is not None) else None
+    assert len(pending) == t % m, "tokens of a sequence must arrive in order"
+    pending.append((C, Z))
+    if t % m != m - 1:
+        return None
+    Cg = np.stack([c for c, _ in pending])
+    Zg = np.stack([z for _, z in pending]) if m > 1 else None
+    pending.clear()
+    return t // m, compress_quant(Cg, Zg, m, np.array([t]), cos_tab, sin_tab, d_rope, W_ik)

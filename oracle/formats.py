@@ -185,3 +185,36 @@ def fp8_rows_dequantize(rows, row_scale):
     """SWA rows: E4M3 bytes times a per-row float32 scale (READING: one scale per
     row), exact in float64."""
     return e4m3_value(rows) * np.asarray(row_scale, dtype=np.float64)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# FP8 rows with one float32 scale per row: the SWA window rows, rebuilt here when a
+# window is replayed [deep-dive §3.4, "SWA Bounded Replay"], and the optional compressed
+# indexer-K plane.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0      # the largest finite E4M3 magnitude
+
+
+def fp8_rows_quantize(x):
+    """Quantise rows ``x[..., d]`` (float32 values; bf16 values are exact in float32) to
+    E4M3 bytes with one float32 scale per row.
+
+    READING (the pages say only that SWA KV stays FP8 [deep-dive §3.4]): the row's scale
+    maps its largest magnitude onto the largest E4M3 value, as the FP4 scale maps a
+    group's onto the largest E2M1 value:
+      a = max_i |x_i|                              (exact)
+      s = a / 448                                  (float32 division, correctly rounded)
+      s == 0 -> every byte 0
+      else   -> byte_i = E4M3_RNE_satfinite(x_i / s)   (float32 division)
+
+    Returns (bytes uint8[..., d], scales float32[...]).
+    """
+    x = np.asarray(x, dtype=np.float32)
+    a = np.max(np.abs(x), axis=-1)
+    s = (a / np.float32(E4M3_MAX)).astype(np.float32)          # float32 division
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = (x / s[..., None]).astype(np.float32)              # float32 division
+    b = e4m3_encode(np.where(s[..., None] > 0, q, np.float32(0.0)))
+    b = np.where(s[..., None] > 0, b, 0).astype(np.uint8)
+    return b, s

@@ -165,3 +165,76 @@ def test_empty_batches_need_no_pointers(L):
     assert _ws(L, "csa2_sparse_attn", _attn(k=0, topk=None))[0] == OK
     assert _ws(L, "csa2_sparse_attn", _attn(swa_max=0, swa=None, swa_scale=None, swa_start=None,
                                             swa_len=None))[0] == OK
+
+
+def _swaq(**kw):
+    a = _lib.SwaQuantArgs()
+    a.struct_size = ctypes.sizeof(a)
+    a.R, a.d, a.x_dtype, a.x, a.row_idx, a.swa, a.swa_scale, a.swa_rows = 4, 512, 0, P, 0, P, P, 16
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("change,status,msg", [
+    (dict(struct_size=8), INVALID, "struct_size"),
+    (dict(R=-1), INVALID, "R < 0"),
+    (dict(d=256), SHAPE, "d must be"),
+    (dict(x_dtype=7), INVALID, "x_dtype"),
+    (dict(x=0), INVALID, "NULL"),
+    (dict(swa_scale=0), INVALID, "NULL"),
+    (dict(swa_rows=0), INVALID, "swa_rows"),
+    (dict(R=17), INVALID, "R > swa_rows"),
+    (dict(x=U), INVALID, "x must be 16-byte aligned"),
+    (dict(swa=U), INVALID, "swa must be"),
+])
+def test_swa_quant_one_bad_field(L, change, status, msg):
+    a = _swaq(**change)
+    assert L.csa2_swa_quant(ctypes.byref(a), None) == status
+    assert msg in L.csa2_last_error_message().decode()
+
+
+def test_swa_quant_empty_needs_no_pointers(L):
+    a = _swaq(R=0, x=0, swa=0, swa_scale=0, swa_rows=0)
+    assert L.csa2_swa_quant(ctypes.byref(a), None) == OK
+
+
+def _append(**kw):
+    a = _lib.AppendArgs()
+    a.struct_size = ctypes.sizeof(a)
+    a.B, a.m, a.d_model, a.h_dtype = 4, 2, 512, 0
+    a.H, a.W_kv, a.W_z, a.seq, a.tok_pos, a.pend = P, P, P, P, P, P
+    a.cache = _cache()
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_append_valid_struct_passes(L):
+    n = ctypes.c_size_t(0)
+    assert L.csa2_compress_append_workspace(ctypes.byref(_append()), ctypes.byref(n)) == OK
+
+
+@pytest.mark.parametrize("change,status,msg", [
+    (dict(struct_size=8), INVALID, "struct_size"),
+    (dict(B=-1), INVALID, "B < 0"),
+    (dict(m=9), SHAPE, "m must be"),
+    (dict(d_model=100), SHAPE, "d_model"),
+    (dict(h_dtype=5), INVALID, "h_dtype"),
+    (dict(H=0), INVALID, "NULL"),
+    (dict(tok_pos=0), INVALID, "NULL"),
+    (dict(pend=0), INVALID, "pend"),
+    (dict(W_z=0), INVALID, "W_z"),
+    (dict(d_rope=16), SHAPE, "d_rope"),
+    (dict(d_rope=32, rope_cos=0), INVALID, "RoPE"),
+    (dict(H=U), INVALID, "16-byte aligned"),
+])
+def test_append_one_bad_field(L, change, status, msg):
+    n = ctypes.c_size_t(0)
+    assert L.csa2_compress_append_workspace(ctypes.byref(_append(**change)), ctypes.byref(n)) == status
+    assert msg in L.csa2_last_error_message().decode()
+
+
+def test_append_at_m1_needs_no_pending_buffer(L):
+    n = ctypes.c_size_t(0)
+    assert L.csa2_compress_append_workspace(ctypes.byref(_append(m=1, pend=0, W_z=0)), ctypes.byref(n)) == OK

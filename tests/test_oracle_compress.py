@@ -3,6 +3,7 @@ RoPE and the indexer-K projection, against closed forms and scalar loops."""
 import math
 
 import numpy as np
+import pytest
 
 from fp4_compressed_sparse_02_gb300 import synth
 from oracle import compress, formats
@@ -118,3 +119,32 @@ def test_compress_pipeline_order_rope_before_quant():
     np.testing.assert_array_equal(res["scales"], scales)
     unrot, _ = formats.fp4_quantize(C.astype(np.float32))
     assert not np.array_equal(unrot, codes)
+
+
+@pytest.mark.parametrize("m", [1, 2, 4])
+def test_append_token_by_token_equals_compressing_the_whole_sequence(m):
+    # buffering each token until its group completes, then compressing the group, must
+    # give the entries of compressing all tokens at once (entries of complete groups only)
+    r = np.random.default_rng(70 + m)
+    d_model, d, d_ik, T = 64, 128, 64, 11
+    H = r.standard_normal((T, d_model))
+    Wkv = r.standard_normal((d_model, d)) / 8
+    Wz = r.standard_normal((d_model, d)) / 8
+    Wik = r.standard_normal((d, d_ik)) / 11
+    cos, sin = synth.rope_tables(64, 32)
+    pending, got = [], {}
+    for t in range(T):
+        res = compress.append_token(pending, H[t], t, Wkv, Wz, m, cos, sin, 32, Wik)
+        if t % m != m - 1:
+            assert res is None
+        else:
+            got[res[0]] = res[1]
+    G = T // m
+    assert sorted(got) == list(range(G)) and len(pending) == T % m
+    pos = np.arange(G) * m + m - 1
+    ref = compress.compress_quant_from_hidden(H[:G * m], Wkv, Wz, m, pos, cos, sin, 32, Wik)
+    for g in range(G):
+        np.testing.assert_array_equal(got[g]["y"][0], ref["y"][g])
+        np.testing.assert_array_equal(got[g]["codes"][0], ref["codes"][g])
+        np.testing.assert_array_equal(got[g]["scales"][0], ref["scales"][g])
+        np.testing.assert_array_equal(got[g]["idx_k"][0], ref["idx_k"][g])

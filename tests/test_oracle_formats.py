@@ -163,3 +163,66 @@ def test_fp4_quantize_uses_float32_division(bad):
     s = np.float32(formats.e4m3_value(scales[0]))
     q = np.float32(bad) / s
     assert formats.fp4_unpack(codes)[1] == _e2m1_bruteforce(q)
+
+
+# ---- FP8 rows with one float32 scale per row -------------------------------------------
+
+def _fp8_rows_by_torch(x):
+    """The same row quantiser written with torch's own float32 arithmetic and its E4M3 cast
+    (torch rounds to nearest even; the quotients are clamped to the finite range first,
+    which is what satfinite does)."""
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32))
+    a = t.abs().amax(dim=-1)
+    s = a / torch.tensor(448.0, dtype=torch.float32)
+    q = torch.where(s[..., None] > 0, t / s[..., None], torch.zeros_like(t)).clamp(-448.0, 448.0)
+    return q.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), s.numpy()
+
+
+def test_fp8_rows_quantize_matches_torch_on_wide_rows():
+    r = np.random.default_rng(11)
+    x = r.standard_normal((300, 512)).astype(np.float32)
+    x *= np.exp2(r.integers(-30, 30, size=(300, 1))).astype(np.float32)     # rows over 60 octaves
+    x[::7] *= np.exp2(r.uniform(-20, 0, size=(43, 512))).astype(np.float32)  # within-row spread
+    got_b, got_s = formats.fp8_rows_quantize(x)
+    want_b, want_s = _fp8_rows_by_torch(x)
+    np.testing.assert_array_equal(got_s.view(np.uint32), want_s.view(np.uint32))
+    np.testing.assert_array_equal(got_b, want_b)
+
+
+def test_fp8_rows_largest_magnitude_maps_to_448():
+    r = np.random.default_rng(12)
+    x = (r.standard_normal((200, 128)) * np.exp2(r.integers(-40, 40, size=(200, 1)))).astype(np.float32)
+    b, s = formats.fp8_rows_quantize(x)
+    i = np.argmax(np.abs(x), axis=1)
+    top = b[np.arange(200), i]
+    assert ((top & 0x7F) == 0x7E).all()                          # +-448
+    assert (np.signbit(x[np.arange(200), i]) == ((top & 0x80) != 0)).all()
+
+
+def test_fp8_rows_roundtrip_of_representable_rows_is_identity():
+    # rows that are E4M3 values times a power of two, with a +-448 element: quantising
+    # gives back the same bytes and exactly that scale
+    r = np.random.default_rng(13)
+    finite = np.array([v for v in range(256) if (v & 0x7F) != 0x7F], dtype=np.uint8)
+    b0 = r.choice(finite, size=(64, 512))
+    b0[:, 5] = np.where(r.random(64) < 0.5, 0x7E, 0xFE)
+    s0 = np.exp2(r.integers(-20, 10, size=64)).astype(np.float32)
+    x = (formats.e4m3_value(b0) * s0[:, None]).astype(np.float32)
+    b, s = formats.fp8_rows_quantize(x)
+    np.testing.assert_array_equal(s, s0)
+    np.testing.assert_array_equal(formats.e4m3_value(b), formats.e4m3_value(b0))   # +-0 may swap sign bytes only
+
+
+def test_fp8_rows_error_bound_and_zero_rows():
+    r = np.random.default_rng(14)
+    x = r.standard_normal((50, 512)).astype(np.float32)
+    x[3] = 0.0
+    x[4] = -0.0
+    b, s = formats.fp8_rows_quantize(x)
+    assert s[3] == 0 and s[4] == 0 and (b[3] == 0).all() and (b[4] == 0).all()
+    deq = formats.fp8_rows_dequantize(b, s)
+    # |x - deq| <= s * (half the E4M3 gap at |x|/s): gap 2^(e-3) in [2^e, 2^(e+1)), 2^-9 below 2^-6
+    q = np.abs(x.astype(np.float64)) / np.where(s > 0, s, 1)[:, None]
+    e = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_gap = np.where(q < 2.0 ** -6, 2.0 ** -10, np.exp2(e - 4))
+    assert (np.abs(deq - x) <= s[:, None] * half_gap * (1 + 1e-6) + 1e-30).all()
