@@ -14,7 +14,8 @@ c_vp = ctypes.c_void_p
 class Cache(ctypes.Structure):
     _fields_ = [("codes", c_vp), ("scales", c_vp), ("idx_k", c_vp), ("page_table", c_vp),
                 ("num_pages", c_i32), ("page_size", c_i32), ("num_seqs", c_i32),
-                ("max_pages", c_i32), ("d", c_i32), ("d_ik", c_i32)]
+                ("max_pages", c_i32), ("d", c_i32), ("d_ik", c_i32), ("idx_k_dtype", c_i32), ("idx_k8", c_vp),
+                ("idx_k8_scale", c_vp)]
 
 
 class CompressArgs(ctypes.Structure):

@@ -15,7 +15,7 @@ import torch
 from . import _lib
 
 PAGE = 64
-BF16, F32 = 0, 1
+BF16, F32, FP8E4M3 = 0, 1, 2
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -46,11 +46,15 @@ def _stream():
 @dataclass
 class PagedCache:
     """Paged Main KV planes: codes uint8 [pages, 64, d/2], scales uint8 [pages, 64, d/16],
-    idx_k bf16 [pages, 64, d_ik] (optional), page_table int32 [seqs, max_pages]."""
+    page_table int32 [seqs, max_pages], and indexer K in one of two forms: idx_k bf16
+    [pages, 64, d_ik], or (compressed) idx_k8 uint8 E4M3 [pages, 64, d_ik] with
+    idx_k8_scale float32 [pages, 64].  The FP8 form is used when idx_k8 is set."""
     codes: torch.Tensor
     scales: torch.Tensor
     idx_k: Optional[torch.Tensor]
     page_table: torch.Tensor
+    idx_k8: Optional[torch.Tensor] = None
+    idx_k8_scale: Optional[torch.Tensor] = None
 
     @property
     def d(self):
@@ -58,6 +62,8 @@ class PagedCache:
 
     @property
     def d_ik(self):
+        if self.idx_k8 is not None:
+            return self.idx_k8.shape[-1]
         return self.idx_k.shape[-1] if self.idx_k is not None else 0
 
     @property
@@ -73,7 +79,7 @@ class PagedCache:
         return self.page_table.shape[1]
 
     @staticmethod
-    def allocate(num_seqs, entries_per_seq, d, d_ik, device, page_table=None):
+    def allocate(num_seqs, entries_per_seq, d, d_ik, device, page_table=None, idx_k_fp8=False):
         mp = (entries_per_seq + PAGE - 1) // PAGE
         npg = num_seqs * mp
         if page_table is None:
@@ -82,16 +88,24 @@ class PagedCache:
         npg = max(npg, int(page_table.max().item()) + 1) if page_table.numel() else npg
         codes = torch.zeros((npg, PAGE, d // 2), dtype=torch.uint8, device=device)
         scales = torch.zeros((npg, PAGE, d // 16), dtype=torch.uint8, device=device)
-        idx_k = torch.zeros((npg, PAGE, d_ik), dtype=torch.bfloat16, device=device) if d_ik else None
-        return PagedCache(codes, scales, idx_k, page_table)
+        idx_k = idx_k8 = idx_k8_scale = None
+        if d_ik and idx_k_fp8:
+            idx_k8 = torch.zeros((npg, PAGE, d_ik), dtype=torch.uint8, device=device)
+            idx_k8_scale = torch.zeros((npg, PAGE), dtype=torch.float32, device=device)
+        elif d_ik:
+            idx_k = torch.zeros((npg, PAGE, d_ik), dtype=torch.bfloat16, device=device)
+        return PagedCache(codes, scales, idx_k, page_table, idx_k8, idx_k8_scale)
 
     def c_struct(self):
-        for t, n in [(self.codes, "codes"), (self.scales, "scales")]:
+        for t, n in [(self.codes, "codes"), (self.scales, "scales"), (self.idx_k8, "idx_k8")]:
             _expect(t, _U8, n)
         _expect(self.idx_k, _B16, "idx_k")
+        _expect(self.idx_k8_scale, _F32, "idx_k8_scale")
         _expect(self.page_table, _I32, "page_table")
+        fp8 = self.idx_k8 is not None
         return _lib.Cache(_ptr(self.codes), _ptr(self.scales), _ptr(self.idx_k), _ptr(self.page_table),
-                          self.num_pages, PAGE, self.num_seqs, self.max_pages, self.d, self.d_ik)
+                          self.num_pages, PAGE, self.num_seqs, self.max_pages, self.d, self.d_ik,
+                          FP8E4M3 if fp8 else BF16, _ptr(self.idx_k8), _ptr(self.idx_k8_scale))
 
 
 class Workspace:

@@ -49,9 +49,17 @@ csa2_status check_cache(const csa2_cache& c, bool need_codes, bool need_idx) {
     REQUIRE(((uintptr_t)c.codes & 15) == 0 && ((uintptr_t)c.scales & 15) == 0, CSA2_ERR_INVALID_ARG,
             "cache.codes/scales must be 16-byte aligned");
   }
+  REQUIRE(c.idx_k_dtype == CSA2_BF16 || c.idx_k_dtype == CSA2_FP8E4M3, CSA2_ERR_INVALID_ARG,
+          "cache.idx_k_dtype must be CSA2_BF16 or CSA2_FP8E4M3");
   if (need_idx) {
-    REQUIRE(c.idx_k, CSA2_ERR_INVALID_ARG, "cache.idx_k is NULL");
-    REQUIRE(((uintptr_t)c.idx_k & 15) == 0, CSA2_ERR_INVALID_ARG, "cache.idx_k must be 16-byte aligned");
+    if (c.idx_k_dtype == CSA2_BF16) {
+      REQUIRE(c.idx_k, CSA2_ERR_INVALID_ARG, "cache.idx_k is NULL");
+      REQUIRE(((uintptr_t)c.idx_k & 15) == 0, CSA2_ERR_INVALID_ARG, "cache.idx_k must be 16-byte aligned");
+    } else {
+      REQUIRE(c.idx_k8 && c.idx_k8_scale, CSA2_ERR_INVALID_ARG, "cache.idx_k8 / idx_k8_scale is NULL");
+      REQUIRE(((uintptr_t)c.idx_k8 & 15) == 0 && ((uintptr_t)c.idx_k8_scale & 15) == 0, CSA2_ERR_INVALID_ARG,
+              "cache.idx_k8 and idx_k8_scale must be 16-byte aligned");
+    }
     REQUIRE(c.d_ik == 64 || c.d_ik == 128, CSA2_ERR_UNSUPPORTED_SHAPE, "cache.d_ik must be 64 or 128 (got %d)",
             c.d_ik);
   }
@@ -255,6 +263,9 @@ csa2_status csa2_index_full(const csa2_index_full_args* a, void* ws, size_t ws_b
 csa2_status csa2_index_full_noalloc(const csa2_index_full_args* a, void* stream) {
   csa2_status s = check_full(a);
   if (s != CSA2_OK) return s;
+  REQUIRE(a->cache.idx_k_dtype == CSA2_BF16, CSA2_ERR_UNSUPPORTED_SHAPE,
+          "csa2_index_full_noalloc: the FP8 indexer-K form needs workspace for the quantised indexer Q; "
+          "use csa2_index_full");
   const long long need = (long long)a->B * a->num_blocks * a->per_block;
   REQUIRE(need <= CSA2_NOALLOC_MAX_SCORES, CSA2_ERR_UNSUPPORTED_SHAPE,
           "csa2_index_full_noalloc: B*num_blocks*per_block = %lld exceeds the fixed scratch of %d scores",

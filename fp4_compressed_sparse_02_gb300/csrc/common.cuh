@@ -138,6 +138,16 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// mma.sync m16n8k32 with E4M3 operands (four per 32-bit register), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3_16832(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // mma.sync m16n8k16, fp32 accumulate.  BF16 or F16 operands.
 __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                                uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -207,6 +217,32 @@ __device__ __forceinline__ void fp4_group16(const float* y, uint32_t& w0, uint32
       w1 |= cvt_e2m1x2(__fdiv_rn(y[8 + 2 * i], s), __fdiv_rn(y[9 + 2 * i], s)) << (8 * i);
     }
   }
+}
+
+// One row quantised to E4M3 with one float32 scale, spread over a warp (lane l holds
+// N consecutive values): s = amax / 448, byte = E4M3_RNE_satfinite(x / s) (float32
+// divisions), s == 0 -> zero bytes.  Stores the lane's N bytes at dst (N = 4: one 32-bit
+// store; N = 2: 16-bit) and lane 0 the scale.  Every lane of the warp must call it.
+template <int N>
+__device__ __forceinline__ float fp8_row_store(const float* v, uint8_t* dst, float* scale) {
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) a = fmaxf(a, fabsf(v[j]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float s = __fdiv_rn(a, 448.0f);
+  uint32_t w = 0;
+  if (s > 0.f)
+#pragma unroll
+    for (int j = 0; j < N; ++j) w |= cvt_e4m3(__fdiv_rn(v[j], s)) << (8 * j);
+  if constexpr (N == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = w;
+  } else {
+    static_assert(N == 2, "2 or 4 values a lane");
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w;
+  }
+  if ((threadIdx.x & 31) == 0) *scale = s;
+  return s;
 }
 
 // RoPE of one channel pair, every product and sum rounded on its own.

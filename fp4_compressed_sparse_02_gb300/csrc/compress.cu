@@ -453,6 +453,23 @@ __device__ __forceinline__ void index_k_product(const csa2_cache& cache, const l
 #pragma unroll
     for (int j = 0; j < CPL; ++j) part[(warp * E + e) * DIK + lane * CPL + j] = acc[e][j];
   __syncthreads();
+  if (cache.idx_k_dtype == CSA2_FP8E4M3) {
+    // the compressed form: warp e quantises entry e's bf16 row (lane l: columns l*CPL ..)
+    for (int e = warp; e < E; e += 8) {
+      const long long r = rows[e];
+      if (r < 0) continue;
+      float v[CPL];
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) sum += part[(w8 * E + e) * DIK + lane * CPL + j];
+        v[j] = __bfloat162float(__float2bfloat16_rn(sum));
+      }
+      fp8_row_store<CPL>(v, cache.idx_k8 + r * DIK + lane * CPL, cache.idx_k8_scale + r);
+    }
+    return;
+  }
   for (int i = tid; i < E * DIK; i += 256) {
     const int e = i / DIK, j = i % DIK;
     const long long r = rows[e];

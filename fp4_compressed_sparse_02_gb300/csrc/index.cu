@@ -28,52 +28,97 @@ CSA2_DEFINE_ERROR_WORD(g_err_index);
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
 
-template <int DK, int NHG>
+// A thread's slices of one indexer-K row: bf16 (uint4 j = dims 32j + 8c + [0, 8) of lane c of a
+// row quad) or, in the FP8 form, the bytes [DK/4 c, DK/4 (c + 1)) with the row's scale.
+template <int DK, bool F8>
+struct KRow {
+  uint4 v[F8 ? DK / 64 : DK / 32];
+  float s;
+};
+
+// The query's indexer Q in the same dim mapping (head g of lane (g, c), one head group per
+// entry of v) and the head weights of the lane's two accumulator columns.  FP8 form: the Q
+// bytes and the weights w_h * sq_h quantised by k_quant_q8.
+template <int DK, int NHG, bool F8>
 struct QFrag {
-  uint4 v[NHG][DK / 32];
+  uint4 v[NHG][F8 ? DK / 64 : DK / 32];
   float w[NHG][2];
 };
 
-template <int DK, int NHG>
-__device__ __forceinline__ void load_qfrag(const uint16_t* __restrict__ q, const float* __restrict__ w,
-                                           int H_i, QFrag<DK, NHG>& f) {
+template <int DK, int NHG, bool F8>
+__device__ __forceinline__ void load_qfrag(const void* __restrict__ qv, const float* __restrict__ w, int H_i,
+                                           QFrag<DK, NHG, F8>& f) {
   const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int hg = 0; hg < NHG; ++hg) {
-    int head = hg * 8 + g;
+    const int head = hg * 8 + g;
+    if constexpr (F8) {
+      const uint8_t* q = static_cast<const uint8_t*>(qv);
 #pragma unroll
-    for (int j = 0; j < DK / 32; ++j) {
-      f.v[hg][j] = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + 32 * j + 8 * c))
-                                : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < DK / 64; ++j)
+        f.v[hg][j] = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + (DK / 4) * c + 16 * j))
+                                  : make_uint4(0, 0, 0, 0);
+    } else {
+      const uint16_t* q = static_cast<const uint16_t*>(qv);
+#pragma unroll
+      for (int j = 0; j < DK / 32; ++j)
+        f.v[hg][j] = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + 32 * j + 8 * c))
+                                  : make_uint4(0, 0, 0, 0);
     }
-    int h0 = hg * 8 + 2 * c;
+    const int h0 = hg * 8 + 2 * c;
     f.w[hg][0] = (h0 < H_i) ? __ldg(w + h0) : 0.f;
     f.w[hg][1] = (h0 + 1 < H_i) ? __ldg(w + h0 + 1) : 0.f;
   }
 }
 
 // Load the thread's slices of one cache row (zeros when row < 0).
-template <int DK>
-__device__ __forceinline__ void load_row(const uint16_t* __restrict__ idxk, long long row, uint4* a) {
+template <int DK, bool F8>
+__device__ __forceinline__ void load_row(const csa2_cache& cache, long long row, KRow<DK, F8>& a) {
   const int c = threadIdx.x & 3;
+  if constexpr (F8) {
+    const uint8_t* p = cache.idx_k8 + row * DK + (DK / 4) * c;
 #pragma unroll
-  for (int j = 0; j < DK / 32; ++j)
-    a[j] = (row >= 0) ? ldg_stream_v4(idxk + row * DK + 32 * j + 8 * c) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < DK / 64; ++j) a.v[j] = (row >= 0) ? ldg_stream_v4(p + 16 * j) : make_uint4(0, 0, 0, 0);
+    a.s = (row >= 0) ? __ldg(cache.idx_k8_scale + row) : 0.f;
+  } else {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j)
+      a.v[j] = (row >= 0) ? ldg_stream_v4(cache.idx_k + row * DK + 32 * j + 8 * c) : make_uint4(0, 0, 0, 0);
+    a.s = 1.f;
+  }
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4* v, int w) {
+  const uint4 x = v[w >> 2];
+  return (w & 3) == 0 ? x.x : (w & 3) == 1 ? x.y : (w & 3) == 2 ? x.z : x.w;
 }
 
 // Scores of rows (g) and (g + 8) of a 16-row tile; identical in the 4 lanes of a quad.
-template <int DK, int NHG>
-__device__ __forceinline__ void tile_scores(const QFrag<DK, NHG>& f, const uint4* A0, const uint4* A1,
-                                            bool relu, float& s0, float& s1) {
+// bf16: m16n8k16 products over dims; FP8: m16n8k32 E4M3 products (exact in float32), the
+// k-slots 4c + i / 16 + 4c + i of step j mapped to the lane's bytes 8j + i / 8j + 4 + i,
+// and the row scale applied after the weighted ReLU sum (both scales are >= 0).
+template <int DK, int NHG, bool F8>
+__device__ __forceinline__ void tile_scores(const QFrag<DK, NHG, F8>& f, const KRow<DK, F8>& A0,
+                                            const KRow<DK, F8>& A1, bool relu, float& s0, float& s1) {
   float acc[NHG][4];
 #pragma unroll
   for (int hg = 0; hg < NHG; ++hg) acc[hg][0] = acc[hg][1] = acc[hg][2] = acc[hg][3] = 0.f;
+  if constexpr (F8) {
 #pragma unroll
-  for (int j = 0; j < DK / 32; ++j) {
+    for (int j = 0; j < DK / 32; ++j) {
 #pragma unroll
-    for (int hg = 0; hg < NHG; ++hg) {
-      mma_bf16_16816(acc[hg], A0[j].x, A1[j].x, A0[j].y, A1[j].y, f.v[hg][j].x, f.v[hg][j].y);
-      mma_bf16_16816(acc[hg], A0[j].z, A1[j].z, A0[j].w, A1[j].w, f.v[hg][j].z, f.v[hg][j].w);
+      for (int hg = 0; hg < NHG; ++hg)
+        mma_e4m3_16832(acc[hg], word_of(A0.v, 2 * j), word_of(A1.v, 2 * j), word_of(A0.v, 2 * j + 1),
+                       word_of(A1.v, 2 * j + 1), word_of(f.v[hg], 2 * j), word_of(f.v[hg], 2 * j + 1));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < DK / 32; ++j) {
+#pragma unroll
+      for (int hg = 0; hg < NHG; ++hg) {
+        mma_bf16_16816(acc[hg], A0.v[j].x, A1.v[j].x, A0.v[j].y, A1.v[j].y, f.v[hg][j].x, f.v[hg][j].y);
+        mma_bf16_16816(acc[hg], A0.v[j].z, A1.v[j].z, A0.v[j].w, A1.v[j].w, f.v[hg][j].z, f.v[hg][j].w);
+      }
     }
   }
   float p0 = 0.f, p1 = 0.f;
@@ -90,8 +135,32 @@ __device__ __forceinline__ void tile_scores(const QFrag<DK, NHG>& f, const uint4
   p1 += __shfl_xor_sync(FULL_MASK, p1, 1);
   p0 += __shfl_xor_sync(FULL_MASK, p0, 2);
   p1 += __shfl_xor_sync(FULL_MASK, p1, 2);
+  if constexpr (F8) {
+    p0 *= A0.s;
+    p1 *= A1.s;
+  }
   s0 = p0;
   s1 = p1;
+}
+
+// The FP8 form's indexer Q: each (query, head) row of q_idx (bf16) quantised as the
+// compressed indexer K is (s = amax / 448, E4M3 bytes; zero row -> zero bytes), into q8,
+// and the head weight times that scale into w8.  One warp per row.
+template <int DK>
+__global__ void __launch_bounds__(256) k_quant_q8(const uint16_t* __restrict__ q, const float* __restrict__ w, int rows,
+                                                  uint8_t* __restrict__ q8, float* __restrict__ w8) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int N = DK / 32;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  float v[N];
+#pragma unroll
+  for (int j = 0; j < N; ++j) v[j] = bf16_bits_to_f32(__ldg(q + (long long)r * DK + lane * N + j));
+  float sq;
+  const float s = fp8_row_store<N>(v, q8 + (long long)r * DK + lane * N, &sq);
+  if (lane == 0) w8[r] = __ldg(w + r) * s;
 }
 
 __device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
@@ -105,6 +174,8 @@ __device__ __forceinline__ bool better(float av, int ai, float bv, int bi) {
 struct ScanParams {
   const uint16_t* q;      // [B][H_i][DK]
   const float* w;         // [B][H_i]
+  const uint8_t* q8;      // FP8 form: [B][H_i][DK] quantised indexer Q (workspace)
+  const float* w8;        // FP8 form: [B][H_i] weights times the Q scales (workspace)
   csa2_cache cache;
   const int* seq_of;
   const int* n_vis;
@@ -190,7 +261,7 @@ __device__ __forceinline__ void topp_write(const ScanParams& p, int b, int j, in
   }
 }
 
-template <int DK, int NHG>
+template <int DK, int NHG, bool F8>
 __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -215,10 +286,12 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   // one group at a time (registers for two resident CTAs per SM)
   constexpr bool STREAM_Q = NHG > 2;
   constexpr int NHG_REG = STREAM_Q ? 1 : NHG;
-  const uint16_t* qb = p.q + (long long)b * p.H_i * DK;
-  const float* wb = p.w + (long long)b * p.H_i;
-  QFrag<DK, NHG_REG> f;
-  if (!STREAM_Q) load_qfrag<DK, NHG_REG>(qb, wb, p.H_i, f);
+  constexpr int QB = F8 ? 1 : 2;                 // bytes per indexer-Q element
+  const uint8_t* qb = reinterpret_cast<const uint8_t*>(F8 ? (const void*)p.q8 : (const void*)p.q) +
+                      (long long)b * p.H_i * DK * QB;
+  const float* wb = (F8 ? p.w8 : p.w) + (long long)b * p.H_i;
+  QFrag<DK, NHG_REG, F8> f;
+  if (!STREAM_Q) load_qfrag<DK, NHG_REG, F8>(qb, wb, p.H_i, f);
 
   float tv = -INFINITY;
   int ti = 0x7fffffff;
@@ -227,29 +300,29 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
 
   for (long long base = lo; base < hi; base += 32) {
     long long r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
-    uint4 A[4][DK / 32];
+    KRow<DK, F8> A[4];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       long long row = (r[t] < hi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
-      load_row<DK>(p.cache.idx_k, row, A[t]);
+      load_row<DK, F8>(p.cache, row, A[t]);
     }
     float sc[4];
     if (STREAM_Q) {
       sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
 #pragma unroll 1
       for (int hg = 0; hg < NHG; ++hg) {
-        load_qfrag<DK, NHG_REG>(qb + hg * 8 * DK, wb + hg * 8, p.H_i - hg * 8, f);
+        load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, p.H_i - hg * 8, f);
         float x0, x1, x2, x3;
-        tile_scores<DK, NHG_REG>(f, A[0], A[1], p.relu != 0, x0, x1);
-        tile_scores<DK, NHG_REG>(f, A[2], A[3], p.relu != 0, x2, x3);
+        tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], p.relu != 0, x0, x1);
+        tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], p.relu != 0, x2, x3);
         sc[0] += x0;
         sc[1] += x1;
         sc[2] += x2;
         sc[3] += x3;
       }
     } else {
-      tile_scores<DK, NHG_REG>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
-      tile_scores<DK, NHG_REG>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+      tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+      tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
     }
     // lane (g, c) owns candidate row r[c] = base + g + 8c (a permutation of the 32 rows)
     float cv = sc[0];
@@ -269,7 +342,7 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
 // once and scored against every query (H_i <= 8).  Query q keeps its own blocks of its own
 // n_vis: the warp of block j reads rows [min_q lo_q, max_q hi_q) and offers each query only
 // its rows, so every query's pool and scores equal those of scanning it alone.
-template <int DK, int G>
+template <int DK, int G, bool F8>
 __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -308,11 +381,11 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
     }
     for (int base = rlo; base < rhi; base += 32) {
       const int r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
-      uint4 A[4][DK / 32];
+      KRow<DK, F8> A[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const long long row = (r[t] < rhi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
-        load_row<DK>(p.cache.idx_k, row, A[t]);
+        load_row<DK, F8>(p.cache, row, A[t]);
       }
       // lane (g, c) owns candidate row base + g + 8c (a permutation of the 32 rows)
       int ci = r[0];
@@ -321,11 +394,14 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
         if (c == t) ci = r[t];
 #pragma unroll
       for (int q = 0; q < G; ++q) {
-        QFrag<DK, 1> f;
-        load_qfrag<DK, 1>(p.q + (long long)(b0 + q) * p.H_i * DK, p.w + (long long)(b0 + q) * p.H_i, p.H_i, f);
+        QFrag<DK, 1, F8> f;
+        if constexpr (F8)
+          load_qfrag<DK, 1, F8>(p.q8 + (long long)(b0 + q) * p.H_i * DK, p.w8 + (long long)(b0 + q) * p.H_i, p.H_i, f);
+        else
+          load_qfrag<DK, 1, F8>(p.q + (long long)(b0 + q) * p.H_i * DK, p.w + (long long)(b0 + q) * p.H_i, p.H_i, f);
         float sc[4];
-        tile_scores<DK, 1>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
-        tile_scores<DK, 1>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
+        tile_scores<DK, 1, F8>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, 1, F8>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
         float cv = sc[0];
 #pragma unroll
         for (int t = 1; t < 4; ++t)
@@ -345,6 +421,8 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
 struct PoolScoreParams {
   const uint16_t* q;
   const float* w;
+  const uint8_t* q8;      // FP8 form (workspace), as in ScanParams
+  const float* w8;
   csa2_cache cache;
   const int* seq_of;
   const int* pool;
@@ -428,7 +506,7 @@ __device__ __forceinline__ void hist_add_warp(int* hist, int bin, int cnt) {
   if (active && !same) atomicAdd(&hist[bin], cnt);
 }
 
-template <int DK, int NHG, bool SCORE>
+template <int DK, int NHG, bool SCORE, bool F8>
 __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_select_cl(SelectParams p, PoolScoreParams sp) {
   pdl_wait();
   pdl_trigger();
@@ -482,10 +560,12 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     // as in the Full scan: more than two head groups stream their Q fragments from L1
     constexpr bool STREAM_Q = NHG > 2;
     constexpr int NHG_REG = STREAM_Q ? 1 : NHG;
-    const uint16_t* qb = sp.q + (long long)b * sp.H_i * DK;
-    const float* wb = sp.w + (long long)b * sp.H_i;
-    QFrag<DK, NHG_REG> f;
-    if (!STREAM_Q) load_qfrag<DK, NHG_REG>(qb, wb, sp.H_i, f);
+    constexpr int QB = F8 ? 1 : 2;               // bytes per indexer-Q element
+    const uint8_t* qb = reinterpret_cast<const uint8_t*>(F8 ? (const void*)sp.q8 : (const void*)sp.q) +
+                        (long long)b * sp.H_i * DK * QB;
+    const float* wb = (F8 ? sp.w8 : sp.w) + (long long)b * sp.H_i;
+    QFrag<DK, NHG_REG, F8> f;
+    if (!STREAM_Q) load_qfrag<DK, NHG_REG, F8>(qb, wb, sp.H_i, f);
     auto pos_of = [&](int it, int u) { return s0 + 32 * (warp + 8 * it) + g + 8 * u; };
     auto fetch_ent = [&](int it, int* e) {
 #pragma unroll
@@ -509,9 +589,9 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     fetch_ent(1, en);
 #pragma unroll 1
     for (int it = 0; it < NT && s0 + 32 * (warp + 8 * it) < e1; ++it) {
-      uint4 A[4][DK / 32];
+      KRow<DK, F8> A[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) load_row<DK>(sp.cache.idx_k, rw[u], A[u]);
+      for (int u = 0; u < 4; ++u) load_row<DK, F8>(sp.cache, rw[u], A[u]);
       resolve(it + 1, en, rw);                            // next tile, while these rows load
       fetch_ent(it + 2, en);
       float sc[4];
@@ -519,18 +599,18 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
         sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
 #pragma unroll 1
         for (int hg = 0; hg < NHG; ++hg) {
-          load_qfrag<DK, NHG_REG>(qb + hg * 8 * DK, wb + hg * 8, sp.H_i - hg * 8, f);
+          load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, sp.H_i - hg * 8, f);
           float x0, x1, x2, x3;
-          tile_scores<DK, NHG_REG>(f, A[0], A[1], sp.relu != 0, x0, x1);
-          tile_scores<DK, NHG_REG>(f, A[2], A[3], sp.relu != 0, x2, x3);
+          tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], sp.relu != 0, x0, x1);
+          tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], sp.relu != 0, x2, x3);
           sc[0] += x0;
           sc[1] += x1;
           sc[2] += x2;
           sc[3] += x3;
         }
       } else {
-        tile_scores<DK, NHG_REG>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
-        tile_scores<DK, NHG_REG>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
+        tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
       }
       if (c == 0) {
 #pragma unroll
@@ -796,27 +876,39 @@ static void launch_persistent(K kernel, const ScanParams& sp, long long units, c
   launch_k(kernel, grid, 256, 0, st, sp);
 }
 
-template <int DK>
+template <int DK, bool F8>
 static void launch_scan_group(const ScanParams& sp, int group, long long units, cudaStream_t st) {
   switch (group) {
-    case 2: launch_persistent(k_full_scan_g<DK, 2>, sp, units, st); break;
-    case 3: launch_persistent(k_full_scan_g<DK, 3>, sp, units, st); break;
-    case 4: launch_persistent(k_full_scan_g<DK, 4>, sp, units, st); break;
-    case 5: launch_persistent(k_full_scan_g<DK, 5>, sp, units, st); break;
-    case 6: launch_persistent(k_full_scan_g<DK, 6>, sp, units, st); break;
-    case 7: launch_persistent(k_full_scan_g<DK, 7>, sp, units, st); break;
-    default: launch_persistent(k_full_scan_g<DK, 8>, sp, units, st); break;
+    case 2: launch_persistent(k_full_scan_g<DK, 2, F8>, sp, units, st); break;
+    case 3: launch_persistent(k_full_scan_g<DK, 3, F8>, sp, units, st); break;
+    case 4: launch_persistent(k_full_scan_g<DK, 4, F8>, sp, units, st); break;
+    case 5: launch_persistent(k_full_scan_g<DK, 5, F8>, sp, units, st); break;
+    case 6: launch_persistent(k_full_scan_g<DK, 6, F8>, sp, units, st); break;
+    case 7: launch_persistent(k_full_scan_g<DK, 7, F8>, sp, units, st); break;
+    default: launch_persistent(k_full_scan_g<DK, 8, F8>, sp, units, st); break;
   }
 }
 
-template <int DK>
+template <int DK, bool F8>
 static void launch_scan_dk(const ScanParams& sp, int nhg, long long units, cudaStream_t st) {
   switch (nhg) {
-    case 1: launch_persistent(k_full_scan<DK, 1>, sp, units, st); break;
-    case 2: launch_persistent(k_full_scan<DK, 2>, sp, units, st); break;
-    case 3: launch_persistent(k_full_scan<DK, 3>, sp, units, st); break;
-    default: launch_persistent(k_full_scan<DK, 4>, sp, units, st); break;
+    case 1: launch_persistent(k_full_scan<DK, 1, F8>, sp, units, st); break;
+    case 2: launch_persistent(k_full_scan<DK, 2, F8>, sp, units, st); break;
+    case 3: launch_persistent(k_full_scan<DK, 3, F8>, sp, units, st); break;
+    default: launch_persistent(k_full_scan<DK, 4, F8>, sp, units, st); break;
   }
+}
+
+// The FP8 form's quantised indexer Q and weights, after `at` bytes of the workspace.
+static size_t q8_bytes(int B, int H_i, int DK) { return (((size_t)B * H_i * DK + 255) & ~(size_t)255); }
+static size_t q8_total(int B, int H_i, int DK) { return q8_bytes(B, H_i, DK) + (size_t)B * H_i * sizeof(float); }
+
+static cudaError_t launch_quant_q8(const uint16_t* q, const float* w, int B, int H_i, int DK, uint8_t* q8, float* w8,
+                                   cudaStream_t st) {
+  const int rows = B * H_i;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (DK == 128) return launch_k(k_quant_q8<128>, grid, 256, 0, st, q, w, rows, q8, w8);
+  return launch_k(k_quant_q8<64>, grid, 256, 0, st, q, w, rows, q8, w8);
 }
 
 // The tensor-core scoring streams every row once per group of queries and scores it against
@@ -834,8 +926,14 @@ bool full_scores_tc_chosen(const csa2_index_full_args& a) {
   return force == 1 || G * a.H_i >= 16;
 }
 
+static size_t pool_score_bytes(const csa2_index_full_args& a) {
+  return (((size_t)a.B * a.num_blocks * a.per_block * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
-  // pool scores, then (tensor-core scoring) the score matrix
+  // pool scores, then (tensor-core scoring) the score matrix, or (FP8 form) the quantised
+  // indexer Q and weights
+  if (a.cache.idx_k_dtype == CSA2_FP8E4M3) return pool_score_bytes(a) + q8_total(a.B, a.H_i, a.cache.d_ik);
   const size_t pool = (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
   return pool + (full_scores_tc_chosen(a) ? full_scores_tc_bytes(a) : 0);
 }
@@ -862,18 +960,34 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
   // CTAs of 8 blocks' work: per group of queries (grouped scan) or per query
   const long long units_g = ((long long)(a.B / group) * a.num_blocks + 7) / 8;
   const long long units = ((long long)a.B * a.num_blocks + 7) / 8;
-  if (allow_tc && full_scores_tc_chosen(a)) {     // groups of queries of one sequence: a dense product
+  const bool f8 = a.cache.idx_k_dtype == CSA2_FP8E4M3;
+  if (f8) {                                        // the indexer Q quantised like the compressed K
+    uint8_t* q8 = static_cast<uint8_t*>(ws) + pool_score_bytes(a);
+    float* w8 = reinterpret_cast<float*>(q8 + q8_bytes(a.B, a.H_i, a.cache.d_ik));
+    cudaError_t e = launch_quant_q8(a.q_idx, a.w, a.B, a.H_i, a.cache.d_ik, q8, w8, st);
+    if (e != cudaSuccess) return e;
+    sp.q8 = q8;
+    sp.w8 = w8;
+    if (group > 1 && group <= 8 && a.H_i <= 8) {
+      if (a.cache.d_ik == 128) launch_scan_group<128, true>(sp, group, units_g, st);
+      else launch_scan_group<64, true>(sp, group, units_g, st);
+    } else if (a.cache.d_ik == 128) {
+      launch_scan_dk<128, true>(sp, nhg, units, st);
+    } else {
+      launch_scan_dk<64, true>(sp, nhg, units, st);
+    }
+  } else if (allow_tc && full_scores_tc_chosen(a)) {     // groups of queries of one sequence: a dense product
     float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (size_t)a.B * a.num_blocks * a.per_block *
                                                                         sizeof(float));
     cudaError_t e = launch_full_scores_tc(a, S, static_cast<float*>(ws), st);
     if (e != cudaSuccess) return e;
   } else if (group > 1 && group <= 8 && a.H_i <= 8) {
-    if (a.cache.d_ik == 128) launch_scan_group<128>(sp, group, units_g, st);
-    else launch_scan_group<64>(sp, group, units_g, st);
+    if (a.cache.d_ik == 128) launch_scan_group<128, false>(sp, group, units_g, st);
+    else launch_scan_group<64, false>(sp, group, units_g, st);
   } else if (a.cache.d_ik == 128) {
-    launch_scan_dk<128>(sp, nhg, units, st);
+    launch_scan_dk<128, false>(sp, nhg, units, st);
   } else {
-    launch_scan_dk<64>(sp, nhg, units, st);
+    launch_scan_dk<64, false>(sp, nhg, units, st);
   }
   SelectParams sel{};
   sel.score = static_cast<const float*>(ws);
@@ -896,28 +1010,28 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
     launch_k(k_select_cta, a.B, C1_THREADS, C1_SMEM, st, sel);
   } else {
     PoolScoreParams none{};
-    launch_k_late(k_select_cl<128, 1, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
+    launch_k_late(k_select_cl<128, 1, false, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
   }
   return cudaGetLastError();
 }
 
+// Reindex keeps its scores in shared memory; the FP8 form needs the quantised indexer Q
 size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a) {
-  return (size_t)a.B * a.pool_stride * sizeof(float);
+  return a.cache.idx_k_dtype == CSA2_FP8E4M3 ? q8_total(a.B, a.H_i, a.cache.d_ik) : 0;
 }
 
-template <int DK>
+template <int DK, bool F8>
 static void launch_reindex_dk(const SelectParams& sel, const PoolScoreParams& pp, int nhg, int B, cudaStream_t st) {
   const dim3 grid(NCL, B);
   switch (nhg) {
-    case 1: launch_k_late(k_select_cl<DK, 1, true>, grid, CL_THREADS, 0, st, sel, pp); break;
-    case 2: launch_k_late(k_select_cl<DK, 2, true>, grid, CL_THREADS, 0, st, sel, pp); break;
-    case 3: launch_k_late(k_select_cl<DK, 3, true>, grid, CL_THREADS, 0, st, sel, pp); break;
-    default: launch_k_late(k_select_cl<DK, 4, true>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 1: launch_k_late(k_select_cl<DK, 1, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 2: launch_k_late(k_select_cl<DK, 2, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 3: launch_k_late(k_select_cl<DK, 3, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
+    default: launch_k_late(k_select_cl<DK, 4, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
   }
 }
 
 cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cudaStream_t st) {
-  (void)ws;
   if (a.B == 0) return cudaSuccess;
   PoolScoreParams pp{};
   pp.q = a.q_idx;
@@ -937,8 +1051,20 @@ cudaError_t launch_index_reindex(const csa2_index_reindex_args& a, void* ws, cud
   sel.topk = a.topk;
   sel.topk_len = a.topk_len;
   const int nhg = (a.H_i + 7) / 8;
-  if (a.cache.d_ik == 128) launch_reindex_dk<128>(sel, pp, nhg, a.B, st);
-  else launch_reindex_dk<64>(sel, pp, nhg, a.B, st);
+  if (a.cache.idx_k_dtype == CSA2_FP8E4M3) {
+    uint8_t* q8 = static_cast<uint8_t*>(ws);
+    float* w8 = reinterpret_cast<float*>(q8 + q8_bytes(a.B, a.H_i, a.cache.d_ik));
+    cudaError_t e = launch_quant_q8(a.q_idx, a.w, a.B, a.H_i, a.cache.d_ik, q8, w8, st);
+    if (e != cudaSuccess) return e;
+    pp.q8 = q8;
+    pp.w8 = w8;
+    if (a.cache.d_ik == 128) launch_reindex_dk<128, true>(sel, pp, nhg, a.B, st);
+    else launch_reindex_dk<64, true>(sel, pp, nhg, a.B, st);
+  } else if (a.cache.d_ik == 128) {
+    launch_reindex_dk<128, false>(sel, pp, nhg, a.B, st);
+  } else {
+    launch_reindex_dk<64, false>(sel, pp, nhg, a.B, st);
+  }
   return cudaGetLastError();
 }
 

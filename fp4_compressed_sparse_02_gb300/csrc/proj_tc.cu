@@ -379,7 +379,44 @@ __global__ void __launch_bounds__(iktc::THREADS, 1)
   }
   __syncthreads();
   tc::fence_after_sync();
-  if (warp < 4 && ok_flag) {                         // warp w: TMEM lanes (rows) 32 w ..
+  if (warp < 4 && ok_flag && cache.idx_k_dtype == CSA2_FP8E4M3) {
+    // the compressed form: each thread owns one entry's row (TMEM lane); a first pass finds
+    // the largest |bf16 value|, a second quantises (s = amax / 448, float32 divisions)
+    const long long row = rows[32 * warp + lane];
+    const uint32_t lanes = (uint32_t)(32 * warp) << 16;
+    float a = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < NK; c += 32) {
+      uint32_t v[32];
+      tc::tmem_ld32(tb + lanes + (uint32_t)c, v);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[i])))));
+    }
+    const float sc = __fdiv_rn(a, 448.0f);
+#pragma unroll 1
+    for (int c = 0; c < NK; c += 32) {
+      uint32_t v[32];
+      tc::tmem_ld32(tb + lanes + (uint32_t)c, v);
+      tc::tmem_ld_wait();
+      if (row >= 0) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          pk[i] = 0u;
+          if (sc > 0.f)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              pk[i] |= cvt_e4m3(__fdiv_rn(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[4 * i + j]))), sc))
+                       << (8 * j);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(cache.idx_k8 + row * NK + c);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+    if (row >= 0) cache.idx_k8_scale[row] = sc;
+  } else if (warp < 4 && ok_flag) {                  // warp w: TMEM lanes (rows) 32 w ..
     const long long row = rows[32 * warp + lane];
 #pragma unroll 1
     for (int c = 0; c < NK; c += 32) {

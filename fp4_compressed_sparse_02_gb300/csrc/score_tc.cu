@@ -467,7 +467,8 @@ static int tc_query_tile(const csa2_index_full_args& a) {
 
 bool full_scores_tc_supported(const csa2_index_full_args& a) {
   const int QT = tc_query_tile(a);
-  return QT > 0 && a.B % QT == 0 && a.cache.d_ik == stc::DK && a.per_block >= 1 && a.per_block <= 16 &&
+  return QT > 0 && a.B % QT == 0 && a.cache.idx_k_dtype == CSA2_BF16 && a.cache.d_ik == stc::DK &&
+         a.per_block >= 1 && a.per_block <= 16 &&
          a.max_n > 0 && ((uintptr_t)a.q_idx & 15) == 0 && ((uintptr_t)a.cache.idx_k & 15) == 0 &&
          ((uintptr_t)a.w & 15) == 0 && tensor_map_encoder() != nullptr;
 }

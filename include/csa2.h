@@ -49,7 +49,10 @@ typedef enum csa2_status {
   CSA2_ERR_DEVICE_CHECK = 5        /* the device error word was non-zero */
 } csa2_status;
 
-typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
+/* Element types.  CSA2_FP8E4M3 selects the compressed indexer-K plane (csa2_cache);
+ * CSA2_FP4E2M1X2 names the packed Main KV codes (two E2M1 codes per byte), which no
+ * argument takes as a choice. */
+typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1, CSA2_FP8E4M3 = 2, CSA2_FP4E2M1X2 = 3 } csa2_dtype;
 
 /* Device error word bits (csa2_get_device_error). */
 #define CSA2_DEVERR_PAGE_ID      0x1u  /* page id outside [0, num_pages) */
@@ -65,13 +68,27 @@ typedef enum csa2_dtype { CSA2_BF16 = 0, CSA2_F32 = 1 } csa2_dtype;
 #define CSA2_PAGE_SIZE 64
 
 /* Paged cache planes (all device).  d in {128, 512}; d_ik in {64, 128};
- * num_pages <= 2^25 (2^31 entries). */
+ * num_pages <= 2^25 (2^31 entries).
+ *
+ * Indexer K is kept in one of two forms, chosen by idx_k_dtype:
+ *   CSA2_BF16    (0, the form the pages imply): idx_k, bf16.
+ *   CSA2_FP8E4M3 (compressed; not on the pages): idx_k8 and idx_k8_scale -- each entry's
+ *                bf16 indexer K row x quantised to E4M3 with one float32 scale:
+ *                s = amax|x| / 448 (float32 division), byte = E4M3_RNE_satfinite(x / s),
+ *                s == 0 -> zero bytes (the quantiser of csa2_swa_quant).  d_ik + 4 bytes
+ *                an entry instead of 2 d_ik: the Full scan streams half the bytes.  The
+ *                indexer then quantises each query head's bf16 indexer Q the same way and
+ *                scores the dequantised values:
+ *                s(e) = sum_h w_h ReLU((sq_h q8_h) . (sk_e k8_e)),
+ *                its dot products on FP8 tensor-core operands (exact products, float32
+ *                sums).
+ */
 typedef struct csa2_cache {
   uint8_t* codes;              /* [num_pages][64][d/2]  E2M1 pairs, even channel in the low nibble;
                                   16-byte aligned */
   uint8_t* scales;             /* [num_pages][64][d/16] E4M3 scale of each 16 channels; 16-byte aligned */
-  uint16_t* idx_k;             /* [num_pages][64][d_ik] bf16 indexer K (may be NULL if unused);
-                                  16-byte aligned */
+  uint16_t* idx_k;             /* [num_pages][64][d_ik] bf16 indexer K (CSA2_BF16 form; may be NULL
+                                  if unused); 16-byte aligned */
   const int32_t* page_table;   /* [num_seqs][max_pages] page id of each 64-entry page */
   int32_t num_pages;
   int32_t page_size;           /* must be 64 */
@@ -79,6 +96,10 @@ typedef struct csa2_cache {
   int32_t max_pages;
   int32_t d;
   int32_t d_ik;
+  csa2_dtype idx_k_dtype;      /* CSA2_BF16 (0) or CSA2_FP8E4M3 */
+  uint8_t* idx_k8;             /* [num_pages][64][d_ik] E4M3 indexer K (CSA2_FP8E4M3 form); 16-byte
+                                  aligned */
+  float* idx_k8_scale;         /* [num_pages][64] float32 scale of each idx_k8 row; 16-byte aligned */
 } csa2_cache;
 
 /* ------------------------------------------------------------------------------

@@ -131,3 +131,9 @@ def append_token(pending, h, t, W_kv, W_z, m, cos_tab, sin_tab, d_rope, W_ik=Non
     Zg = np.stack([z for _, z in pending]) if m > 1 else None
     pending.clear()
     return t // m, compress_quant(Cg, Zg, m, np.array([t]), cos_tab, sin_tab, d_rope, W_ik)
+
+
+def index_k_fp8(idx_k_bits):
+    """The compressed form of indexer K (READING, see indexer.fp8_form): each bf16 row
+    quantised to E4M3 with one float32 scale amax / 448.  Returns (bytes, scales)."""
+    return formats.fp8_rows_quantize(formats.bf16_value(idx_k_bits).astype(np.float32))

@@ -96,3 +96,20 @@ def reindex(q, w, K, pool, k, relu=True):
 def reuse(previous_topk):
     """Reuse mode [deep-dive §3.2]: no indexer; the most recent Top-k is used as is."""
     return np.asarray(previous_topk).copy()
+
+
+def fp8_form(q, K8, Ks):
+    """The compressed (FP8) indexer: the values it scores.
+
+    READING (not on the pages; the pages keep indexer K in the form Main KV implies): each
+    entry's bf16 indexer K row is stored as E4M3 bytes K8 with one float32 scale Ks =
+    amax / 448 (formats.fp8_rows_quantize), and each query head's bf16 indexer Q row is
+    quantised the same way at scoring time, as FP8 indexers do.  The scores are then those
+    of scores() / full() / reindex() over the dequantised values of both.
+
+    q: [H, dk] float values of the bf16 indexer Q; K8: [n, dk] uint8; Ks: [n] float32.
+    Returns (q_hat [H, dk], K_hat [n, dk]) in float64, both exact.
+    """
+    from . import formats
+    q8, qs = formats.fp8_rows_quantize(np.asarray(q, dtype=np.float32))
+    return formats.fp8_rows_dequantize(q8, qs), formats.fp8_rows_dequantize(K8, Ks)

@@ -238,3 +238,20 @@ def test_append_one_bad_field(L, change, status, msg):
 def test_append_at_m1_needs_no_pending_buffer(L):
     n = ctypes.c_size_t(0)
     assert L.csa2_compress_append_workspace(ctypes.byref(_append(m=1, pend=0, W_z=0)), ctypes.byref(n)) == OK
+
+
+def test_fp8_form_needs_its_planes(L):
+    n = ctypes.c_size_t(0)
+    a = _full(cache=_cache(idx_k_dtype=2))                 # FP8 form without idx_k8
+    assert L.csa2_index_full_workspace(ctypes.byref(a), ctypes.byref(n)) == INVALID
+    assert "idx_k8" in L.csa2_last_error_message().decode()
+    a = _full(cache=_cache(idx_k_dtype=2, idx_k8=P, idx_k8_scale=P))
+    assert L.csa2_index_full_workspace(ctypes.byref(a), ctypes.byref(n)) == OK
+    a = _full(cache=_cache(idx_k_dtype=9))
+    assert L.csa2_index_full_workspace(ctypes.byref(a), ctypes.byref(n)) == INVALID
+
+
+def test_noalloc_rejects_the_fp8_form_before_any_cuda_call(L):
+    a = _full(cache=_cache(idx_k_dtype=2, idx_k8=P, idx_k8_scale=P))
+    assert L.csa2_index_full_noalloc(ctypes.byref(a), None) == SHAPE
+    assert "FP8" in L.csa2_last_error_message().decode()

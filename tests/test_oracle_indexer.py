@@ -7,7 +7,8 @@ import numpy as np
 import pytest
 
 from conftest import read_golden
-from oracle import indexer
+from fp4_compressed_sparse_02_gb300 import synth
+from oracle import formats, indexer
 
 
 def _golden():
@@ -145,3 +146,23 @@ def test_reindex_scores_only_the_pool():
 def test_reuse_is_identity():
     t = np.array([3, 9, 27, -1])
     np.testing.assert_array_equal(indexer.reuse(t), t)
+
+
+def test_fp8_form_scores_equal_the_scaled_byte_products():
+    # the FP8 indexer's score of an entry is sk * sum_h w_h sq_h ReLU(sum_c q8 k8): the row
+    # scales (>= 0) factor out of the ReLU
+    r = np.random.default_rng(31)
+    H, dk, n = 8, 128, 300
+    q = formats.bf16_value(synth.bf16_normal(r, (H, dk)))
+    K = formats.bf16_value(synth.bf16_normal(r, (n, dk)))
+    w = r.standard_normal(H)
+    K8, Ks = formats.fp8_rows_quantize(K.astype(np.float32))
+    qh, Kh = indexer.fp8_form(q, K8, Ks)
+    s = indexer.scores(qh, w, Kh)
+    q8, qs = formats.fp8_rows_quantize(q.astype(np.float32))
+    dots = formats.e4m3_value(K8) @ formats.e4m3_value(q8).T          # exact integer-grid products
+    want = Ks.astype(np.float64) * (np.maximum(dots, 0) @ (w * qs.astype(np.float64)))
+    np.testing.assert_allclose(s, want, rtol=1e-12, atol=0)
+    # and the quantised K is within half an E4M3 step of K (relative 2^-4 of each value, or
+    # an absolute 2^-10 s below the normal range)
+    assert (np.abs(Kh - K) <= np.maximum(np.abs(K) * 2.0 ** -4, Ks[:, None] * 2.0 ** -10) + 1e-30).all()
