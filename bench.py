@@ -33,6 +33,7 @@ from fp4_compressed_sparse_02_gb300.schedule import FULL, REINDEX, REUSE  # noqa
 
 METRIC = "CSA2 decode query-layers/s at 128K–1M ctx; achieved HBM GB/s vs ~8 TB/s peak"
 WORKLOADS = {"decode128k": synth.DEC128K, "decode1m": synth.DEC1M, "decode128k_hi32": synth.DEC128K_HI32,
+             "decode128k_ik8": synth.DEC128K_IK8, "decode1m_ik8": synth.DEC1M_IK8,
              "decode128k_verify6": synth.DEC128K_V6, "prefill_compress": synth.PREFILL, "prefill": synth.PREFILL,
              "sweep": synth.DEC1M}
 SYNTH_NAME = {"decode128k": "DEC128K", "decode1m": "DEC1M", "decode128k_hi32": "DEC128K_HI32",
@@ -692,13 +693,16 @@ def main():
         reindex_gbs = reindex_bytes / (reindex_ms / 1000.0) / 1e9
         step_gbs = nbytes["total"] / (ms_step / 1000.0) / 1e9
         # the Full call scores on the tensor cores when a group's heads fill >= 16 columns
-        tc_full = info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and info["H_i"] * info.get("G", 1) >= 16
-        full_kernels = "k_score_tc + k_block_topp + k_select_cl" if tc_full else "k_full_scan + k_select_cl"
+        ik8 = bool(info.get("ik8"))
+        tc_full = (not ik8 and info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and
+                   info["H_i"] * info.get("G", 1) >= 16)
+        full_kernels = ("k_score_tc + k_block_topp + k_select_cl" if tc_full else
+                        "k_full_scan + k_select_cl" + (" (+ k_quant_q8, FP8 indexer)" if ik8 else ""))
         # kernels per step: compressor append 2 (projection; quantisation + indexer K), Full
-        # indexer 2 (scan, select) or 3 (score, block top-P, select), Reindex 1, attention 1
-        # per layer
-        launches = (2 + (3 if tc_full else 2) * list(modes).count(FULL) + list(modes).count(REINDEX) +
-                    len(modes))
+        # indexer 2 (scan, select) or 3 (score, block top-P, select; or FP8: Q quantisation,
+        # scan, select), Reindex 1 (FP8: 2), attention 1 per layer
+        launches = (2 + (3 if (tc_full or ik8) else 2) * list(modes).count(FULL) +
+                    (2 if ik8 else 1) * list(modes).count(REINDEX) + len(modes))
         n_full = list(modes).count(FULL)
         n_reindex = list(modes).count(REINDEX)
         roof = {
@@ -731,7 +735,9 @@ def main():
                                       f"queries per GPU (Full scan of a sequence shared by its {info['G']} queries)")
                                    + f", Top-{info['k']}, SWA {info['W']}, pool {info['NB']}x{info['P']}",
                        "N": info["N"], "B": B, "layers": info["layers"], "d_kv": info["d"], "Hq": info["Hq"],
-                       "indexer": f"{info['H_i']}x{info['d_ik']}", "parallelism": f"replicas x{world}",
+                       "indexer": f"{info['H_i']}x{info['d_ik']}" + (", FP8 E4M3 indexer K and Q" if ik8 else
+                                                                      ", bf16 indexer K"),
+                       "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2: {nbytes['total'] / 1e9:.2f} GB algorithmic bytes per step"},
             "roofline": dict(roof[dominant], dominant_of=sorted(roof), event_samples=len(evs)),
             "roofline_attn": roof["attn"],
@@ -744,7 +750,7 @@ def main():
             "e2e": {"value": e2e_val, "unit": "query-layers/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
         }
-        if not a.no_cpu_baseline:
+        if not a.no_cpu_baseline and a.workload in SYNTH_NAME:
             line["cpu_baseline"] = cpu_baseline(info["N"], SYNTH_NAME[a.workload])
         print(json.dumps(line), flush=True)
     if world > 1:

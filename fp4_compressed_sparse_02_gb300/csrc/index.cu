@@ -298,40 +298,49 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   float thv = -INFINITY;
   int thi = 0x7fffffff;
 
-  for (long long base = lo; base < hi; base += 32) {
-    long long r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
-    KRow<DK, F8> A[4];
+  // rows of TPI tiles of 32 are loaded per iteration: the FP8 form's rows are half the
+  // bytes, so it takes two tiles to keep as many bytes in flight as the bf16 form
+  constexpr int TPI = F8 ? 2 : 1;
+  for (long long base = lo; base < hi; base += 32 * TPI) {
+    long long r[TPI][4];
+    KRow<DK, F8> A[TPI][4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      long long row = (r[t] < hi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
-      load_row<DK, F8>(p.cache, row, A[t]);
-    }
-    float sc[4];
-    if (STREAM_Q) {
-      sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
-#pragma unroll 1
-      for (int hg = 0; hg < NHG; ++hg) {
-        load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, p.H_i - hg * 8, f);
-        float x0, x1, x2, x3;
-        tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], p.relu != 0, x0, x1);
-        tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], p.relu != 0, x2, x3);
-        sc[0] += x0;
-        sc[1] += x1;
-        sc[2] += x2;
-        sc[3] += x3;
+    for (int tt = 0; tt < TPI; ++tt)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        r[tt][t] = base + 32 * tt + 8 * t + g;
+        const long long row = (r[tt][t] < hi) ? entry_row(p.cache, s, r[tt][t], &g_err_index) : -1;
+        load_row<DK, F8>(p.cache, row, A[tt][t]);
       }
-    } else {
-      tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], p.relu != 0, sc[0], sc[1]);
-      tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], p.relu != 0, sc[2], sc[3]);
-    }
-    // lane (g, c) owns candidate row r[c] = base + g + 8c (a permutation of the 32 rows)
-    float cv = sc[0];
-    int ci = (int)r[0];
 #pragma unroll
-    for (int t = 1; t < 4; ++t)
-      if (c == t) { cv = sc[t]; ci = (int)r[t]; }
-    if ((long long)ci >= hi) { cv = -INFINITY; ci = 0x7fffffff; }
-    topp_offer(cv, ci, P, tv, ti, thv, thi);
+    for (int tt = 0; tt < TPI; ++tt) {
+      float sc[4];
+      if (STREAM_Q) {
+        sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+#pragma unroll 1
+        for (int hg = 0; hg < NHG; ++hg) {
+          load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, p.H_i - hg * 8, f);
+          float x0, x1, x2, x3;
+          tile_scores<DK, NHG_REG, F8>(f, A[tt][0], A[tt][1], p.relu != 0, x0, x1);
+          tile_scores<DK, NHG_REG, F8>(f, A[tt][2], A[tt][3], p.relu != 0, x2, x3);
+          sc[0] += x0;
+          sc[1] += x1;
+          sc[2] += x2;
+          sc[3] += x3;
+        }
+      } else {
+        tile_scores<DK, NHG_REG, F8>(f, A[tt][0], A[tt][1], p.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, NHG_REG, F8>(f, A[tt][2], A[tt][3], p.relu != 0, sc[2], sc[3]);
+      }
+      // lane (g, c) owns candidate row r[c] = base + g + 8c (a permutation of the 32 rows)
+      float cv = sc[0];
+      int ci = (int)r[tt][0];
+#pragma unroll
+      for (int t = 1; t < 4; ++t)
+        if (c == t) { cv = sc[t]; ci = (int)r[tt][t]; }
+      if ((long long)ci >= hi) { cv = -INFINITY; ci = 0x7fffffff; }
+      topp_offer(cv, ci, P, tv, ti, thv, thi);
+    }
   }
   topp_write(p, b, j, n, lo, hi, tv, ti);
   }
@@ -379,14 +388,22 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
       thv[q] = -INFINITY;
       thi[q] = 0x7fffffff;
     }
-    for (int base = rlo; base < rhi; base += 32) {
-      const int r[4] = {base + g, base + g + 8, base + 16 + g, base + 24 + g};
-      KRow<DK, F8> A[4];
+    constexpr int TPI = F8 ? 2 : 1;              // as in k_full_scan
+    for (int base0 = rlo; base0 < rhi; base0 += 32 * TPI) {
+      int rr[TPI][4];
+      KRow<DK, F8> AA[TPI][4];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const long long row = (r[t] < rhi) ? entry_row(p.cache, s, r[t], &g_err_index) : -1;
-        load_row<DK, F8>(p.cache, row, A[t]);
-      }
+      for (int tt = 0; tt < TPI; ++tt)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          rr[tt][t] = base0 + 32 * tt + 8 * t + g;
+          const long long row = (rr[tt][t] < rhi) ? entry_row(p.cache, s, rr[tt][t], &g_err_index) : -1;
+          load_row<DK, F8>(p.cache, row, AA[tt][t]);
+        }
+#pragma unroll
+      for (int tt = 0; tt < TPI; ++tt) {
+      const int* r = rr[tt];
+      const KRow<DK, F8>* A = AA[tt];
       // lane (g, c) owns candidate row base + g + 8c (a permutation of the 32 rows)
       int ci = r[0];
 #pragma unroll
@@ -408,6 +425,7 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
           if (c == t) cv = sc[t];
         const bool mine = ci >= lo[q] && ci < hi[q];
         topp_offer(mine ? cv : -INFINITY, mine ? ci : 0x7fffffff, p.P, tv[q], ti[q], thv[q], thi[q]);
+      }
       }
     }
 #pragma unroll
@@ -554,7 +572,9 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     //      of 32 positions; lane (g, c) owns rows g + 8u of a tile.  While a tile's rows
     //      are loading, the next tile's rows are resolved (pool id -> page table) and the
     //      pool ids of the tile after that are fetched.
-    constexpr int NT = CL_SLICE / 32 / (CL_THREADS / 32);   // tiles per warp: 8
+    constexpr int TPI = F8 ? 2 : 1;               // tiles of 32 positions per iteration, as in the scan
+    constexpr int U = 4 * TPI;                     // rows per lane per iteration
+    constexpr int NT = CL_SLICE / (32 * TPI) / (CL_THREADS / 32);   // iterations per warp: 8 (bf16), 4 (FP8)
     const int g = lane >> 2, c = lane & 3;
     const int sq = __ldg(sp.seq_of + b);
     // as in the Full scan: more than two head groups stream their Q fragments from L1
@@ -566,55 +586,60 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     const float* wb = (F8 ? sp.w8 : sp.w) + (long long)b * sp.H_i;
     QFrag<DK, NHG_REG, F8> f;
     if (!STREAM_Q) load_qfrag<DK, NHG_REG, F8>(qb, wb, sp.H_i, f);
-    auto pos_of = [&](int it, int u) { return s0 + 32 * (warp + 8 * it) + g + 8 * u; };
+    auto pos_of = [&](int it, int u) { return s0 + 32 * TPI * (warp + 8 * it) + g + 8 * u; };
     auto fetch_ent = [&](int it, int* e) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int pos = pos_of(it, u);
         e[u] = (it < NT && pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
       }
     };
     auto resolve = [&](int it, const int* e, long long* rw) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < U; ++u) {
         const int pos = pos_of(it, u);
         if (it < NT && pos < e1 && c == 0) sent[pos - s0] = e[u];
         rw[u] = (e[u] >= 0) ? entry_row(sp.cache, sq, e[u], &g_err_index) : -1;
       }
     };
-    int en[4];
-    long long rw[4];
+    int en[U];
+    long long rw[U];
     fetch_ent(0, en);
     resolve(0, en, rw);
     fetch_ent(1, en);
 #pragma unroll 1
-    for (int it = 0; it < NT && s0 + 32 * (warp + 8 * it) < e1; ++it) {
-      KRow<DK, F8> A[4];
+    for (int it = 0; it < NT && s0 + 32 * TPI * (warp + 8 * it) < e1; ++it) {
+      KRow<DK, F8> A[U];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) load_row<DK, F8>(sp.cache, rw[u], A[u]);
+      for (int u = 0; u < U; ++u) load_row<DK, F8>(sp.cache, rw[u], A[u]);
       resolve(it + 1, en, rw);                            // next tile, while these rows load
       fetch_ent(it + 2, en);
-      float sc[4];
-      if (STREAM_Q) {
-        sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+      float sc[U];
+#pragma unroll
+      for (int tt = 0; tt < TPI; ++tt) {
+        float* st = sc + 4 * tt;
+        const KRow<DK, F8>* At = A + 4 * tt;
+        if (STREAM_Q) {
+          st[0] = st[1] = st[2] = st[3] = 0.f;
 #pragma unroll 1
-        for (int hg = 0; hg < NHG; ++hg) {
-          load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, sp.H_i - hg * 8, f);
-          float x0, x1, x2, x3;
-          tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], sp.relu != 0, x0, x1);
-          tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], sp.relu != 0, x2, x3);
-          sc[0] += x0;
-          sc[1] += x1;
-          sc[2] += x2;
-          sc[3] += x3;
+          for (int hg = 0; hg < NHG; ++hg) {
+            load_qfrag<DK, NHG_REG, F8>(qb + hg * 8 * DK * QB, wb + hg * 8, sp.H_i - hg * 8, f);
+            float x0, x1, x2, x3;
+            tile_scores<DK, NHG_REG, F8>(f, At[0], At[1], sp.relu != 0, x0, x1);
+            tile_scores<DK, NHG_REG, F8>(f, At[2], At[3], sp.relu != 0, x2, x3);
+            st[0] += x0;
+            st[1] += x1;
+            st[2] += x2;
+            st[3] += x3;
+          }
+        } else {
+          tile_scores<DK, NHG_REG, F8>(f, At[0], At[1], sp.relu != 0, st[0], st[1]);
+          tile_scores<DK, NHG_REG, F8>(f, At[2], At[3], sp.relu != 0, st[2], st[3]);
         }
-      } else {
-        tile_scores<DK, NHG_REG, F8>(f, A[0], A[1], sp.relu != 0, sc[0], sc[1]);
-        tile_scores<DK, NHG_REG, F8>(f, A[2], A[3], sp.relu != 0, sc[2], sc[3]);
       }
       if (c == 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
           const int pos = pos_of(it, u);
           if (pos < e1) sscore[pos - s0] = sc[u];
         }

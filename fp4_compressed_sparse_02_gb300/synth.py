@@ -103,6 +103,9 @@ DEC128K_V6 = dict(name="decoder_N131072_B32x6", N=131072, m=1, d=512, d_model=51
                   d_ik=128, NB=2048, P=8, k=512, W=128, B=32, G=6, d_rope=64)
 DEC1M = dict(name="decoder_N1048576_B64", N=1048576, m=1, d=512, d_model=5120, Hq=64, H_i=8,
              d_ik=128, NB=2048, P=8, k=512, W=128, B=64, d_rope=64)
+# the same decode workloads with the compressed (FP8) indexer-K form
+DEC128K_IK8 = dict(DEC128K, name="decoder_N131072_B32_ik8", ik8=True)
+DEC1M_IK8 = dict(DEC1M, name="decoder_N1048576_B64_ik8", ik8=True)
 PREFILL = dict(name="encoder_prefill_T65536", T=65536, m=2, d=512, d_model=5120, Hq=64, H_i=8,
                d_ik=128, NB=2048, P=8, k=512, W=128, Q=8192, d_rope=64)
 PAGE = 64

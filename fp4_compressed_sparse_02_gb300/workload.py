@@ -61,18 +61,25 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
         page_table[b, :u] = perm[o:o + u]
         o += u
     page_table = page_table.to(device)
+    ik8 = bool(cfg.get("ik8"))
     cache = csa2.PagedCache(
         codes=torch.empty((num_pages, 64, d // 2), dtype=torch.uint8, device=device),
         scales=torch.empty((num_pages, 64, d // 16), dtype=torch.uint8, device=device),
-        idx_k=torch.empty((num_pages, 64, d_ik), dtype=torch.bfloat16, device=device),
-        page_table=page_table)
+        idx_k=None if ik8 else torch.empty((num_pages, 64, d_ik), dtype=torch.bfloat16, device=device),
+        page_table=page_table,
+        idx_k8=torch.empty((num_pages, 64, d_ik), dtype=torch.uint8, device=device) if ik8 else None,
+        idx_k8_scale=torch.empty((num_pages, 64), dtype=torch.float32, device=device) if ik8 else None)
     for p0 in range(0, num_pages, chunk_pages):
         p1 = min(num_pages, p0 + chunk_pages)
         cache.codes[p0:p1] = torch.randint(0, 256, (p1 - p0, 64, d // 2), generator=g, device=device,
                                            dtype=torch.uint8)
         cache.scales[p0:p1] = torch.randint(0x20, 0x40, (p1 - p0, 64, d // 16), generator=g, device=device,
                                             dtype=torch.uint8)
-        cache.idx_k[p0:p1] = _randn_bf16((p1 - p0, 64, d_ik), g, device)
+        if ik8:
+            cache.idx_k8[p0:p1] = _fp8_rows((p1 - p0) * 64, d_ik, g, device).view(p1 - p0, 64, d_ik)
+            cache.idx_k8_scale[p0:p1] = torch.rand((p1 - p0, 64), generator=g, device=device) * 0.015 + 0.005
+        else:
+            cache.idx_k[p0:p1] = _randn_bf16((p1 - p0, 64, d_ik), g, device)
     seq_of = torch.arange(B, dtype=torch.int32, device=device).repeat_interleave(G)
     nq = [n - G + 1 + t for n in Ns for t in range(G)]
     n_vis = torch.tensor(nq, dtype=torch.int32, device=device)
@@ -101,7 +108,7 @@ def build_decode(cfg, B=None, N=None, seed=0, device="cuda", append=True, schedu
         rope = (torch.from_numpy(cos).to(device), torch.from_numpy(sin).to(device))
     step = DecodeStep(cache, seq_of, n_vis, N, layers, NB, P, k, W, append=app, rope=rope, group=G)
     info = dict(B=Q, G=G, seqs=B, N=N, Ns=Ns, layers=len(sched), schedule=sched, d=d, d_ik=d_ik, H_i=H_i, Hq=Hq,
-                W=W, k=k, NB=NB, P=P, d_model=d_model, d_rope=d_rope)
+                W=W, k=k, NB=NB, P=P, d_model=d_model, d_rope=d_rope, ik8=ik8)
     return step, info
 
 
@@ -191,21 +198,23 @@ def algorithmic_bytes(info):
     """Bytes a decode step must move at minimum (each byte read or written once):
 
     append     : H row (d_model*2) + W_kv + W_ik once (shared by the batch) + the new
-                 entry (d/2 + d/16 + 2*d_ik) per query
-    Full       : n*2*d_ik of indexer K (once per group of G queries of a sequence) + q_idx
+                 entry (d/2 + d/16 + ik) per query
+    Full       : n*ik of indexer K (once per group of G queries of a sequence) + q_idx
                  + w + pool (4*NB*P) + topk (4k) per query
-    Reindex    : pool*(2*d_ik) gathered indexer K + pool ids (4*NB*P) + q_idx + w + topk
+    Reindex    : pool*ik gathered indexer K + pool ids (4*NB*P) + q_idx + w + topk
+    (ik = the bytes of one entry's indexer K: 2*d_ik in bf16, d_ik + 4 in the FP8 form)
     attention  : k*(d/2 + d/16) FP4 rows + W*(d + 4) SWA rows + q (2*Hq*d)
                  + out (2*Hq*d) + topk ids (4k) per query-layer
     """
     B, N, d, d_ik, H_i, Hq, W, k = (info[x] for x in ("B", "N", "d", "d_ik", "H_i", "Hq", "W", "k"))
     pool = info["NB"] * info["P"]
     G = info.get("G", 1)
+    ik = d_ik + 4 if info.get("ik8") else 2 * d_ik
 
     def per_query(n):
         q = {}
-        q["full"] = n * 2 * d_ik // G + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
-        q["reindex"] = min(n, pool) * 2 * d_ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
+        q["full"] = n * ik // G + 2 * H_i * d_ik + 4 * H_i + 4 * pool + 4 * k
+        q["reindex"] = min(n, pool) * ik + 4 * pool + 2 * H_i * d_ik + 4 * H_i + 4 * k
         q["attn"] = k * (d // 2 + d // 16) + W * (d + 4) + 2 * Hq * d * 2 + 4 * k
         return q
 
@@ -221,17 +230,21 @@ def algorithmic_bytes(info):
             tot += G * q["attn"]
     app = 0
     if info.get("append", True):
-        app = B * (info["d_model"] * 2 + d // 2 + d // 16 + 2 * d_ik) + info["d_model"] * d * 2 + d * d_ik * 2
+        app = B * (info["d_model"] * 2 + d // 2 + d // 16 + ik) + info["d_model"] * d * 2 + d * d_ik * 2
     return dict(total=tot + app, per_query=per_q, append=app)
 
 
 def host_sequence(step, b, n):
-    """Entries [0, n) of sequence b (codes, scales, idx_k bits) copied to the host."""
-    pt = step.cache.page_table[b].cpu().numpy()
+    """Entries [0, n) of query b's sequence copied to the host: (codes, scales, indexer K),
+    the indexer K as bf16 bits, or as (E4M3 bytes, float32 scales) in the FP8 form."""
+    pt = step.cache.page_table[int(step.seq_of[b].item())].cpu().numpy()
     e = np.arange(n)
     pages = torch.from_numpy(pt[e // 64].astype(np.int64)).to(step.cache.codes.device)
     slots = torch.from_numpy(e % 64).to(step.cache.codes.device)
     codes = step.cache.codes[pages, slots].cpu().numpy()
     scales = step.cache.scales[pages, slots].cpu().numpy()
-    idxk = step.cache.idx_k[pages, slots].view(torch.int16).cpu().numpy().view(np.uint16)
+    if step.cache.idx_k8 is not None:
+        idxk = (step.cache.idx_k8[pages, slots].cpu().numpy(), step.cache.idx_k8_scale[pages, slots].cpu().numpy())
+    else:
+        idxk = step.cache.idx_k[pages, slots].view(torch.int16).cpu().numpy().view(np.uint16)
     return codes, scales, idxk
