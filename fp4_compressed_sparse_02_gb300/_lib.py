@@ -61,7 +61,7 @@ class SwaQuantArgs(ctypes.Structure):
 
 
 STATUS = {0: "OK", 1: "ERR_INVALID_ARG", 2: "ERR_UNSUPPORTED_SHAPE", 3: "ERR_WORKSPACE_TOO_SMALL",
-          4: "ERR_CUDA", 5: "ERR_DEVICE_CHECK"}
+          4: "ERR_CUDA", 5: "ERR_DEVICE_CHECK", 6: "ERR_TIMEOUT"}
 
 EXPORTS = ["csa2_compress_quant", "csa2_compress_quant_workspace", "csa2_index_full",
            "csa2_index_full_workspace", "csa2_index_reindex", "csa2_index_reindex_workspace",

@@ -325,7 +325,11 @@ csa2_status csa2_get_device_error(uint32_t* word) {
   if (e != cudaSuccess) return cuda_status(e, "csa2_get_device_error");
   *word = csa2::read_clear_error_compress() | csa2::read_clear_error_proj() | csa2::read_clear_error_index() |
           csa2::read_clear_error_score() | csa2::read_clear_error_attn();
-  return cuda_status(cudaGetLastError(), "csa2_get_device_error");
+  csa2_status s = cuda_status(cudaGetLastError(), "csa2_get_device_error");
+  if (s != CSA2_OK) return s;
+  if (*word & CSA2_DEVERR_TIMEOUT) return fail(CSA2_ERR_TIMEOUT, "a bounded wait gave up (device word 0x%x)", *word);
+  if (*word) return fail(CSA2_ERR_DEVICE_CHECK, "a device-side check failed (device word 0x%x)", *word);
+  return CSA2_OK;
 }
 
 int32_t csa2_version(void) { return 100; }

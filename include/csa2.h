@@ -46,7 +46,8 @@ typedef enum csa2_status {
   CSA2_ERR_UNSUPPORTED_SHAPE = 2,  /* a size outside the supported set below */
   CSA2_ERR_WORKSPACE_TOO_SMALL = 3,
   CSA2_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed */
-  CSA2_ERR_DEVICE_CHECK = 5        /* the device error word was non-zero */
+  CSA2_ERR_DEVICE_CHECK = 5,       /* csa2_get_device_error: the word had a bounds-check bit */
+  CSA2_ERR_TIMEOUT = 6             /* csa2_get_device_error: the word had CSA2_DEVERR_TIMEOUT */
 } csa2_status;
 
 /* Element types.  CSA2_FP8E4M3 selects the compressed indexer-K plane (csa2_cache);
@@ -405,8 +406,12 @@ csa2_status csa2_swa_quant(const csa2_swa_quant_args* args, void* stream);
 /* Thread-local description of the last failed call ("" if none). */
 const char* csa2_last_error_message(void);
 
-/* Synchronises the current device, returns the device error word (CSA2_DEVERR_* bits)
- * accumulated since the last read, and clears it.  For tests and debugging: it blocks. */
+/* Synchronises the current device, stores the device error word (CSA2_DEVERR_* bits)
+ * accumulated since the last read in *word, and clears it.  Returns CSA2_OK for a zero
+ * word, CSA2_ERR_TIMEOUT when the word has CSA2_DEVERR_TIMEOUT, CSA2_ERR_DEVICE_CHECK
+ * when it has any other bit (CSA2_ERR_CUDA if the synchronisation failed; *word is then
+ * not written).  For tests and debugging: it blocks.  The word is per device, not per
+ * stream, so the call takes no stream. */
 csa2_status csa2_get_device_error(uint32_t* word);
 
 /* Library version: major*10000 + minor*100 + patch. */

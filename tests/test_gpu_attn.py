@@ -206,7 +206,11 @@ def test_swa_window_outside_rows_is_flagged():
 def test_bounded_wait_times_out_reports_and_context_survives():
     # a wait that nothing satisfies gives up, sets the timeout bit and returns
     csa2.selftest_wait_timeout(1000)
-    assert csa2.device_error() & 0x80
+    import ctypes
+    from fp4_compressed_sparse_02_gb300 import _lib
+    word = ctypes.c_uint32(0)
+    assert _lib.lib().csa2_get_device_error(ctypes.byref(word)) == 6      # CSA2_ERR_TIMEOUT
+    assert word.value & 0x80
     assert csa2.device_error() == 0                 # the word was cleared by the read
     # the context is still usable: a normal call right after runs and agrees
     r = np.random.default_rng(55)
