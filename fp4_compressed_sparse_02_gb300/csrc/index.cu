@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(256, 2) k_full_scan_g(ScanParams p) {
       thv[q] = -INFINITY;
       thi[q] = 0x7fffffff;
     }
-    constexpr int TPI = F8 ? 2 : 1;              // as in k_full_scan
+    constexpr int TPI = 1;                       // each row is scored G times: compute, not bytes, bounds it
     for (int base0 = rlo; base0 < rhi; base0 += 32 * TPI) {
       int rr[TPI][4];
       KRow<DK, F8> AA[TPI][4];
@@ -572,7 +572,9 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     //      of 32 positions; lane (g, c) owns rows g + 8u of a tile.  While a tile's rows
     //      are loading, the next tile's rows are resolved (pool id -> page table) and the
     //      pool ids of the tile after that are fetched.
-    constexpr int TPI = F8 ? 2 : 1;               // tiles of 32 positions per iteration, as in the scan
+    // tiles of 32 positions per iteration: two for the FP8 form's half-size rows (as in the
+    // scan), one when several head groups need the registers
+    constexpr int TPI = (F8 && NHG == 1) ? 2 : 1;
     constexpr int U = 4 * TPI;                     // rows per lane per iteration
     constexpr int NT = CL_SLICE / (32 * TPI) / (CL_THREADS / 32);   // iterations per warp: 8 (bf16), 4 (FP8)
     const int g = lane >> 2, c = lane & 3;
