@@ -45,7 +45,7 @@ class AttnArgs(ctypes.Structure):
                 ("cache", Cache), ("seq_of", c_vp), ("topk", c_vp), ("topk_len", c_vp), ("k", c_i32),
                 ("swa", c_vp), ("swa_scale", c_vp), ("swa_rows", c_i32), ("swa_start", c_vp),
                 ("swa_len", c_vp), ("swa_max", c_i32), ("softmax_scale", ctypes.c_float),
-                ("out", c_vp), ("out_dtype", c_i32), ("lse", c_vp)]
+                ("out", c_vp), ("out_dtype", c_i32), ("lse", c_vp), ("inputs_ready", c_i32)]
 
 
 class AppendArgs(ctypes.Structure):

@@ -247,9 +247,11 @@ def index_reindex(cache: PagedCache, q_idx, w, seq_of, pool, pool_len, k=512, re
 
 
 def sparse_attn(cache: PagedCache, q, seq_of, topk, topk_len, swa, swa_scale, swa_start, swa_len, swa_max,
-                softmax_scale=None, out_dtype=torch.bfloat16, out=None, lse=None, ws=None):
+                softmax_scale=None, out_dtype=torch.bfloat16, out=None, lse=None, ws=None, inputs_ready=False):
     """One softmax over the selected FP4 entries plus the SWA window.  q bf16 [B, Hq, d].
-    Returns (out [B, Hq, d], lse float32 [B, Hq])."""
+    inputs_ready: the kernel launched just before on the stream writes none of this call's
+    inputs (a Reuse layer after the previous layer's attention), so the call may read them
+    before that kernel completes.  Returns (out [B, Hq, d], lse float32 [B, Hq])."""
     B, Hq, d = q.shape
     dev = q.device
     if softmax_scale is None:
@@ -271,6 +273,7 @@ def sparse_attn(cache: PagedCache, q, seq_of, topk, topk_len, swa, swa_scale, sw
     a.out = _ptr(out)
     a.out_dtype = F32 if out.dtype == torch.float32 else BF16
     a.lse = _ptr(lse)
+    a.inputs_ready = int(bool(inputs_ready))
     _call("csa2_sparse_attn", a, ws, dev)
     return out, lse
 

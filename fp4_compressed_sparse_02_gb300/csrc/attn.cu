@@ -51,6 +51,10 @@ struct AttnParams {
   void* out;
   int out_f32;
   float* lse;
+  int early;                      // inputs_ready: read and compute before waiting on the
+                                  // previous kernel, wait only before the first write.  The
+                                  // wait returns once that kernel (and so, transitively, every
+                                  // earlier one) has completed, so all writes stay ordered.
 };
 
 // byte offset of 16-byte chunk `ch` of row `row` in a swizzled tile of `rowbytes`
@@ -118,7 +122,7 @@ struct ACfg {
 
 template <int DIM, int MT>
 __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
-  pdl_wait();
+  if (!p.early) pdl_wait();         // otherwise the wait comes before the first write (below)
   pdl_trigger();
   using C = ACfg<DIM, MT>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -397,6 +401,7 @@ __global__ void __launch_bounds__(ATHREADS, 1) k_attn_chunk(AttnParams p) {
     }
   }
   // ---- 7. partial outputs (the probability factor 2^-G undone) ------------------------
+  if (p.early) pdl_wait();          // the workspace may still be read by the previous kernel
   const long long pbase = ((long long)b * p.nchunk + chunk) * p.Hq;
   if (r0 < p.Hq) {
     float* o = p.opart + (pbase + r0) * DIM + dbase + 2 * c;
@@ -516,7 +521,7 @@ __device__ __forceinline__ bool wait_mma(uint64_t* mbar, uint32_t parity) {
 __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS, 1)
     k_attn_tc(AttnParams p, const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
               const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap wmap) {
-  pdl_wait();
+  if (!p.early) pdl_wait();         // otherwise the wait comes before the merge's writes
   pdl_trigger();
   using namespace tca;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -959,6 +964,7 @@ __global__ void __cluster_dims__(tca::NCH, 1, 1) __launch_bounds__(tca::THREADS,
   __syncthreads();
   // ---- merge: CTA r combines the 4 chunks of heads [16 r, 16 r + 16) from its Q space
   //      (slot c = chunk c) -------------------------------------------------------------
+  if (p.early) pdl_wait();          // the first global write of the kernel comes next
   {
     float* wts = reinterpret_cast<float*>(&pmax[0][0]);       // [16][NCH] merge weights
     if (tid < 16) {
@@ -1172,6 +1178,7 @@ cudaError_t launch_attn(const csa2_attn_args& a, void* ws, cudaStream_t st) {
   ap.out = a.out;
   ap.out_f32 = a.out_dtype == CSA2_F32;
   ap.lse = a.lse;
+  ap.early = a.inputs_ready != 0;
   const int mt = (a.Hq + 15) / 16;
   if (a.cache.d == 512 && a.Hq == 64 && a.k <= tca::NCH * tca::KT && a.swa_max <= tca::NCH * tca::KW &&
       (long long)a.cache.num_pages * 64 < (1ll << 31) && tensor_map_encoder() != nullptr && !attn_force_legacy())

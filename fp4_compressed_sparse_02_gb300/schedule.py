@@ -75,12 +75,18 @@ class DecodeStep:
             csa2.index_reindex(self.cache, L["q_idx"], L["w"], self.seq_of, self.pool, self.pool_len, self.k,
                                out=(self.topk[i], self.topk_len[i]), ws=self.ws)
 
-    def run_attn(self, i):
-        """The sparse attention of layer i over its own (or the reused) index set."""
+    def run_attn(self, i, after_attn=None):
+        """The sparse attention of layer i over its own (or the reused) index set.  A Reuse
+        layer runs right after the previous layer's attention, which writes none of its
+        inputs, so it may start reading them before that kernel completes (after_attn: whether
+        the kernel just before on the stream is that attention; by default, for Reuse layers)."""
         L = self.layers[i]
         tk, tl = self.result_topk(i)
+        if after_attn is None:
+            after_attn = L["mode"] == REUSE and i > 0
         csa2.sparse_attn(self.cache, L["q"], self.seq_of, tk, tl, L["swa"], L["swa_scale"], L["swa_start"],
-                         L["swa_len"], self.swa_max, out=self.out[i], lse=self.lse[i], ws=self.ws)
+                         L["swa_len"], self.swa_max, out=self.out[i], lse=self.lse[i], ws=self.ws,
+                         inputs_ready=after_attn)
 
     def _last_topk(self, i):
         for j in range(i - 1, -1, -1):

@@ -365,6 +365,15 @@ typedef struct csa2_attn_args {
   void* out;                   /* device [B][Hq][d] */
   csa2_dtype out_dtype;
   float* lse;                  /* device f32 [B][Hq], or NULL */
+  int32_t inputs_ready;        /* 1: none of this call's inputs (q, topk, topk_len, seq_of, the
+                                  cache, the window rows and scales) is written by a kernel launched
+                                  on the stream since the last library call made without this flag
+                                  -- e.g. a Reuse layer's attention after the attention calls of the
+                                  layers since the last index call, which write only their own
+                                  outputs.  The call then reads and computes while those kernels
+                                  finish, and waits for them only before its first write (so its
+                                  writes stay in stream order).  0: it waits before its first
+                                  read, as every other call does. */
 } csa2_attn_args;
 
 csa2_status csa2_sparse_attn(const csa2_attn_args* args, void* workspace,
