@@ -262,7 +262,7 @@ __device__ __forceinline__ void topp_write(const ScanParams& p, int b, int j, in
 }
 
 template <int DK, int NHG, bool F8>
-__global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
+__global__ void __launch_bounds__(256, 2) k_full_scan(ScanParams p) {
   pdl_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -304,12 +304,20 @@ __global__ void __launch_bounds__(256) k_full_scan(ScanParams p) {
   for (long long base = lo; base < hi; base += 32 * TPI) {
     long long r[TPI][4];
     KRow<DK, F8> A[TPI][4];
+    // lane (g, c) resolves row 8c + g of each tile through the page table; the four lanes of
+    // a quad then share their rows (each row is loaded in slices by a whole quad)
+    int mine[TPI];
+#pragma unroll
+    for (int tt = 0; tt < TPI; ++tt) {
+      const long long rr = base + 32 * tt + 8 * c + g;
+      mine[tt] = (rr < hi) ? (int)entry_row(p.cache, s, rr, &g_err_index) : -1;
+    }
 #pragma unroll
     for (int tt = 0; tt < TPI; ++tt)
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         r[tt][t] = base + 32 * tt + 8 * t + g;
-        const long long row = (r[tt][t] < hi) ? entry_row(p.cache, s, r[tt][t], &g_err_index) : -1;
+        const int row = __shfl_sync(FULL_MASK, mine[tt], (lane & ~3) | t);
         load_row<DK, F8>(p.cache, row, A[tt][t]);
       }
 #pragma unroll
@@ -589,23 +597,25 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     QFrag<DK, NHG_REG, F8> f;
     if (!STREAM_Q) load_qfrag<DK, NHG_REG, F8>(qb, wb, sp.H_i, f);
     auto pos_of = [&](int it, int u) { return s0 + 32 * TPI * (warp + 8 * it) + g + 8 * u; };
+    // lane (g, c) fetches the pool ids of rows u = c + 4v (v < TPI) and resolves them; the
+    // four lanes of a quad share the rows (each row is loaded in slices by a whole quad)
     auto fetch_ent = [&](int it, int* e) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int pos = pos_of(it, u);
-        e[u] = (it < NT && pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
+      for (int v = 0; v < TPI; ++v) {
+        const int pos = pos_of(it, c + 4 * v);
+        e[v] = (it < NT && pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
       }
     };
-    auto resolve = [&](int it, const int* e, long long* rw) {
+    auto resolve = [&](int it, const int* e, int* rw) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int pos = pos_of(it, u);
-        if (it < NT && pos < e1 && c == 0) sent[pos - s0] = e[u];
-        rw[u] = (e[u] >= 0) ? entry_row(sp.cache, sq, e[u], &g_err_index) : -1;
+      for (int v = 0; v < TPI; ++v) {
+        const int pos = pos_of(it, c + 4 * v);
+        if (it < NT && pos < e1) sent[pos - s0] = e[v];
+        rw[v] = (e[v] >= 0) ? (int)entry_row(sp.cache, sq, e[v], &g_err_index) : -1;
       }
     };
-    int en[U];
-    long long rw[U];
+    int en[TPI];
+    int rw[TPI];
     fetch_ent(0, en);
     resolve(0, en, rw);
     fetch_ent(1, en);
@@ -613,7 +623,8 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     for (int it = 0; it < NT && s0 + 32 * TPI * (warp + 8 * it) < e1; ++it) {
       KRow<DK, F8> A[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) load_row<DK, F8>(sp.cache, rw[u], A[u]);
+      for (int u = 0; u < U; ++u)
+        load_row<DK, F8>(sp.cache, __shfl_sync(FULL_MASK, rw[u >> 2], (lane & ~3) | (u & 3)), A[u]);
       resolve(it + 1, en, rw);                            // next tile, while these rows load
       fetch_ent(it + 2, en);
       float sc[U];

@@ -320,3 +320,42 @@ def test_attn_q_full_range(B, Hq, d, k, W):
     ref, rlse = _oracle(c)
     _assert_close_per_head(out, ref, "Q range")
     _lse_close(lse, rlse)
+
+
+@pytest.mark.parametrize("shape", [(40, 64, 512, 512, 128), (6, 8, 128, 64, 32)])
+def test_attn_inputs_ready_matches_the_ordered_call(shape):
+    # Reuse layers: calls after an attention call that writes none of their inputs start
+    # before it completes; their results equal the ordinary calls' bit for bit, eagerly and
+    # replayed from a CUDA graph, and their outputs are written after the previous call's
+    B, Hq, d, k, W = shape
+    r = np.random.default_rng(990 + d)
+    c = _case(r, B, Hq, d, k, W, n=3000)
+    args = [c["cache"], bf16_dev(c["q"]), to_dev(c["seq_of"]), to_dev(c["topk"]), to_dev(c["tlen"]),
+            to_dev(c["swa"]), to_dev(c["swa_scale"]), to_dev(c["swa_start"]), to_dev(c["swa_len"]), W]
+    ref, rlse = csa2.sparse_attn(*args, out_dtype=torch.float32)
+    outs = [torch.full((B, Hq, d), float("nan"), device="cuda") for _ in range(3)]
+    lses = [torch.empty((B, Hq), device="cuda") for _ in range(3)]
+    ws = csa2.Workspace()
+
+    def chain():
+        for i in range(3):
+            csa2.sparse_attn(*args, out_dtype=torch.float32, out=outs[i], lse=lses[i], ws=ws, inputs_ready=i > 0)
+
+    chain()
+    torch.cuda.synchronize()
+    assert csa2.device_error() == 0
+    for o, l in zip(outs, lses):
+        assert torch.equal(o, ref) and torch.equal(l, rlse)
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        chain()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=st):
+        chain()
+    for o in outs:
+        o.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    for o, l in zip(outs, lses):
+        assert torch.equal(o, ref) and torch.equal(l, rlse)
