@@ -191,6 +191,15 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   return r;
 }
 
+// The same for scattered rows shorter than 256 bytes: no L2 prefetch beyond the requested
+// 128-byte line (the 256-byte hint would double the DRAM bytes of a 128-byte row).
+__device__ __forceinline__ uint4 ldg_gather_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::128B.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
 // 32-byte streaming load (p 32-byte aligned) into two 16-byte halves: half the load
 // requests of two 16-byte loads for the same bytes.
 __device__ __forceinline__ void ldg_stream_v8(const void* p, uint4& lo, uint4& hi) {

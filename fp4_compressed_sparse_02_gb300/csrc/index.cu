@@ -71,14 +71,17 @@ __device__ __forceinline__ void load_qfrag(const void* __restrict__ qv, const fl
   }
 }
 
-// Load the thread's slices of one cache row (zeros when row < 0).
-template <int DK, bool F8>
+// Load the thread's slices of one cache row (zeros when row < 0).  SEQ: rows of a sequential
+// run (the scan: the 256-byte L2 prefetch serves the next row too); otherwise scattered rows
+// (Reindex), whose FP8 rows are 128 bytes: no prefetch past the row.
+template <int DK, bool F8, bool SEQ = true>
 __device__ __forceinline__ void load_row(const csa2_cache& cache, long long row, KRow<DK, F8>& a) {
   const int c = threadIdx.x & 3;
   if constexpr (F8) {
     const uint8_t* p = cache.idx_k8 + row * DK + (DK / 4) * c;
 #pragma unroll
-    for (int j = 0; j < DK / 64; ++j) a.v[j] = (row >= 0) ? ldg_stream_v4(p + 16 * j) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < DK / 64; ++j)
+      a.v[j] = (row >= 0) ? (SEQ ? ldg_stream_v4(p + 16 * j) : ldg_gather_v4(p + 16 * j)) : make_uint4(0, 0, 0, 0);
     a.s = (row >= 0) ? __ldg(cache.idx_k8_scale + row) : 0.f;
   } else {
 #pragma unroll
@@ -624,7 +627,7 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
       KRow<DK, F8> A[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        load_row<DK, F8>(sp.cache, __shfl_sync(FULL_MASK, rw[u >> 2], (lane & ~3) | (u & 3)), A[u]);
+        load_row<DK, F8, false>(sp.cache, __shfl_sync(FULL_MASK, rw[u >> 2], (lane & ~3) | (u & 3)), A[u]);
       resolve(it + 1, en, rw);                            // next tile, while these rows load
       fetch_ent(it + 2, en);
       float sc[U];
