@@ -74,15 +74,18 @@ __device__ __forceinline__ void load_qfrag(const void* __restrict__ qv, const fl
 // Load the thread's slices of one cache row (zeros when row < 0).  SEQ: rows of a sequential
 // run (the scan: the 256-byte L2 prefetch serves the next row too); otherwise scattered rows
 // (Reindex), whose FP8 rows are 128 bytes: no prefetch past the row.
+// In the FP8 form the row's scale is given (loaded once by the lane that resolved the row);
+// a negative `scale` asks for the load here.
 template <int DK, bool F8, bool SEQ = true>
-__device__ __forceinline__ void load_row(const csa2_cache& cache, long long row, KRow<DK, F8>& a) {
+__device__ __forceinline__ void load_row(const csa2_cache& cache, long long row, KRow<DK, F8>& a,
+                                         float scale = -1.f) {
   const int c = threadIdx.x & 3;
   if constexpr (F8) {
     const uint8_t* p = cache.idx_k8 + row * DK + (DK / 4) * c;
 #pragma unroll
     for (int j = 0; j < DK / 64; ++j)
       a.v[j] = (row >= 0) ? (SEQ ? ldg_stream_v4(p + 16 * j) : ldg_gather_v4(p + 16 * j)) : make_uint4(0, 0, 0, 0);
-    a.s = (row >= 0) ? __ldg(cache.idx_k8_scale + row) : 0.f;
+    a.s = (row < 0) ? 0.f : (scale >= 0.f ? scale : __ldg(cache.idx_k8_scale + row));
   } else {
 #pragma unroll
     for (int j = 0; j < DK / 32; ++j)
@@ -310,18 +313,21 @@ __global__ void __launch_bounds__(256, 2) k_full_scan(ScanParams p) {
     // lane (g, c) resolves row 8c + g of each tile through the page table; the four lanes of
     // a quad then share their rows (each row is loaded in slices by a whole quad)
     int mine[TPI];
+    float msc[TPI];                                // FP8 form: the resolved row's scale
 #pragma unroll
     for (int tt = 0; tt < TPI; ++tt) {
       const long long rr = base + 32 * tt + 8 * c + g;
       mine[tt] = (rr < hi) ? (int)entry_row(p.cache, s, rr, &g_err_index) : -1;
+      msc[tt] = (F8 && mine[tt] >= 0) ? __ldg(p.cache.idx_k8_scale + mine[tt]) : 0.f;
     }
 #pragma unroll
     for (int tt = 0; tt < TPI; ++tt)
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         r[tt][t] = base + 32 * tt + 8 * t + g;
-        const int row = __shfl_sync(FULL_MASK, mine[tt], (lane & ~3) | t);
-        load_row<DK, F8>(p.cache, row, A[tt][t]);
+        const int src = (lane & ~3) | t;
+        const int row = __shfl_sync(FULL_MASK, mine[tt], src);
+        load_row<DK, F8>(p.cache, row, A[tt][t], F8 ? __shfl_sync(FULL_MASK, msc[tt], src) : -1.f);
       }
 #pragma unroll
     for (int tt = 0; tt < TPI; ++tt) {
@@ -609,26 +615,31 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
         e[v] = (it < NT && pos < e1) ? __ldg(sp.pool + rowb + pos) : -1;
       }
     };
-    auto resolve = [&](int it, const int* e, int* rw) {
+    auto resolve = [&](int it, const int* e, int* rw, float* rs) {
 #pragma unroll
       for (int v = 0; v < TPI; ++v) {
         const int pos = pos_of(it, c + 4 * v);
         if (it < NT && pos < e1) sent[pos - s0] = e[v];
         rw[v] = (e[v] >= 0) ? (int)entry_row(sp.cache, sq, e[v], &g_err_index) : -1;
+        rs[v] = (F8 && rw[v] >= 0) ? __ldg(sp.cache.idx_k8_scale + rw[v]) : 0.f;
       }
     };
     int en[TPI];
     int rw[TPI];
+    float rs[TPI];                                 // FP8 form: the resolved rows' scales
     fetch_ent(0, en);
-    resolve(0, en, rw);
+    resolve(0, en, rw, rs);
     fetch_ent(1, en);
 #pragma unroll 1
     for (int it = 0; it < NT && s0 + 32 * TPI * (warp + 8 * it) < e1; ++it) {
       KRow<DK, F8> A[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        load_row<DK, F8, false>(sp.cache, __shfl_sync(FULL_MASK, rw[u >> 2], (lane & ~3) | (u & 3)), A[u]);
-      resolve(it + 1, en, rw);                            // next tile, while these rows load
+      for (int u = 0; u < U; ++u) {
+        const int src = (lane & ~3) | (u & 3);
+        load_row<DK, F8, false>(sp.cache, __shfl_sync(FULL_MASK, rw[u >> 2], src), A[u],
+                                F8 ? __shfl_sync(FULL_MASK, rs[u >> 2], src) : -1.f);
+      }
+      resolve(it + 1, en, rw, rs);                        // next tile, while these rows load
       fetch_ent(it + 2, en);
       float sc[U];
 #pragma unroll
