@@ -33,7 +33,8 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // (launch_k), or without it (launch_k_late: the kernel starts only once the previous
 // kernel has completed, and its pdl_wait() is a no-op).  The cluster Top-k is launched
 // late: its 8-CTA clusters placed early on the few SMs a running attention leaves idle
-// pack worse than on an empty GPU.
+// pack worse than on an empty GPU.  So are the persistent kernels (the Full scan, the
+// tensor-core scoring and projection), whose grids are sized to fill an empty GPU.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                             Args&&... args) {

@@ -503,8 +503,8 @@ cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, bool fuse
       if (e != cudaSuccess) return e;
       attr_set = true;
     }
-    return launch_k(k_proj_tc<true>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N, ntn,
-                    ntiles, ep);
+    return launch_k_late(k_proj_tc<true>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d,
+                         N, ntn, ntiles, ep);
   }
   static bool attr_set = false;
   if (!attr_set) {
@@ -512,8 +512,9 @@ cudaError_t launch_project_tc(const csa2_compress_args& a, float* out, bool fuse
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_k(k_proj_tc<false>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N, ntn,
-                  ntiles, ep);
+  // persistent (one CTA per SM): started only once the previous kernel has completed
+  return launch_k_late(k_proj_tc<false>, grid, ptc::THREADS, ptc::SMEM, st, mh, mkv, mz, out, a.T, a.d_model, d, N,
+                       ntn, ntiles, ep);
 }
 
 uint32_t read_clear_error_proj() {

@@ -488,7 +488,8 @@ static cudaError_t launch_score(const CUtensorMap& kmap, const CUtensorMap& qmap
     attr_set = true;
   }
   const int grid = std::max(1, std::min(p.units, sms));
-  return launch_k(k_score_tc<HI>, grid, stc::THREADS, smem, st, kmap, qmap, p);
+  // persistent (one CTA per SM): started only once the previous kernel has completed
+  return launch_k_late(k_score_tc<HI>, grid, stc::THREADS, smem, st, kmap, qmap, p);
 }
 
 cudaError_t launch_full_scores_tc(const csa2_index_full_args& a, float* S, float* pool_score, cudaStream_t st) {
