@@ -61,6 +61,7 @@ def bf16_peak():
 PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
             ("k_attn_tc", "decode1m"): ("k_attn_tc_decode1m.md", "attn.cu"),
             ("k_full_scan", "decode1m"): ("k_full_scan_decode1m.md", "index.cu"),
+            ("k_full_scan", "decode1m_ik8"): ("k_full_scan_decode1m_ik8.md", "index.cu"),
             ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu"),
             ("k_select_cl_reindex", "decode128k"): ("k_select_cl_reindex_decode128k.md", "index.cu"),
             ("k_proj_tc", "prefill_compress"): ("k_proj_tc_prefill_compress.md", "proj_tc.cu"),
