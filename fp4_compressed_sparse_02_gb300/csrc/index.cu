@@ -541,22 +541,145 @@ __device__ __forceinline__ void hist_add_warp(int* hist, int bin, int cnt) {
   if (active && !same) atomicAdd(&hist[bin], cnt);
 }
 
+// The cluster radix select's digits, from the top of the 32-bit key: 11, 11 and 10 bits.  A
+// histogram is summed over the cluster in two steps, so that the distributed-shared-memory
+// traffic stays at one word per thread and CTA: its 256 super-bins (8 or 4 bins each) first,
+// then the bins of the one super-bin that holds the wanted key.
+__host__ __device__ constexpr int radix_shift(int pass) { return pass == 0 ? 21 : pass == 1 ? 10 : 0; }
+__host__ __device__ constexpr int radix_bins(int pass) { return pass == 2 ? 1024 : 2048; }
+
+// One pass of the cluster's radix select: count the live keys (those whose resolved bits equal
+// `prefix`) by this pass's digit into `hb` (zeroed), sum the NCL CTAs' histograms through
+// distributed shared memory and find the digit of the `remaining`-th largest live key.  `sup`
+// receives this CTA's super-bin sums, `tot` is scratch for 256 sums.
+// Returns true when every live key with that digit is selected (the digit's count equals what
+// remains): the bits below it then decide nothing and the later passes are skipped.  Every CTA
+// of the cluster computes the same totals, so all take the same decision.
+template <int PASS>
+__device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const uint32_t (&key)[CL_PER_T], int q0,
+                                           int e1, uint32_t& prefix, uint32_t& mask, int& remaining, int* pick) {
+  constexpr int SHIFT = radix_shift(PASS), NB = radix_bins(PASS), SB = NB / CL_THREADS;   // bins per super-bin
+  const int tid = threadIdx.x;
+  {
+    // this thread's keys in the digit of its first live key are counted once; the rest one by one
+    int b0 = 0, c0 = 0;
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < CL_PER_T; ++i) {
+      const bool live = q0 + i < e1 && (key[i] & mask) == prefix;
+      const int bi = (int)((key[i] >> SHIFT) & (NB - 1));
+      if (live && !any) { b0 = bi; any = true; }
+      c0 += (live && bi == b0) ? 1 : 0;
+    }
+    hist_add_warp(hb, b0, c0);
+#pragma unroll
+    for (int i = 0; i < CL_PER_T; ++i) {
+      const int bi = (int)((key[i] >> SHIFT) & (NB - 1));
+      if (q0 + i < e1 && (key[i] & mask) == prefix && bi != b0) atomicAdd(&hb[bi], 1);
+    }
+  }
+  // super-bin t (thread t's) = bins [NB - SB (t + 1), NB - SB t): thread 0 has the top bins
+  __syncthreads();                                        // this CTA's histogram is complete
+  {
+    const int4* h4 = reinterpret_cast<const int4*>(hb + NB - SB * (tid + 1));
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < SB / 4; ++j) {
+      const int4 v = h4[j];
+      sum += v.x + v.y + v.z + v.w;
+    }
+    sup[tid] = sum;
+  }
+  tc::cluster_sync();                                     // every CTA's counts are complete
+  {
+    const uint32_t a = smem_u32(sup + tid);
+    int sum = 0;
+#pragma unroll
+    for (int cc = 0; cc < NCL; ++cc) sum += tc::ld_dsmem_s32(tc::mapa(a, cc));
+    tot[tid] = sum;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // warp 0 scans the 256 super-bin totals from the top, 8 a lane
+    int c8[8], local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { c8[i] = tot[8 * tid + i]; local += c8[i]; }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL_MASK, incl, o);
+      if (tid >= o) incl += y;
+    }
+    int sstar = -1, before = 0;
+    if (incl - local < remaining && remaining <= incl) {
+      int cum = incl - local;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (cum < remaining && cum + c8[i] >= remaining) { sstar = 8 * tid + i; before = cum; }
+        cum += c8[i];
+      }
+    }
+    const int src = __ffs(__ballot_sync(FULL_MASK, sstar >= 0)) - 1;   // exactly one lane
+    sstar = __shfl_sync(FULL_MASK, sstar, src);
+    before = __shfl_sync(FULL_MASK, before, src);
+    // the SB bins of super-bin s*, summed over the cluster: lane l < NJ * NCL loads 4 bins
+    // (4 j .. 4 j + 3, j = l % NJ) of CTA l / NJ, and the lanes with the same j are summed
+    constexpr int NJ = SB / 4;
+    static_assert(SB % 4 == 0 && NJ * NCL <= 32, "one 4-bin load a lane");
+    const int lo = NB - SB * (sstar + 1), j = tid % NJ;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tid < NJ * NCL) v = tc::ld_dsmem_v4(tc::mapa(smem_u32(hb + lo + 4 * j), (uint32_t)(tid / NJ)));
+    int x[4] = {(int)v.x, (int)v.y, (int)v.z, (int)v.w};
+#pragma unroll
+    for (int o = NJ; o < 32; o <<= 1)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] += __shfl_xor_sync(FULL_MASK, x[i], o);
+    int bin[SB];
+#pragma unroll
+    for (int jj = 0; jj < NJ; ++jj)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) bin[4 * jj + i] = __shfl_sync(FULL_MASK, x[i], jj);
+    if (tid == 0) {
+      int cum = before;
+#pragma unroll
+      for (int i = SB - 1; i >= 0; --i) {
+        if (cum < remaining && cum + bin[i] >= remaining) {
+          pick[0] = lo + i;
+          pick[1] = remaining - cum;
+          pick[2] = bin[i];
+        }
+        cum += bin[i];
+      }
+    }
+  }
+  __syncthreads();
+  prefix |= ((uint32_t)pick[0]) << SHIFT;
+  mask |= (uint32_t)(NB - 1) << SHIFT;
+  remaining = pick[1];
+  // (pick and tot are next written after the next pass's cluster barrier, once every thread
+  //  of this CTA has read them)
+  return pick[2] == remaining;
+}
+
 template <int DK, int NHG, bool SCORE, bool F8>
 __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_select_cl(SelectParams p, PoolScoreParams sp) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float sscore[SCORE ? CL_SLICE : 1];
-  __shared__ int sent[SCORE ? CL_SLICE : 1];        // pool entries of the slice (Reindex)
-  __shared__ int hist[4][256];                      // one per radix pass, zeroed at entry
-  __shared__ int total[256];
+  // Reindex: the slice's scores and pool entries (2,048 each); once they are in registers,
+  // the histograms of the first two passes (2,048 bins each)
+  __shared__ __align__(16) int sbuf[2 * CL_SLICE];
+  float* sscore = reinterpret_cast<float*>(sbuf);
+  int* sent = sbuf + CL_SLICE;
+  __shared__ __align__(16) int hist2[1024];         // the third pass's histogram
+  __shared__ int sup[3][256];                       // each pass's super-bin sums
+  __shared__ int tot[256];                          // scratch of the passes
   __shared__ int scan_sh[32];
-  __shared__ int pick[2];
+  __shared__ int pick[3];
   __shared__ int xfer;                              // this CTA's packed (above, equal) count
   __shared__ int base_sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b = blockIdx.y;
   const int rank = (int)tc::cluster_ctarank();
-  for (int i = tid; i < 4 * 256; i += CL_THREADS) (&hist[0][0])[i] = 0;
   int P;
   if (p.n_vis) {
     int n = __ldg(p.n_vis + b);
@@ -584,6 +707,7 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     return;                                               // the same in every CTA of the cluster
   }
   const int e1 = min(s1, P);                              // valid positions [s0, e1)
+  for (int i = tid; i < 1024; i += CL_THREADS) hist2[i] = 0;
   if constexpr (SCORE) {
     // ---- score this CTA's slice of the pool (Reindex).  Warp w owns tiles w, w+8, ...
     //      of 32 positions; lane (g, c) owns rows g + 8u of a tile.  While a tile's rows
@@ -678,91 +802,55 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   uint32_t key[CL_PER_T];
   int ent[CL_PER_T];
   const int q0 = s0 + tid * CL_PER_T;
+  {
+    // Reindex: the slice's positions q0 - s0 .. + 7 in two 16-byte loads of each array
+    float sv[CL_PER_T];
+    if constexpr (SCORE) {
+      const float4* s4 = reinterpret_cast<const float4*>(sscore + (q0 - s0));
+      const int4* e4 = reinterpret_cast<const int4*>(sent + (q0 - s0));
 #pragma unroll
-  for (int i = 0; i < CL_PER_T; ++i) {
-    const int q = q0 + i;
-    float sv = 0.f;
-    ent[i] = -1;
-    if (q < e1) {
-      sv = SCORE ? sscore[q - s0] : __ldg(p.score + rowb + q);
-      ent[i] = SCORE ? sent[q - s0] : __ldg(p.pool + rowb + q);
+      for (int h = 0; h < 2; ++h) {
+        const float4 a = s4[h];
+        const int4 c = e4[h];
+        sv[4 * h] = a.x; sv[4 * h + 1] = a.y; sv[4 * h + 2] = a.z; sv[4 * h + 3] = a.w;
+        ent[4 * h] = c.x; ent[4 * h + 1] = c.y; ent[4 * h + 2] = c.z; ent[4 * h + 3] = c.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < CL_PER_T; ++i) {
+        sv[i] = q0 + i < e1 ? __ldg(p.score + rowb + q0 + i) : 0.f;
+        ent[i] = q0 + i < e1 ? __ldg(p.pool + rowb + q0 + i) : -1;
+      }
     }
-    key[i] = (q < e1) ? float_key(sv) : 0u;
+#pragma unroll
+    for (int i = 0; i < CL_PER_T; ++i) {
+      if (q0 + i >= e1) ent[i] = -1;
+      key[i] = (q0 + i < e1) ? float_key(sv[i]) : 0u;
+    }
   }
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    int* hb = hist[pass];
-    // this thread's keys in the digit of its first live key are counted once; the rest
-    // (rare in the leading digits) one by one
-    int b0 = 0, c0 = 0;
-    bool any = false;
-#pragma unroll
-    for (int i = 0; i < CL_PER_T; ++i) {
-      const bool live = q0 + i < e1 && (key[i] & mask) == prefix;
-      const int bi = (int)((key[i] >> shift) & 255u);
-      if (live && !any) { b0 = bi; any = true; }
-      c0 += (live && bi == b0) ? 1 : 0;
-    }
-    hist_add_warp(hb, b0, c0);
-#pragma unroll
-    for (int i = 0; i < CL_PER_T; ++i) {
-      const int bi = (int)((key[i] >> shift) & 255u);
-      if (q0 + i < e1 && (key[i] & mask) == prefix && bi != b0) atomicAdd(&hb[bi], 1);
-    }
-    tc::cluster_sync();                                   // every CTA's histogram is complete
-    {
-      const uint32_t ha = smem_u32(&hb[tid]);
-      int tsum = 0;
-#pragma unroll
-      for (int cc = 0; cc < NCL; ++cc) tsum += tc::ld_dsmem_s32(tc::mapa(ha, cc));
-      total[tid] = tsum;
-    }
-    __syncthreads();
-    if (tid < 32) {
-      int cnt[8], local = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { cnt[i] = total[255 - 8 * tid - i]; local += cnt[i]; }
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(FULL_MASK, incl, o);
-        if (tid >= o) incl += y;
-      }
-      const int excl = incl - local;
-      if (excl < remaining && remaining <= incl) {
-        int cum = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (cum + cnt[i] >= remaining) {
-            pick[0] = 255 - 8 * tid - i;
-            pick[1] = remaining - cum;
-            break;
-          }
-          cum += cnt[i];
-        }
-      }
-    }
-    __syncthreads();
-    prefix |= ((uint32_t)pick[0]) << shift;
-    mask |= 0xFFu << shift;
-    remaining = pick[1];
-  }
-  // ---- output slots from one scan of (keys above the threshold, keys equal to it):
-  //      ties at the threshold go to the lowest positions, cluster-wide ---------------------
+  __syncthreads();                                        // every key is in registers: sbuf
+  for (int i = tid; i < 2 * CL_SLICE; i += CL_THREADS) sbuf[i] = 0;   // becomes two histograms
+  __syncthreads();
+  bool done = radix_pass<0>(sbuf, sup[0], tot, key, q0, e1, prefix, mask, remaining, pick);
+  if (!done) done = radix_pass<1>(sbuf + 2048, sup[1], tot, key, q0, e1, prefix, mask, remaining, pick);
+  if (!done) radix_pass<2>(hist2, sup[2], tot, key, q0, e1, prefix, mask, remaining, pick);
+  // ---- output slots from one scan of (keys above the threshold, keys equal to it), keys
+  //      compared on the bits the passes resolved: ties at the threshold go to the lowest
+  //      positions, cluster-wide (when the passes stopped early, every key equal on those
+  //      bits is taken) ---------------------------------------------------------------------
   int gt = 0, eq = 0;
 #pragma unroll
   for (int i = 0; i < CL_PER_T; ++i) {
     if (q0 + i < e1) {
-      gt += key[i] > prefix ? 1 : 0;
-      eq += key[i] == prefix ? 1 : 0;
+      gt += (key[i] & mask) > prefix ? 1 : 0;
+      eq += (key[i] & mask) == prefix ? 1 : 0;
     }
   }
-  int tot;
-  const int ex = block_exclusive_scan(gt | (eq << 16), scan_sh, tot);   // counts < 2^15
-  if (tid == 0) xfer = tot;
+  int packed;
+  const int ex = block_exclusive_scan(gt | (eq << 16), scan_sh, packed);   // counts < 2^15
+  if (tid == 0) xfer = packed;
   tc::cluster_sync();
   if (tid == 0) {
     int bsum = 0;
@@ -775,7 +863,8 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   int o = (before & 0xffff) + min(er, remaining);
 #pragma unroll
   for (int i = 0; i < CL_PER_T; ++i) {
-    if (q0 + i < e1 && (key[i] > prefix || (key[i] == prefix && er++ < remaining))) {
+    const uint32_t km = key[i] & mask;
+    if (q0 + i < e1 && (km > prefix || (km == prefix && er++ < remaining))) {
       if (o < k) out[o] = ent[i];
       ++o;
     }
