@@ -192,6 +192,12 @@ __device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
   return r;
 }
 
+// Bring `bytes` (a multiple of 16) from the 16-byte aligned global address p into L2 with one
+// bulk request (nothing is returned to the thread): later loads of those bytes hit L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 // The same for scattered rows shorter than 256 bytes: no L2 prefetch beyond the requested
 // 128-byte line (the 256-byte hint would double the DRAM bytes of a 128-byte row).
 __device__ __forceinline__ uint4 ldg_gather_v4(const void* p) {
