@@ -229,6 +229,65 @@ def test_exact_ties_break_to_lower_index():
         np.testing.assert_array_equal(topk[b, :tlen[b]], rtopk)
 
 
+def _exact_score_problem(r, n, kinds):
+    """Indexer K rows whose scores are exact in float32 whatever the summation order: every
+    head's q is (1, 2^-12, 0, ...), every weight 1/8, and row i holds (A_i, B_i) in its first
+    two dims (integers, exact in bf16) and random values elsewhere, so that its score is
+    A_i + B_i / 4096.  kinds[s] picks sequence s's (A, B): 'low' -- A in {200, 201}, B in
+    [0, 256): thousands of keys share their top 22 bits and ties are exact; 'spread' -- A in
+    [1, 256), B = 0; 'flat' -- every score equal."""
+    d_ik, H_i = 128, 8
+    mp = (n + 63) // 64
+    pt = synth.page_table(r, len(kinds), mp)
+    K = []
+    for kind in kinds:
+        Kb = synth.bf16_normal(r, (n, d_ik)).astype(np.float32)
+        if kind == "low":
+            A, Bv = r.integers(200, 202, n), r.integers(0, 256, n)
+        elif kind == "spread":
+            A, Bv = r.integers(1, 256, n), np.zeros(n, np.int64)
+        else:
+            A, Bv = np.full(n, 37), np.full(n, 5)
+        Kb[:, 0], Kb[:, 1] = A, Bv
+        K.append(synth.bf16_bits_from_f32(Kb))
+    cache = csa2.PagedCache.allocate(len(kinds), n, 512, d_ik, "cuda", torch.from_numpy(pt))
+    cache.idx_k.copy_(bf16_dev(logical_to_paged(K, pt, len(kinds) * mp, d_ik, np.uint16)))
+    qh = np.zeros((len(kinds), H_i, d_ik), np.float32)
+    qh[:, :, 0], qh[:, :, 1] = 1.0, 2.0 ** -12
+    q = synth.bf16_bits_from_f32(qh)
+    w = np.full((len(kinds), H_i), 0.125, np.float32)
+    return cache, K, q, w
+
+
+def test_select_resolves_every_key_bit():
+    # scores exact on both sides, so the pool and the Top-k must equal the oracle's bit for
+    # bit: the radix select must resolve keys that agree on their top 22 bits (all three of
+    # its passes), stop early when a digit's keys are all taken, and break exact ties by
+    # position, in the Full scan's select and in Reindex
+    r = np.random.default_rng(25)
+    NB, P, k, n = 2048, 8, 512, 40000
+    kinds = ["low", "spread", "flat"]
+    cache, K, q, w = _exact_score_problem(r, n, kinds)
+    B = len(kinds)
+    seq_of = np.arange(B, dtype=np.int32)
+    n_vis = np.array([n, n - 777, n], dtype=np.int32)
+    pool, plen, topk, tlen = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
+    for b in range(B):
+        Kb = formats.bf16_value(K[b][:n_vis[b]])
+        rpool, rtopk, _ = indexer.full(formats.bf16_value(q[b]), w[b].astype(np.float64), Kb, NB, P, k)
+        np.testing.assert_array_equal(pool[b, :plen[b]], rpool, err_msg=kinds[b])
+        np.testing.assert_array_equal(topk[b, :tlen[b]], rtopk, err_msg=kinds[b])
+    # Reindex over the same pools
+    q2 = q.copy()
+    topk2, tlen2 = csa2.index_reindex(cache, bf16_dev(q2), to_dev(w), to_dev(seq_of), to_dev(pool), to_dev(plen), k)
+    assert csa2.device_error() == 0
+    topk2, tlen2 = topk2.cpu().numpy(), tlen2.cpu().numpy()
+    for b in range(B):
+        Kb = formats.bf16_value(K[b])
+        rt, _ = indexer.reindex(formats.bf16_value(q2[b]), w[b].astype(np.float64), Kb, pool[b, :plen[b]], k)
+        np.testing.assert_array_equal(topk2[b, :tlen2[b]], rt, err_msg=kinds[b])
+
+
 def test_reindex_matches_oracle():
     r = np.random.default_rng(30)
     NB, P, k, d_ik, H_i = 2048, 8, 512, 128, 8
