@@ -204,6 +204,7 @@ csa2_status check_swa_quant(const csa2_swa_quant_args* a) {
 csa2_status check_ws(size_t need, void* ws, size_t have) {
   REQUIRE(have >= need, CSA2_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes, got %zu", need, have);
   REQUIRE(need == 0 || ws, CSA2_ERR_INVALID_ARG, "workspace is NULL");
+  REQUIRE(need == 0 || ((uintptr_t)ws & 255) == 0, CSA2_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   return CSA2_OK;
 }
 

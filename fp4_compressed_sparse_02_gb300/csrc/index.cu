@@ -1092,9 +1092,10 @@ static size_t pool_score_bytes(const csa2_index_full_args& a) {
 size_t index_full_workspace_bytes(const csa2_index_full_args& a) {
   // pool scores, then (tensor-core scoring) the score matrix, or (FP8 form) the quantised
   // indexer Q and weights
+  // (the score matrix starts 256-byte aligned: its rows are read in 16-byte loads)
   if (a.cache.idx_k_dtype == CSA2_FP8E4M3) return pool_score_bytes(a) + q8_total(a.B, a.H_i, a.cache.d_ik);
-  const size_t pool = (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
-  return pool + (full_scores_tc_chosen(a) ? full_scores_tc_bytes(a) : 0);
+  if (full_scores_tc_chosen(a)) return pool_score_bytes(a) + full_scores_tc_bytes(a);
+  return (size_t)a.B * a.num_blocks * a.per_block * sizeof(float);
 }
 
 cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStream_t st, bool allow_tc) {
@@ -1136,8 +1137,7 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
       launch_scan_dk<64, true>(sp, nhg, units, st);
     }
   } else if (allow_tc && full_scores_tc_chosen(a)) {     // groups of queries of one sequence: a dense product
-    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (size_t)a.B * a.num_blocks * a.per_block *
-                                                                        sizeof(float));
+    float* S = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pool_score_bytes(a));
     cudaError_t e = launch_full_scores_tc(a, S, static_cast<float*>(ws), st);
     if (e != cudaSuccess) return e;
   } else if (group > 1 && group <= 8 && a.H_i <= 8) {

@@ -318,14 +318,22 @@ __global__ void __launch_bounds__(BT_WARPS * 32) k_block_topp(const float* __res
   const int e1 = __shfl_sync(0xffffffffu, hi, min(31, NB - 1 - j0));
   const float* s = S + (long long)b * ldS;
   float* w = bt_sh + warp * wfloats;
-  // the warp's slice, eight loads in flight per lane
-  for (int e = e0 + lane; e < e1; e += 256) {
-    float v[8];
+  // the warp's slice in 16-byte loads, four in flight a lane (a score row starts 16-byte
+  // aligned and is a whole number of 128-entry tiles long, so a load that starts below e1
+  // stays inside the row)
+  for (int e = (e0 & ~3) + 4 * lane; e < e1; e += 512) {
+    float4 v[4];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = (e + 32 * u < e1) ? __ldg(s + e + 32 * u) : 0.f;
+    for (int u = 0; u < 4; ++u)
+      v[u] = (e + 128 * u < e1) ? __ldg(reinterpret_cast<const float4*>(s + e + 128 * u)) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      if (e + 32 * u < e1) w[bt_pad(e + 32 * u - e0)] = v[u];
+    for (int u = 0; u < 4; ++u) {
+      const int eu = e + 128 * u;
+      const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (eu + c >= e0 && eu + c < e1) w[bt_pad(eu + c - e0)] = x[c];
+    }
   }
   __syncwarp();
   if (j >= NB) return;

@@ -14,6 +14,10 @@
  *     library never allocates, frees or keeps device memory between calls (except one
  *     4-byte error word per device, see csa2_get_device_error, and the fixed score
  *     array of csa2_index_full_noalloc).
+ *   - A call that takes a workspace (a device buffer of at least the bytes its *_workspace
+ *     function reports, owned by the caller and free for the library's use until the
+ *     call's work on the stream has completed) wants it 256-byte aligned: a misaligned
+ *     workspace is rejected with CSA2_ERR_INVALID_ARG.
  *   - Every compute call is asynchronous on the given cudaStream_t (passed as void*;
  *     NULL = legacy default stream) and never synchronises.
  *   - Arguments are validated on the host before any launch; a failed check returns a

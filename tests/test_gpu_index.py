@@ -346,3 +346,25 @@ def test_n_vis_beyond_max_n_is_flagged():
     n_vis = np.array([1000], dtype=np.int32)
     csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(np.zeros(1, np.int32)), to_dev(n_vis), 900, 64, 8, 64)
     assert csa2.device_error() & 0x4
+
+
+class _OffsetWorkspace(csa2.Workspace):
+    """A workspace whose buffer starts 16 bytes past an aligned allocation."""
+
+    def get(self, nbytes):
+        return super().get(nbytes + 16)[16:]
+
+
+def test_misaligned_workspace_is_rejected():
+    r = np.random.default_rng(40)
+    cache, K, q, w = _setup(r, 1, 3000, 128, 8, 2)
+    n_vis = np.array([3000, 2000], dtype=np.int32)
+    outs = [torch.full((2, 16384), -7, dtype=torch.int32, device="cuda"),
+            torch.full((2,), -7, dtype=torch.int32, device="cuda"),
+            torch.full((2, 512), -7, dtype=torch.int32, device="cuda"),
+            torch.full((2,), -7, dtype=torch.int32, device="cuda")]
+    with pytest.raises(csa2._lib.Csa2Error, match="256-byte aligned"):
+        csa2.index_full(cache, bf16_dev(q), to_dev(w), to_dev(np.zeros(2, np.int32)), to_dev(n_vis), 3000,
+                        out=outs, ws=_OffsetWorkspace("cuda"))
+    torch.cuda.synchronize()
+    assert all((o == -7).all() for o in outs)           # nothing was launched
