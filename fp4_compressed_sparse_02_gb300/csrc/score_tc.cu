@@ -283,9 +283,11 @@ __global__ void __launch_bounds__(stc::THREADS, 1)
 
 // Best per_block entries of every block of every query from the score matrix.  A warp takes
 // 32 consecutive blocks of one query: it copies their scores (at most 64 per block) into
-// shared memory with coalesced loads, then lane i keeps the best of block i and writes them
-// to the pool (and their scores to pool_score) in ascending entry order, at the offsets of
-// the scan kernels.  "Best" = larger score, then lower entry.
+// shared memory with coalesced loads, then lane i keeps the best of block i in ascending entry
+// order, at the offsets of the scan kernels.  "Best" = larger score, then lower entry.  The 32
+// blocks' kept entries form one contiguous run of the pool (P per block, or every entry when
+// the query has fewer than P x NB), so they are staged in shared memory and written with
+// coalesced stores (per-lane stores of P consecutive words made the kernel twice as slow).
 constexpr int BT_WARPS = 4;
 // A warp's scores sit in shared memory with one pad word after every 32, so that lanes
 // walking blocks of ~16 entries side by side read distinct banks.
@@ -317,7 +319,9 @@ __global__ void __launch_bounds__(BT_WARPS * 32) k_block_topp(const float* __res
   const int e0 = __shfl_sync(0xffffffffu, lo, 0);
   const int e1 = __shfl_sync(0xffffffffu, hi, min(31, NB - 1 - j0));
   const float* s = S + (long long)b * ldS;
-  float* w = bt_sh + warp * wfloats;
+  float* w = bt_sh + warp * (wfloats + 64 * P);
+  int* oid = reinterpret_cast<int*>(w + wfloats);      // the warp's kept entries, then scores
+  float* osc = w + wfloats + 32 * P;
   // the warp's slice in 16-byte loads, four in flight a lane (a score row starts 16-byte
   // aligned and is a whole number of 128-entry tiles long, so a load that starts below e1
   // stays inside the row)
@@ -336,14 +340,14 @@ __global__ void __launch_bounds__(BT_WARPS * 32) k_block_topp(const float* __res
     }
   }
   __syncwarp();
-  if (j >= NB) return;
   // the P best values, descending: each score bubbles down the sorted list (a later
   // entry never displaces an equal earlier one, so this is the best-first order of the
-  // tie rule "larger score, then lower entry")
+  // tie rule "larger score, then lower entry"); lanes past NB have no entries
   float kv[P];
 #pragma unroll
   for (int i = 0; i < P; ++i) kv[i] = -INFINITY;
-  for (int e = lo; e < hi; ++e) {
+  const int cnt = j < NB ? hi - lo : 0;
+  for (int e = lo; e < lo + cnt; ++e) {
     float v = w[bt_pad(e - e0)];
 #pragma unroll
     for (int i = 0; i < P; ++i) {
@@ -352,8 +356,6 @@ __global__ void __launch_bounds__(BT_WARPS * 32) k_block_topp(const float* __res
       kv[i] = t;
     }
   }
-  const int cnt = hi - lo;
-  if (cnt <= 0) return;
   // kept: every entry above the P-th best tv, then entries equal to tv in ascending order
   // up to P in all; a block of fewer than P entries keeps them all
   const float tv = (cnt >= P) ? kv[P - 1] : -INFINITY;
@@ -361,15 +363,23 @@ __global__ void __launch_bounds__(BT_WARPS * 32) k_block_topp(const float* __res
 #pragma unroll
   for (int i = 0; i < P; ++i) quota -= (kv[i] > tv) ? 1 : 0;
   const long long off = ((long long)n >= (long long)P * NB) ? (long long)P * j : lo;
-  const long long o = (long long)b * NB * P + off;
+  const long long off0 = __shfl_sync(0xffffffffu, off, 0);   // lane 0's block is below NB
+  const int loc = (int)(off - off0);
   int c = 0;
-  for (int e = lo; e < hi; ++e) {                     // ascending entries that are kept
+  for (int e = lo; e < lo + cnt; ++e) {               // ascending entries that are kept
     const float v = w[bt_pad(e - e0)];
     if (v > tv || (v == tv && quota-- > 0)) {
-      pool[o + c] = e;
-      pool_score[o + c] = v;
+      oid[loc + c] = e;
+      osc[loc + c] = v;
       ++c;
     }
+  }
+  const int total = __reduce_max_sync(0xffffffffu, cnt > 0 ? loc + c : 0);
+  __syncwarp();
+  const long long o = (long long)b * NB * P + off0;
+  for (int i = lane; i < total; i += 32) {
+    pool[o + i] = oid[i];
+    pool_score[o + i] = osc[i];
   }
 }
 
@@ -544,7 +554,7 @@ cudaError_t launch_full_scores_tc(const csa2_index_full_args& a, float* S, float
     const long long warps = (long long)a.B * ((a.num_blocks + 31) / 32);
     const unsigned grid2 = (unsigned)((warps + BT_WARPS - 1) / BT_WARPS);
     const int wfloats = bt_warp_floats(per_blk);
-    const size_t smem2 = (size_t)BT_WARPS * wfloats * sizeof(float);
+    const size_t smem2 = (size_t)BT_WARPS * (wfloats + 64 * a.per_block) * sizeof(float);
     switch (a.per_block) {                           // the kept list lives in registers
 #define CSA2_BT(PP) \
   case PP: return launch_k(k_block_topp<PP>, grid2, BT_WARPS * 32, smem2, st, S, p.ldS, a.n_vis, a.max_n, a.B, \
