@@ -890,9 +890,10 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
 }
 
 // ---------------------------------------------------------------------------------
-// Top-k of one query's pool by one CTA, for many queries at once (a prefill chunk): the
-// same 4-pass radix select and tie rule as k_select_cl (so the same output), with block
-// barriers instead of the cluster's.  Full mode (scores written by the scan) only.
+// Top-k of one query's pool by one CTA, for many queries at once (a prefill chunk): an MSB
+// radix select of 8-bit digits with block barriers instead of the cluster's, the same tie rule
+// and early stop as k_select_cl (so the same output).  Full mode (scores written by the scan)
+// only.
 // ---------------------------------------------------------------------------------
 constexpr int C1_THREADS = 512;
 constexpr int C1_PER_T = 16384 / C1_THREADS;          // 32 consecutive positions per thread
@@ -901,14 +902,15 @@ constexpr size_t C1_SMEM = (size_t)C1_PER_T * C1_ROW * sizeof(uint32_t);
 
 // The keys live in shared memory (skey[i * C1_ROW + t] = key of position 32 t + i; the pad
 // word keeps both the coalesced fill and the per-thread reads free of bank conflicts), so
-// that two CTAs share an SM and one's loads overlap the other's passes.
-__global__ void __launch_bounds__(C1_THREADS, 2) k_select_cta(SelectParams p) {
+// that several CTAs share an SM and one's loads overlap the others' passes.  Registers are
+// held to 40 a thread for three CTAs an SM (at two, the 8,192 prefill selects took 9 % longer).
+__global__ void __launch_bounds__(C1_THREADS, 3) k_select_cta(SelectParams p) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint32_t skey[];
   __shared__ int hist[4][256];                      // one per radix pass, zeroed at entry
   __shared__ int scan_sh[32];
-  __shared__ int pick[2];
+  __shared__ int pick[3];
   const int tid = threadIdx.x;
   const int b = blockIdx.x;
   for (int i = tid; i < 4 * 256; i += C1_THREADS) (&hist[0][0])[i] = 0;
@@ -983,6 +985,7 @@ __global__ void __launch_bounds__(C1_THREADS, 2) k_select_cta(SelectParams p) {
           if (cum + cnt[i] >= remaining) {
             pick[0] = 255 - 8 * tid - i;
             pick[1] = remaining - cum;
+            pick[2] = cnt[i];
             break;
           }
           cum += cnt[i];
@@ -993,13 +996,16 @@ __global__ void __launch_bounds__(C1_THREADS, 2) k_select_cta(SelectParams p) {
     prefix |= ((uint32_t)pick[0]) << shift;
     mask |= 0xFFu << shift;
     remaining = pick[1];
+    // every key with the picked digit is selected: the bits below decide nothing (the same
+    // value in every thread, so the whole CTA leaves the loop together)
+    if (pick[2] == remaining) break;
   }
-  // output slots from one scan of (keys above the threshold, keys equal to it): ties at the
-  // threshold go to the lowest positions
+  // output slots from one scan of (keys above the threshold, keys equal to it, both on the
+  // resolved bits): ties at the threshold go to the lowest positions
   int gt = 0, eq = 0;
 #pragma unroll 8
   for (int i = 0; i < nv; ++i) {
-    const uint32_t key = skey[i * C1_ROW + tid];
+    const uint32_t key = skey[i * C1_ROW + tid] & mask;
     gt += key > prefix ? 1 : 0;
     eq += key == prefix ? 1 : 0;
   }
@@ -1009,7 +1015,7 @@ __global__ void __launch_bounds__(C1_THREADS, 2) k_select_cta(SelectParams p) {
   int o = (ex & 0xffff) + min(er, remaining);
 #pragma unroll 8
   for (int i = 0; i < nv; ++i) {
-    const uint32_t key = skey[i * C1_ROW + tid];
+    const uint32_t key = skey[i * C1_ROW + tid] & mask;
     if (key > prefix || (key == prefix && er++ < remaining)) {
       if (o < k) out[o] = __ldg(p.pool + rowb + q0 + i);
       ++o;
