@@ -538,9 +538,9 @@ struct SelectParams {
 // memory; otherwise they read the scores the Full scan wrote (and finish the pool).
 // ---------------------------------------------------------------------------------
 constexpr int NCL = 8;
-constexpr int CL_THREADS = 256;
 constexpr int CL_SLICE = 16384 / NCL;                 // 2048
-constexpr int CL_PER_T = CL_SLICE / CL_THREADS;       // 8
+// Threads per CTA (CT): 256, or 128 when a batch's clusters would not fit the GPU at once with
+// 256 (two CTAs an SM by registers, four at 128), so that they run in one wave.
 
 // Histogram increment of `cnt` at `bin` for a warp: the lanes sharing the first active
 // lane's bin add once (in the leading digits most keys share one); the others add their
@@ -559,21 +559,22 @@ __device__ __forceinline__ void hist_add_warp(int* hist, int bin, int cnt) {
 
 // The cluster radix select's digits, from the top of the 32-bit key: 11, 11 and 10 bits.  A
 // histogram is summed over the cluster in two steps, so that the distributed-shared-memory
-// traffic stays at one word per thread and CTA: its 256 super-bins (8 or 4 bins each) first,
-// then the bins of the one super-bin that holds the wanted key.
+// traffic stays at one word per thread and CTA: its CL_THREADS super-bins first, then the bins
+// of the one super-bin that holds the wanted key.
 __host__ __device__ constexpr int radix_shift(int pass) { return pass == 0 ? 21 : pass == 1 ? 10 : 0; }
 __host__ __device__ constexpr int radix_bins(int pass) { return pass == 2 ? 1024 : 2048; }
 
 // One pass of the cluster's radix select: count the live keys (those whose resolved bits equal
 // `prefix`) by this pass's digit into `hb` (zeroed), sum the NCL CTAs' histograms through
 // distributed shared memory and find the digit of the `remaining`-th largest live key.  `sup`
-// receives this CTA's super-bin sums, `tot` is scratch for 256 sums.
+// receives this CTA's super-bin sums, `tot` is scratch for CL_THREADS sums.
 // Returns true when every live key with that digit is selected (the digit's count equals what
 // remains): the bits below it then decide nothing and the later passes are skipped.  Every CTA
 // of the cluster computes the same totals, so all take the same decision.
-template <int PASS>
-__device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const uint32_t (&key)[CL_PER_T], int q0,
+template <int PASS, int CT>
+__device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const uint32_t (&key)[CL_SLICE / CT], int q0,
                                            int e1, uint32_t& prefix, uint32_t& mask, int& remaining, int* pick) {
+  constexpr int CL_THREADS = CT, CL_PER_T = CL_SLICE / CT;
   constexpr int SHIFT = radix_shift(PASS), NB = radix_bins(PASS), SB = NB / CL_THREADS;   // bins per super-bin
   const int tid = threadIdx.x;
   {
@@ -616,10 +617,11 @@ __device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const ui
   }
   __syncthreads();
   if (tid < 32) {
-    // warp 0 scans the 256 super-bin totals from the top, 8 a lane
-    int c8[8], local = 0;
+    // warp 0 scans the super-bin totals from the top, SPL a lane
+    constexpr int SPL = CL_THREADS / 32;
+    int c8[SPL], local = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { c8[i] = tot[8 * tid + i]; local += c8[i]; }
+    for (int i = 0; i < SPL; ++i) { c8[i] = tot[SPL * tid + i]; local += c8[i]; }
     int incl = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -630,8 +632,8 @@ __device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const ui
     if (incl - local < remaining && remaining <= incl) {
       int cum = incl - local;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (cum < remaining && cum + c8[i] >= remaining) { sstar = 8 * tid + i; before = cum; }
+      for (int i = 0; i < SPL; ++i) {
+        if (cum < remaining && cum + c8[i] >= remaining) { sstar = SPL * tid + i; before = cum; }
         cum += c8[i];
       }
     }
@@ -677,8 +679,9 @@ __device__ __forceinline__ bool radix_pass(int* hb, int* sup, int* tot, const ui
   return pick[2] == remaining;
 }
 
-template <int DK, int NHG, bool SCORE, bool F8>
-__global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_select_cl(SelectParams p, PoolScoreParams sp) {
+template <int DK, int NHG, bool SCORE, bool F8, int CT>
+__global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CT, 512 / CT) k_select_cl(SelectParams p, PoolScoreParams sp) {
+  constexpr int CL_THREADS = CT, CL_WARPS = CT / 32, CL_PER_T = CL_SLICE / CT;
   pdl_wait();
   pdl_trigger();
   // Reindex: the slice's scores and pool entries (2,048 each); once they are in registers,
@@ -687,8 +690,8 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   float* sscore = reinterpret_cast<float*>(sbuf);
   int* sent = sbuf + CL_SLICE;
   __shared__ __align__(16) int hist2[1024];         // the third pass's histogram
-  __shared__ int sup[3][256];                       // each pass's super-bin sums
-  __shared__ int tot[256];                          // scratch of the passes
+  __shared__ int sup[3][CL_THREADS];                // each pass's super-bin sums
+  __shared__ int tot[CL_THREADS];                   // scratch of the passes
   __shared__ int scan_sh[32];
   __shared__ int pick[3];
   __shared__ int xfer;                              // this CTA's packed (above, equal) count
@@ -725,7 +728,7 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   const int e1 = min(s1, P);                              // valid positions [s0, e1)
   for (int i = tid; i < 1024; i += CL_THREADS) hist2[i] = 0;
   if constexpr (SCORE) {
-    // ---- score this CTA's slice of the pool (Reindex).  Warp w owns tiles w, w+8, ...
+    // ---- score this CTA's slice of the pool (Reindex).  Warp w owns tiles w, w + CL_WARPS, ...
     //      of 32 positions; lane (g, c) owns rows g + 8u of a tile.  While a tile's rows
     //      are loading, the next tile's rows are resolved (pool id -> page table) and the
     //      pool ids of the tile after that are fetched.
@@ -745,7 +748,7 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     const float* wb = (F8 ? sp.w8 : sp.w) + (long long)b * sp.H_i;
     QFrag<DK, NHG_REG, F8> f;
     if (!STREAM_Q) load_qfrag<DK, NHG_REG, F8>(qb, wb, sp.H_i, f);
-    auto pos_of = [&](int it, int u) { return s0 + 32 * TPI * (warp + 8 * it) + g + 8 * u; };
+    auto pos_of = [&](int it, int u) { return s0 + 32 * TPI * (warp + CL_WARPS * it) + g + 8 * u; };
     // lane (g, c) fetches the pool ids of rows u = c + 4v (v < TPI) and resolves them; the
     // four lanes of a quad share the rows (each row is loaded in slices by a whole quad)
     auto fetch_ent = [&](int it, int* e) {
@@ -771,7 +774,7 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
     resolve(0, en, rw, rs);
     fetch_ent(1, en);
 #pragma unroll 1
-    for (int it = 0; it < NT && s0 + 32 * TPI * (warp + 8 * it) < e1; ++it) {
+    for (int it = 0; it < NT && s0 + 32 * TPI * (warp + CL_WARPS * it) < e1; ++it) {
       KRow<DK, F8> A[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
@@ -819,13 +822,13 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   int ent[CL_PER_T];
   const int q0 = s0 + tid * CL_PER_T;
   {
-    // Reindex: the slice's positions q0 - s0 .. + 7 in two 16-byte loads of each array
+    // Reindex: the slice's positions q0 - s0 .. + CL_PER_T - 1 in 16-byte loads of each array
     float sv[CL_PER_T];
     if constexpr (SCORE) {
       const float4* s4 = reinterpret_cast<const float4*>(sscore + (q0 - s0));
       const int4* e4 = reinterpret_cast<const int4*>(sent + (q0 - s0));
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < CL_PER_T / 4; ++h) {
         const float4 a = s4[h];
         const int4 c = e4[h];
         sv[4 * h] = a.x; sv[4 * h + 1] = a.y; sv[4 * h + 2] = a.z; sv[4 * h + 3] = a.w;
@@ -849,9 +852,9 @@ __global__ void __cluster_dims__(NCL, 1, 1) __launch_bounds__(CL_THREADS, 2) k_s
   __syncthreads();                                        // every key is in registers: sbuf
   for (int i = tid; i < 2 * CL_SLICE; i += CL_THREADS) sbuf[i] = 0;   // becomes two histograms
   __syncthreads();
-  bool done = radix_pass<0>(sbuf, sup[0], tot, key, q0, e1, prefix, mask, remaining, pick);
-  if (!done) done = radix_pass<1>(sbuf + 2048, sup[1], tot, key, q0, e1, prefix, mask, remaining, pick);
-  if (!done) radix_pass<2>(hist2, sup[2], tot, key, q0, e1, prefix, mask, remaining, pick);
+  bool done = radix_pass<0, CT>(sbuf, sup[0], tot, key, q0, e1, prefix, mask, remaining, pick);
+  if (!done) done = radix_pass<1, CT>(sbuf + 2048, sup[1], tot, key, q0, e1, prefix, mask, remaining, pick);
+  if (!done) radix_pass<2, CT>(hist2, sup[2], tot, key, q0, e1, prefix, mask, remaining, pick);
   // ---- output slots from one scan of (keys above the threshold, keys equal to it), keys
   //      compared on the bits the passes resolved: ties at the threshold go to the lowest
   //      positions, cluster-wide (when the passes stopped early, every key equal on those
@@ -1175,7 +1178,7 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
     launch_k(k_select_cta, a.B, C1_THREADS, C1_SMEM, st, sel);
   } else {
     PoolScoreParams none{};
-    launch_k_late(k_select_cl<128, 1, false, false>, dim3(NCL, a.B), CL_THREADS, 0, st, sel, none);
+    launch_k_late(k_select_cl<128, 1, false, false, 256>, dim3(NCL, a.B), 256, 0, st, sel, none);
   }
   return cudaGetLastError();
 }
@@ -1188,11 +1191,21 @@ size_t index_reindex_workspace_bytes(const csa2_index_reindex_args& a) {
 template <int DK, bool F8>
 static void launch_reindex_dk(const SelectParams& sel, const PoolScoreParams& pp, int nhg, int B, cudaStream_t st) {
   const dim3 grid(NCL, B);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // one head group: 128-thread CTAs once the clusters of 256-thread CTAs (two an SM) would need
+  // a second wave (at 1M x 64, 56 against 63 us a call; at 32 queries 256 threads are faster:
+  // 32 against 43 us)
+  if (nhg == 1 && (long long)B * NCL > 2LL * sms) {
+    launch_k_late(k_select_cl<DK, 1, true, F8, 128>, grid, 128, 0, st, sel, pp);
+    return;
+  }
   switch (nhg) {
-    case 1: launch_k_late(k_select_cl<DK, 1, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
-    case 2: launch_k_late(k_select_cl<DK, 2, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
-    case 3: launch_k_late(k_select_cl<DK, 3, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
-    default: launch_k_late(k_select_cl<DK, 4, true, F8>, grid, CL_THREADS, 0, st, sel, pp); break;
+    case 1: launch_k_late(k_select_cl<DK, 1, true, F8, 256>, grid, 256, 0, st, sel, pp); break;
+    case 2: launch_k_late(k_select_cl<DK, 2, true, F8, 256>, grid, 256, 0, st, sel, pp); break;
+    case 3: launch_k_late(k_select_cl<DK, 3, true, F8, 256>, grid, 256, 0, st, sel, pp); break;
+    default: launch_k_late(k_select_cl<DK, 4, true, F8, 256>, grid, 256, 0, st, sel, pp); break;
   }
 }
 
