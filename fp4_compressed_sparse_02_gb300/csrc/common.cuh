@@ -159,6 +159,10 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The low / high two E4M3 bytes of a word as an f16 pair.
+__device__ __forceinline__ uint32_t e4m3x2_lo_f16x2(uint32_t w) { return e4m3x2_to_f16x2((uint16_t)(w & 0xffffu)); }
+__device__ __forceinline__ uint32_t e4m3x2_hi_f16x2(uint32_t w) { return e4m3x2_to_f16x2((uint16_t)(w >> 16)); }
+
 __device__ __forceinline__ void mma_f16_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
                                               uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -41,7 +41,8 @@ struct KRow {
 // bytes and the weights w_h * sq_h quantised by k_quant_q8.
 template <int DK, int NHG, bool F8>
 struct QFrag {
-  uint4 v[NHG][F8 ? DK / 64 : DK / 32];
+  uint4 v[NHG][DK / 32];         // bf16 pairs, or (FP8 form) the E4M3 bytes as f16 pairs: byte
+                                 // pair (2i, 2i + 1) of the lane's 4-byte word w in word 2w + i
   float w[NHG][2];
 };
 
@@ -55,9 +56,14 @@ __device__ __forceinline__ void load_qfrag(const void* __restrict__ qv, const fl
     if constexpr (F8) {
       const uint8_t* q = static_cast<const uint8_t*>(qv);
 #pragma unroll
-      for (int j = 0; j < DK / 64; ++j)
-        f.v[hg][j] = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + (DK / 4) * c + 16 * j))
-                                  : make_uint4(0, 0, 0, 0);
+      for (int j = 0; j < DK / 64; ++j) {
+        const uint4 b = (head < H_i) ? __ldg(reinterpret_cast<const uint4*>(q + head * DK + (DK / 4) * c + 16 * j))
+                                     : make_uint4(0, 0, 0, 0);
+        f.v[hg][2 * j] = make_uint4(e4m3x2_lo_f16x2(b.x), e4m3x2_hi_f16x2(b.x), e4m3x2_lo_f16x2(b.y),
+                                    e4m3x2_hi_f16x2(b.y));
+        f.v[hg][2 * j + 1] = make_uint4(e4m3x2_lo_f16x2(b.z), e4m3x2_hi_f16x2(b.z), e4m3x2_lo_f16x2(b.w),
+                                        e4m3x2_hi_f16x2(b.w));
+      }
     } else {
       const uint16_t* q = static_cast<const uint16_t*>(qv);
 #pragma unroll
@@ -100,9 +106,12 @@ __device__ __forceinline__ uint32_t word_of(const uint4* v, int w) {
 }
 
 // Scores of rows (g) and (g + 8) of a 16-row tile; identical in the 4 lanes of a quad.
-// bf16: m16n8k16 products over dims; FP8: m16n8k32 E4M3 products (exact in float32), the
-// k-slots 4c + i / 16 + 4c + i of step j mapped to the lane's bytes 8j + i / 8j + 4 + i,
-// and the row scale applied after the weighted ReLU sum (both scales are >= 0).
+// bf16: m16n8k16 products over dims.  FP8: the E4M3 bytes converted to f16 pairs (exact) and
+// multiplied by m16n8k16 f16 products (exact in float32): the k-slots 2c, 2c + 1 / 8 + 2c,
+// 9 + 2c of the product for the lane's row word w take its bytes 0, 1 / 2, 3 (Q's bytes in the
+// same places, converted once when the fragment is loaded; the tensor cores here run E4M3
+// mma.sync as f16 products anyway, converting both operands at every product), and the row
+// scale is applied after the weighted ReLU sum (both scales are >= 0).
 template <int DK, int NHG, bool F8>
 __device__ __forceinline__ void tile_scores(const QFrag<DK, NHG, F8>& f, const KRow<DK, F8>& A0,
                                             const KRow<DK, F8>& A1, bool relu, float& s0, float& s1) {
@@ -110,12 +119,20 @@ __device__ __forceinline__ void tile_scores(const QFrag<DK, NHG, F8>& f, const K
 #pragma unroll
   for (int hg = 0; hg < NHG; ++hg) acc[hg][0] = acc[hg][1] = acc[hg][2] = acc[hg][3] = 0.f;
   if constexpr (F8) {
+    // each row word (4 E4M3 bytes) becomes two f16 pairs, paired with Q's pre-converted pairs
+    // of the same bytes: m16n8k16 f16 products (exact, float32 accumulation)
 #pragma unroll
     for (int j = 0; j < DK / 32; ++j) {
 #pragma unroll
-      for (int hg = 0; hg < NHG; ++hg)
-        mma_e4m3_16832(acc[hg], word_of(A0.v, 2 * j), word_of(A1.v, 2 * j), word_of(A0.v, 2 * j + 1),
-                       word_of(A1.v, 2 * j + 1), word_of(f.v[hg], 2 * j), word_of(f.v[hg], 2 * j + 1));
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t r0 = word_of(A0.v, 2 * j + h), r1 = word_of(A1.v, 2 * j + h);
+        const uint32_t a0 = e4m3x2_lo_f16x2(r0), a1 = e4m3x2_lo_f16x2(r1);
+        const uint32_t a2 = e4m3x2_hi_f16x2(r0), a3 = e4m3x2_hi_f16x2(r1);
+#pragma unroll
+        for (int hg = 0; hg < NHG; ++hg)
+          mma_f16_16816(acc[hg], a0, a1, a2, a3, word_of(f.v[hg], 2 * (2 * j + h)),
+                        word_of(f.v[hg], 2 * (2 * j + h) + 1));
+      }
     }
   } else {
 #pragma unroll
