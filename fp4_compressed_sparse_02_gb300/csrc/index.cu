@@ -396,6 +396,149 @@ __global__ void __launch_bounds__(256, 2) k_full_scan(ScanParams p) {
   }
 }
 
+// Full scan of short blocks (at most 64 entries each, e.g. N = 131,072 over 2,048 blocks) with
+// one head group and P = 8: a warp scores the rows of SEG consecutive blocks of one query into
+// shared memory, then lane j < SEG keeps block j's best P by a min/max bubble down a sorted list
+// of values (the selection of k_block_topp).  k_full_scan keeps each block's list warp-wide and
+// offers it every 32-row tile, which costs a 32-wide sort whenever most of a tile beats the
+// list -- always, for a block of two tiles.  Same pool, pool scores and order as k_full_scan.
+// Used for the FP8 form, whose scan is bound by instruction issue (N = 131,072 x 32 queries:
+// 167 -> 129 us a call).  The bf16 form, bound by bytes, keeps k_full_scan: with SEG = 32 or 4
+// it measured 212 and 216 us against 203 (whole segments balance the persistent warps' shares
+// worse than single blocks).
+constexpr int SS_P = 8;                                   // per_block of this path
+constexpr int SS_MAXB = 64;                               // entries per block at most
+__host__ __device__ constexpr int ss_wfloats(int seg) { return seg * SS_MAXB + SS_MAXB; }   // a pad word per 32
+__host__ __device__ constexpr int ss_warp_words(int seg) { return ss_wfloats(seg) + 2 * seg * SS_P; }
+__host__ __device__ constexpr size_t ss_smem(int seg) { return (size_t)8 * ss_warp_words(seg) * sizeof(float); }
+
+__device__ __forceinline__ int ss_pad(int i) { return i + (i >> 5); }
+
+template <int DK, bool F8, int SEG>
+__global__ void __launch_bounds__(256, 2) k_full_scan_short(ScanParams p) {
+  pdl_wait();
+  extern __shared__ float ss_sh[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  float* wsc = ss_sh + warp * ss_warp_words(SEG);
+  int* oid = reinterpret_cast<int*>(wsc + ss_wfloats(SEG));
+  float* osc = wsc + ss_wfloats(SEG) + SEG * SS_P;
+  constexpr int QB = F8 ? 1 : 2;                 // bytes per indexer-Q element
+  constexpr int TPI = F8 ? 2 : 1;                // 32-row tiles per iteration, as in k_full_scan
+  constexpr int ROWB = F8 ? DK : 2 * DK;
+  const int segs = (p.NB + SEG - 1) / SEG;
+  const long long total = (long long)p.B * segs;
+  QFrag<DK, 1, F8> f;
+  int fb = -1;                                   // the query whose fragment f holds
+  // persistent: warp w of CTA x takes units u = 8 x + w, + 8 gridDim.x, ... (u = b segs + seg)
+  for (long long u = (long long)blockIdx.x * 8 + warp; u < total; u += (long long)gridDim.x * 8) {
+    const int b = (int)(u / segs), j0 = (int)(u % segs) * SEG;
+    int n = __ldg(p.n_vis + b);
+    if (n < 0 || n > p.max_n) {
+      if (lane == 0 && j0 == 0) raise_error(&g_err_index, CSA2_DEVERR_N_VIS);
+      n = max(0, min(n, p.max_n));
+    }
+    const int s = __ldg(p.seq_of + b);
+    if (b != fb) {
+      const uint8_t* qb = reinterpret_cast<const uint8_t*>(F8 ? (const void*)p.q8 : (const void*)p.q) +
+                          (long long)b * p.H_i * DK * QB;
+      load_qfrag<DK, 1, F8>(qb, (F8 ? p.w8 : p.w) + (long long)b * p.H_i, p.H_i, f);
+      fb = b;
+    }
+    // lane j < SEG: block j0 + j = [lo, hi) (the other lanes: empty); the warp's rows [e0, e1)
+    const int j = j0 + min(lane, SEG);
+    const long long lo = ((long long)min(j, p.NB) * n) / p.NB;
+    const long long hi = ((long long)min(j0 + min(lane + 1, SEG), p.NB) * n) / p.NB;
+    const long long e0 = __shfl_sync(FULL_MASK, lo, 0);
+    const long long e1 = ((long long)min(j0 + SEG, p.NB) * n) / p.NB;
+    for (long long base = e0; base < e1; base += 32 * TPI) {
+      if (F8 && lane == 0 && base + 32 * TPI < e1) {       // the next iteration's rows into L2
+        const long long nb = base + 32 * TPI;
+        const long long nrow = entry_row(p.cache, s, nb, &g_err_index);
+        if (nrow >= 0) {
+          long long rows = kPage - (nb & (kPage - 1));
+          rows = rows < 32 * TPI ? rows : 32 * TPI;
+          rows = rows < e1 - nb ? rows : e1 - nb;
+          const uint8_t* src = F8 ? p.cache.idx_k8 : reinterpret_cast<const uint8_t*>(p.cache.idx_k);
+          prefetch_l2_bulk(src + nrow * ROWB, (uint32_t)(rows * ROWB));
+        }
+      }
+      KRow<DK, F8> A[TPI][4];
+      int mine[TPI];
+      float msc[TPI];
+#pragma unroll
+      for (int tt = 0; tt < TPI; ++tt) {
+        const long long rr = base + 32 * tt + 8 * c + g;
+        mine[tt] = (rr < e1) ? (int)entry_row(p.cache, s, rr, &g_err_index) : -1;
+        msc[tt] = (F8 && mine[tt] >= 0) ? __ldg(p.cache.idx_k8_scale + mine[tt]) : 0.f;
+      }
+#pragma unroll
+      for (int tt = 0; tt < TPI; ++tt)
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int src = (lane & ~3) | t;
+          load_row<DK, F8>(p.cache, __shfl_sync(FULL_MASK, mine[tt], src), A[tt][t],
+                           F8 ? __shfl_sync(FULL_MASK, msc[tt], src) : -1.f);
+        }
+#pragma unroll
+      for (int tt = 0; tt < TPI; ++tt) {
+        float sc[4];
+        tile_scores<DK, 1, F8>(f, A[tt][0], A[tt][1], p.relu != 0, sc[0], sc[1]);
+        tile_scores<DK, 1, F8>(f, A[tt][2], A[tt][3], p.relu != 0, sc[2], sc[3]);
+        if (c == 0) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const long long r = base + 32 * tt + 8 * t + g;
+            if (r < e1) wsc[ss_pad((int)(r - e0))] = sc[t];
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // lane j keeps its block's best P: every entry above the P-th best value tv, then the first
+    // entries equal to it in ascending order (all of a block of fewer than P entries)
+    const int cnt = (lane < SEG && j < p.NB) ? (int)(hi - lo) : 0;
+    const int b0 = (int)(lo - e0);
+    float kv[SS_P];
+#pragma unroll
+    for (int i = 0; i < SS_P; ++i) kv[i] = -INFINITY;
+    for (int e = 0; e < cnt; ++e) {
+      float v = wsc[ss_pad(b0 + e)];
+#pragma unroll
+      for (int i = 0; i < SS_P; ++i) {
+        const float t = fmaxf(v, kv[i]);
+        v = fminf(v, kv[i]);
+        kv[i] = t;
+      }
+    }
+    const float tv = (cnt >= SS_P) ? kv[SS_P - 1] : -INFINITY;
+    int quota = SS_P;
+#pragma unroll
+    for (int i = 0; i < SS_P; ++i) quota -= (kv[i] > tv) ? 1 : 0;
+    // the SEG blocks' kept entries are one contiguous run of the pool: staged, then stored
+    const long long off = ((long long)n >= (long long)SS_P * p.NB) ? (long long)SS_P * j : lo;
+    const long long off0 = __shfl_sync(FULL_MASK, off, 0);
+    const int loc = (int)(off - off0);
+    int kept = 0;
+    for (int e = 0; e < cnt; ++e) {
+      const float v = wsc[ss_pad(b0 + e)];
+      if (v > tv || (v == tv && quota-- > 0)) {
+        oid[loc + kept] = (int)(lo + e);
+        osc[loc + kept] = v;
+        ++kept;
+      }
+    }
+    const int tot = __reduce_max_sync(FULL_MASK, cnt > 0 ? loc + kept : 0);
+    __syncwarp();
+    const long long o = (long long)b * p.NB * SS_P + off0;
+    for (int i = lane; i < tot; i += 32) {
+      p.pool[o + i] = oid[i];
+      p.pool_score[o + i] = osc[i];
+    }
+    __syncwarp();                                 // before the next unit reuses the buffers
+  }
+}
+
 // Full scan of G queries of one sequence at once (G consecutive queries sharing seq_of, e.g.
 // the positions of a speculative-decoding verification step): each indexer-K row is read
 // once and scored against every query (H_i <= 8).  Query q keeps its own blocks of its own
@@ -1074,6 +1217,35 @@ static void launch_scan_group(const ScanParams& sp, int group, long long units, 
   }
 }
 
+// The short-block scan, whose score buffers are dynamic shared memory.
+static cudaError_t launch_scan_short(const ScanParams& sp, cudaStream_t st) {
+  constexpr int SEG = 32;
+  auto kernel = k_full_scan_short<128, true, SEG>;
+  constexpr size_t smem = ss_smem(SEG);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const long long units = ((long long)sp.B * ((sp.NB + SEG - 1) / SEG) + 7) / 8;
+  const dim3 grid((unsigned)std::min<long long>(units, (long long)per_sm * (sms > 0 ? sms : 1)));
+  launch_k_late(kernel, grid, 256, smem, st, sp);   // persistent: see launch_persistent
+  return cudaGetLastError();
+}
+
+// the short-block scan serves the FP8 form with one head group, P = 8, d_ik = 128 and blocks
+// of at most 64 entries
+static bool scan_short_chosen(const csa2_index_full_args& a, int nhg, int group) {
+  return a.cache.idx_k_dtype == CSA2_FP8E4M3 && nhg == 1 && group == 1 && a.per_block == SS_P &&
+         a.cache.d_ik == 128 && ((long long)a.max_n + a.num_blocks - 1) / a.num_blocks <= SS_MAXB;
+}
+
 template <int DK, bool F8>
 static void launch_scan_dk(const ScanParams& sp, int nhg, long long units, cudaStream_t st) {
   switch (nhg) {
@@ -1157,6 +1329,9 @@ cudaError_t launch_index_full(const csa2_index_full_args& a, void* ws, cudaStrea
     if (group > 1 && group <= 8 && a.H_i <= 8) {
       if (a.cache.d_ik == 128) launch_scan_group<128, true>(sp, group, units_g, st);
       else launch_scan_group<64, true>(sp, group, units_g, st);
+    } else if (scan_short_chosen(a, nhg, group)) {
+      cudaError_t e = launch_scan_short(sp, st);
+      if (e != cudaSuccess) return e;
     } else if (a.cache.d_ik == 128) {
       launch_scan_dk<128, true>(sp, nhg, units, st);
     } else {
