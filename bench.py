@@ -62,6 +62,7 @@ PROFILES = {("k_attn_tc", "decode128k"): ("k_attn_tc_decode128k.md", "attn.cu"),
             ("k_attn_tc", "decode1m"): ("k_attn_tc_decode1m.md", "attn.cu"),
             ("k_full_scan", "decode1m"): ("k_full_scan_decode1m.md", "index.cu"),
             ("k_full_scan", "decode1m_ik8"): ("k_full_scan_decode1m_ik8.md", "index.cu"),
+            ("k_full_scan_short", "decode128k_ik8"): ("k_full_scan_short_decode128k_ik8.md", "index.cu"),
             ("k_full_scan", "decode128k"): ("k_full_scan_decode128k.md", "index.cu"),
             ("k_select_cl_reindex", "decode128k"): ("k_select_cl_reindex_decode128k.md", "index.cu"),
             ("k_proj_tc", "prefill_compress"): ("k_proj_tc_prefill_compress.md", "proj_tc.cu"),
@@ -699,8 +700,12 @@ def main():
         ik8 = bool(info.get("ik8"))
         tc_full = (not ik8 and info["d_ik"] == 128 and info["H_i"] in (8, 16, 32) and
                    info["H_i"] * info.get("G", 1) >= 16)
+        # the FP8 form scans blocks of at most 64 entries (one head group, P = 8) with k_full_scan_short
+        short_scan = (ik8 and info["d_ik"] == 128 and info["H_i"] <= 8 and info.get("G", 1) == 1 and
+                      info["P"] == 8 and -(-info["N"] // info["NB"]) <= 64)
+        scan_kernel = "k_full_scan_short" if short_scan else "k_full_scan"
         full_kernels = ("k_score_tc + k_block_topp + k_select_cl" if tc_full else
-                        "k_full_scan + k_select_cl" + (" (+ k_quant_q8, FP8 indexer)" if ik8 else ""))
+                        scan_kernel + " + k_select_cl" + (" (+ k_quant_q8, FP8 indexer)" if ik8 else ""))
         # kernels per step: compressor append 2 (projection; quantisation + indexer K), Full
         # indexer 2 (scan, select) or 3 (score, block top-P, select; or FP8: Q quantisation,
         # scan, select), Reindex 1 (FP8: 2), attention 1 per layer
