@@ -259,18 +259,19 @@ def _exact_score_problem(r, n, kinds):
     return cache, K, q, w
 
 
-def test_select_resolves_every_key_bit():
+@pytest.mark.parametrize("B", [3, 40])
+def test_select_resolves_every_key_bit(B):
     # scores exact on both sides, so the pool and the Top-k must equal the oracle's bit for
     # bit: the radix select must resolve keys that agree on their top 22 bits (all three of
     # its passes), stop early when a digit's keys are all taken, and break exact ties by
-    # position, in the Full scan's select and in Reindex
-    r = np.random.default_rng(25)
+    # position, in the Full scan's select and in Reindex (at 40 queries Reindex runs its
+    # 128-thread CTAs: 40 clusters of 8 do not fit at two 256-thread CTAs an SM)
+    r = np.random.default_rng(25 + B)
     NB, P, k, n = 2048, 8, 512, 40000
-    kinds = ["low", "spread", "flat"]
+    kinds = [("low", "spread", "flat")[i % 3] for i in range(B)]
     cache, K, q, w = _exact_score_problem(r, n, kinds)
-    B = len(kinds)
     seq_of = np.arange(B, dtype=np.int32)
-    n_vis = np.array([n, n - 777, n], dtype=np.int32)
+    n_vis = np.array([n - (777 if i % 3 == 1 else 0) for i in range(B)], dtype=np.int32)
     pool, plen, topk, tlen = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
     for b in range(B):
         Kb = formats.bf16_value(K[b][:n_vis[b]])
