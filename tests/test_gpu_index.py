@@ -259,34 +259,35 @@ def _exact_score_problem(r, n, kinds):
     return cache, K, q, w
 
 
-@pytest.mark.parametrize("B", [3, 40])
+@pytest.mark.parametrize("B", [3, 40, 300])
 def test_select_resolves_every_key_bit(B):
     # scores exact on both sides, so the pool and the Top-k must equal the oracle's bit for
     # bit: the radix select must resolve keys that agree on their top 22 bits (all three of
     # its passes), stop early when a digit's keys are all taken, and break exact ties by
-    # position, in the Full scan's select and in Reindex (at 40 queries Reindex runs its
-    # 128-thread CTAs: 40 clusters of 8 do not fit at two 256-thread CTAs an SM)
+    # position, in the Full call's select and in Reindex.  At 40 queries Reindex runs its
+    # 128-thread CTAs (40 clusters of 8 do not fit at two 256-thread CTAs an SM); from 256
+    # queries on the Full call's Top-k is one CTA per query.
     r = np.random.default_rng(25 + B)
     NB, P, k, n = 2048, 8, 512, 40000
-    kinds = [("low", "spread", "flat")[i % 3] for i in range(B)]
-    cache, K, q, w = _exact_score_problem(r, n, kinds)
-    seq_of = np.arange(B, dtype=np.int32)
-    n_vis = np.array([n - (777 if i % 3 == 1 else 0) for i in range(B)], dtype=np.int32)
+    kinds = ["low", "spread", "flat"]
+    cache, K, q3, w3 = _exact_score_problem(r, n, kinds)
+    seq_of = (np.arange(B) % 3).astype(np.int32)                 # query i reads sequence i % 3
+    n_vis = np.array([n - 37 * (i // 3) - (777 if i % 3 == 1 else 0) for i in range(B)], dtype=np.int32)
+    q, w = q3[seq_of], w3[seq_of]
     pool, plen, topk, tlen = _run_full(cache, q, w, seq_of, n_vis, NB, P, k)
     for b in range(B):
-        Kb = formats.bf16_value(K[b][:n_vis[b]])
+        Kb = formats.bf16_value(K[seq_of[b]][:n_vis[b]])
         rpool, rtopk, _ = indexer.full(formats.bf16_value(q[b]), w[b].astype(np.float64), Kb, NB, P, k)
-        np.testing.assert_array_equal(pool[b, :plen[b]], rpool, err_msg=kinds[b])
-        np.testing.assert_array_equal(topk[b, :tlen[b]], rtopk, err_msg=kinds[b])
+        np.testing.assert_array_equal(pool[b, :plen[b]], rpool, err_msg=f"{b} {kinds[seq_of[b]]}")
+        np.testing.assert_array_equal(topk[b, :tlen[b]], rtopk, err_msg=f"{b} {kinds[seq_of[b]]}")
     # Reindex over the same pools
-    q2 = q.copy()
-    topk2, tlen2 = csa2.index_reindex(cache, bf16_dev(q2), to_dev(w), to_dev(seq_of), to_dev(pool), to_dev(plen), k)
+    topk2, tlen2 = csa2.index_reindex(cache, bf16_dev(q), to_dev(w), to_dev(seq_of), to_dev(pool), to_dev(plen), k)
     assert csa2.device_error() == 0
     topk2, tlen2 = topk2.cpu().numpy(), tlen2.cpu().numpy()
     for b in range(B):
-        Kb = formats.bf16_value(K[b])
-        rt, _ = indexer.reindex(formats.bf16_value(q2[b]), w[b].astype(np.float64), Kb, pool[b, :plen[b]], k)
-        np.testing.assert_array_equal(topk2[b, :tlen2[b]], rt, err_msg=kinds[b])
+        Kb = formats.bf16_value(K[seq_of[b]])
+        rt, _ = indexer.reindex(formats.bf16_value(q[b]), w[b].astype(np.float64), Kb, pool[b, :plen[b]], k)
+        np.testing.assert_array_equal(topk2[b, :tlen2[b]], rt, err_msg=f"{b} {kinds[seq_of[b]]}")
 
 
 def test_reindex_matches_oracle():
