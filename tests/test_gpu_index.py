@@ -290,9 +290,11 @@ def test_select_resolves_every_key_bit(B):
         np.testing.assert_array_equal(topk2[b, :tlen2[b]], rt, err_msg=f"{b} {kinds[seq_of[b]]}")
 
 
-def test_reindex_matches_oracle():
-    r = np.random.default_rng(30)
-    NB, P, k, d_ik, H_i = 2048, 8, 512, 128, 8
+@pytest.mark.parametrize("H_i", [8, 12, 16, 32])
+def test_reindex_matches_oracle(H_i):
+    # 8 heads: mma.sync scoring; 12..32 heads: tcgen05 scoring of the gathered rows
+    r = np.random.default_rng(30 + H_i)
+    NB, P, k, d_ik = 2048, 8, 512, 128
     n_vis = np.array([40000, 16384, 9000, 70000], dtype=np.int32)
     B = len(n_vis)
     cache, K, q_full, w_full = _setup(r, 4, int(n_vis.max()), d_ik, H_i, B)
