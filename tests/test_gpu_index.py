@@ -292,7 +292,7 @@ def test_select_resolves_every_key_bit(B):
 
 @pytest.mark.parametrize("H_i", [8, 12, 16, 32])
 def test_reindex_matches_oracle(H_i):
-    # 8 heads: mma.sync scoring; 12..32 heads: tcgen05 scoring of the gathered rows
+    # one head group kept in registers (8), two (12, 16), or four streamed from L1 (32)
     r = np.random.default_rng(30 + H_i)
     NB, P, k, d_ik = 2048, 8, 512, 128
     n_vis = np.array([40000, 16384, 9000, 70000], dtype=np.int32)
