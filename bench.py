@@ -104,7 +104,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "100", "-i", str(self.dev)], stdout=self.f,
+                                          "-lms", "25", "-i", str(self.dev)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
