@@ -1,6 +1,6 @@
 """Parity at the benchmark's full sizes and in its launch configuration: one whole decode
 step (append + the 20-layer schedule) of the N=131,072 / B=32 and N=1,048,576 / B=64
-workloads (bf16 and FP8 indexer-K forms), and of the mixed-context sweep (contexts of
+workloads (bf16 and FP8 indexer-K forms; the FP8 form's short-block scan at N=131,072), and of the mixed-context sweep (contexts of
 4K..1M entries, batch 1..256), runs on the GPU.  Then, for every query of the step: its
 appended entry is recomputed by the oracle, and the attention of every layer is recomputed
 over the index set the GPU chose (the attention rule is stated given identical index sets),
@@ -63,13 +63,20 @@ def _check_append(step, info, b):
     bad, tol = fp4_mismatch_is_tolerated(ref["y"], codes, scales, ref["codes"], ref["scales"])
     assert bad == tol
     if info.get("ik8"):
-        # the GPU's bf16 indexer K is within a bf16 ulp of the oracle's, so its E4M3 row is
-        # within one E4M3 step of the oracle's quantisation of its own row
+        # indexer K is projected from the entry's FP4 form, so the oracle projects the GPU's own
+        # entry (a tolerated FP4 code difference above changes the whole projection).  The GPU's
+        # bf16 indexer K x_g is then within a bf16 ulp of the oracle's x_w, and each side's E4M3
+        # rounding (a normal value) moves it by at most half a step, |x| / 16: so
+        # |got - want| <= (|x_g| + |x_w|) / 16 + |x_g - x_w|, with |x| <= (17/16) |rounded x|;
+        # values in the E4M3 subnormal range are within a subnormal step (2^-9 s) of either
         k8 = step.cache.idx_k8[pg, sl].cpu().numpy()
         ks = step.cache.idx_k8_scale[pg, sl].cpu().numpy()
-        rb, rs = compress.index_k_fp8(ref["idx_k"])
+        Wik = formats.bf16_value(_bits(step.append["W_ik"]))
+        rb, rs = compress.index_k_fp8(compress.project_index_k(codes, scales, Wik))
         got, want = formats.fp8_rows_dequantize(k8, ks), formats.fp8_rows_dequantize(rb, rs)
-        assert (np.abs(got - want) <= 2.0 ** -3 * np.abs(want) + 2.0 ** -8 * rs[:, None] + 1e-30).all()
+        mag = np.maximum(np.abs(got), np.abs(want))
+        tol = (17 / 16) * (np.abs(got) + np.abs(want)) / 16 + 2.0 ** -7 * mag + 2.0 ** -8 * rs[:, None] + 1e-30
+        assert (np.abs(got - want) <= tol).all()
 
 
 def _check_attention_of_gpu_sets(step, info, b):
@@ -131,7 +138,7 @@ def _check_query(step, info, b):
 
 
 @pytest.mark.parametrize("cfg,samples", [(synth.DEC128K, [0, 17, 31]), (synth.DEC1M, [0, 21, 42, 63]),
-                                         (synth.DEC1M_IK8, [5, 50])])
+                                         (synth.DEC128K_IK8, [3, 29]), (synth.DEC1M_IK8, [5, 50])])
 def test_decode_step_full_size(cfg, samples):
     step, info = workload.build_decode(cfg, seed=7)
     step.run()
